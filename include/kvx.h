@@ -1,0 +1,269 @@
+/*
+ * kvx.h -- C ABI of libkvx, the GB300 (sm_103a) paged KV-cache block-transfer
+ * path.
+ *
+ * The method is the one of pegaflow PR #350, "perf(transfer)!: run-encode
+ * QueryBlocksForTransfer addresses and coalesce RDMA READs":
+ *
+ *   kvx_encode_runs  the holder's per-lane run encoding of the block prefix's
+ *                    segment addresses (Holder paragraph; Wire format
+ *                    paragraph: runs_per_lane / run_base / run_stride /
+ *                    run_count parallel arrays)
+ *   kvx_plan_groups  the requester's plan_transfer, steps 1-4 (validate;
+ *                    decode, bucket per NUMA node, sort by remote base; dense
+ *                    grouping; slab carve and one read per dense group or per
+ *                    block) and the READ splitting paragraph (32 MiB pieces)
+ *   kvx_rebuild      step 5: local(b) = group_local + (remote(b) -
+ *                    group_remote), every pointer bounds-checked
+ *   kvx_pack         the data movement of the planned reads: scattered holder
+ *                    segments -> dense staging slab
+ *   kvx_unpack       the inverse copy: slab -> a pool with the holder's layout
+ *                    (not on the page; it closes the round trip)
+ *
+ * Conventions for every call:
+ *   - Array arguments are DEVICE pointers, allocated and owned by the caller.
+ *     The library allocates nothing; scratch memory is the caller's `ws`
+ *     buffer of at least the size the matching *_workspace_size() returns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL is the legacy default stream).  They return after enqueueing.
+ *   - The return value reports host-detectable problems only: KVX_EINVAL
+ *     (null pointer, bad size, too-small workspace), KVX_ECAPACITY (an output
+ *     capacity below the bound the call needs), KVX_ECUDA (a launch failed).
+ *     Nothing is enqueued when the return value is not KVX_OK.
+ *   - Data-dependent problems are OR-ed as KVX_S_* bits into the caller's
+ *     device word `status` (never cleared by the library; the caller zeroes it
+ *     and reads it after synchronising).  A nonzero status means the outputs
+ *     of that call are undefined, except as stated per call.  No call traps,
+ *     asserts or waits on another thread block: bad input cannot hang or
+ *     fault the GPU; every global access is checked against the capacities
+ *     passed in.
+ *   - Outputs must not alias inputs.
+ *
+ * Layouts: the address table and the rebuilt local pointers are block-major,
+ * element [b][l] at b*L + l.  Lane l = 2*slot + kv (kv 0 = K, 1 = V): one
+ * slot's K or V segment followed across the block prefix.  Addresses are byte
+ * offsets into the holder pool; local pointers are byte offsets into the slab.
+ */
+#ifndef KVX_H
+#define KVX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvx_status {
+    KVX_OK = 0,
+    KVX_EINVAL = 1,
+    KVX_ECAPACITY = 3,
+    KVX_ECUDA = 4
+} kvx_status;
+
+/* Device status bits: the plan's validation classes follow the page's Trust
+ * boundary list (wrong lane count, bad coverage, zero-count runs, zero-size
+ * slots, span overflow) and its step 1 (parallel arrays in sync). */
+#define KVX_S_LANES      1u    /* table lane count != template lane count */
+#define KVX_S_ARRAYS     2u    /* per-lane run counts do not add up to the run arrays' length */
+#define KVX_S_COVERAGE   4u    /* a lane's run counts do not add up to the block count */
+#define KVX_S_ZERO_COUNT 8u    /* a run covers zero blocks */
+#define KVX_S_ZERO_LEN   16u   /* a template lane has segment length 0 */
+#define KVX_S_SPAN       32u   /* a run's remote span wraps or leaves the holder pool */
+#define KVX_S_STRIDE1    64u   /* a one-block run with a nonzero stride */
+#define KVX_S_BOUNDS     128u  /* a pointer or copy outside its slab/pool/group range */
+#define KVX_S_DESC       256u  /* descriptors do not tile the slab in order */
+#define KVX_S_CAPACITY   512u  /* a plan output exceeds its capacity, or the slab 2^63 bytes */
+
+/* READ splitting: planned descriptors are split into pieces of at most
+ * MAX_RDMA_READ_BYTES = 32 MiB. */
+#define KVX_MAX_READ_BYTES ((uint64_t)32 * 1024 * 1024)
+
+/* One dense group (Requester step 3): runs that share NUMA node, block range
+ * and stride and whose bases are adjacent, while their summed segment length
+ * (chunk) still fits the stride.  48 bytes. */
+typedef struct kvx_group {
+    uint64_t base;    /* remote address of the group's bytes in its first block */
+    int64_t  stride;  /* remote distance between consecutive blocks */
+    uint64_t chunk;   /* bytes per block = sum of member segment lengths */
+    uint64_t local;   /* slab offset of the group's first byte (the carve) */
+    uint32_t block;   /* first block */
+    uint32_t count;   /* number of blocks */
+    uint32_t node;    /* NUMA node of every member lane */
+    uint32_t dense;   /* 1 when count == 1 or chunk == stride: one remote span */
+} kvx_group;
+
+/* One planned read: slab[local, local+len) <-> pool[remote, remote+len).
+ * 32 bytes.  Descriptors come in group, block, piece order; their local
+ * ranges tile [0, slab bytes) back to back. */
+typedef struct kvx_desc {
+    uint64_t remote;
+    uint64_t local;
+    uint64_t len;      /* 1 .. KVX_MAX_READ_BYTES */
+    uint32_t group;
+    uint32_t reserved; /* 0 */
+} kvx_desc;
+
+/* ------------------------------------------------------------ run encoding */
+
+/* Greedy bound: every run but a lane's last covers >= 2 blocks, so a lane
+ * has at most ceil(B/2) runs.  Returns L * ceil(B/2). */
+uint64_t kvx_run_capacity(uint32_t B, uint32_t L);
+
+size_t kvx_encode_workspace_size(uint32_t B, uint32_t L);
+
+/*
+ * Run-encode the per-segment address table (Holder paragraph, Problem
+ * section: per lane the bump-allocated addresses form addr(i) = base +
+ * i*stride).  Per lane, greedily: a run starts at block s, its stride is the
+ * wrapping difference addr(s+1) - addr(s) (0 when s is the lane's last
+ * block), and it grows while the next difference equals the stride.
+ *
+ *   addr           [B][L] uint64, holder-pool byte offsets (block-major).
+ *   runs_per_lane  [L] out: runs of each lane.
+ *   run_base, run_stride, run_count
+ *                  [run_capacity] out, lane-major, blocks ascending: first
+ *                  address, stride (int64 bit pattern of the uint64
+ *                  difference), blocks covered.
+ *   run_capacity   must be >= kvx_run_capacity(B, L) (else KVX_ECAPACITY).
+ *   num_runs       [1] out: total runs R (device).
+ *   ws, ws_bytes   scratch, >= kvx_encode_workspace_size(B, L).
+ * Encoding cannot fail on data; it writes no status.
+ */
+kvx_status kvx_encode_runs(const uint64_t *addr, uint32_t B, uint32_t L,
+                           uint32_t *runs_per_lane, uint64_t *run_base,
+                           int64_t *run_stride, uint32_t *run_count,
+                           uint64_t run_capacity, uint64_t *num_runs,
+                           void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------ plan */
+
+/* Bound on descriptors for a valid table: at most one span per segment
+ * plus one extra piece per 32 MiB of slab.  seg_bytes_sum = sum of the
+ * template's segment lengths. */
+uint64_t kvx_desc_capacity(uint32_t B, uint32_t L, uint64_t seg_bytes_sum);
+
+size_t kvx_plan_workspace_size(uint32_t L, uint64_t run_capacity, uint64_t pool_bytes);
+
+/*
+ * Plan the transfer (Requester steps 1-4 and READ splitting).
+ *
+ * Step 1, validate: table_lanes == template_lanes (else KVX_S_LANES, nothing
+ * else checked); per-lane run counts add up to *num_runs, which must be <=
+ * run_capacity (KVX_S_ARRAYS); every template segment length > 0
+ * (KVX_S_ZERO_LEN); every lane's counts add up to B (KVX_S_COVERAGE); every
+ * count > 0 (KVX_S_ZERO_COUNT); a one-block run has stride 0
+ * (KVX_S_STRIDE1); base + i*stride for i in [0, count) plus the segment
+ * length stays inside [0, pool_bytes) with exact arithmetic (KVX_S_SPAN).
+ * All failing classes are reported together.  On any failure the counts are
+ * 0 and nothing else is planned.
+ * Step 2: decode each run (lane, first block, node = numa[lane], length =
+ * seg_len[lane]) and sort by (node, base, lane, first block).
+ * Step 3: walk the sorted runs; a run joins the open group when it has the
+ * same node, first block, count and stride, its base equals group base +
+ * chunk, and the grown chunk still fits the stride (count == 1, or stride > 0
+ * and chunk <= stride); otherwise it opens a new group.
+ * Step 4: carve the slab: groups back to back in order (so each NUMA node's
+ * groups form one contiguous partition).  A dense group is one read of
+ * count*chunk bytes; a non-dense group is one read of chunk bytes per block
+ * into a dense local mirror.  Every read is split into 32 MiB pieces.
+ *
+ * Inputs: the run table as kvx_encode_runs writes it (num_runs on the
+ * device); B; the slot template seg_len[template_lanes], numa[template_lanes];
+ * the holder pool size.
+ * Outputs: groups[group_capacity], descs[desc_capacity];
+ * lane_first[table_lanes + 1] (index of each lane's first run, exclusive
+ * prefix of runs_per_lane); per run run_block (decoded first block),
+ * run_group, run_off (run base - group base);
+ * counts[3] = {groups, descriptors, slab bytes} (device).  Capacities below
+ * run_capacity groups or kvx_desc_capacity() descriptors may end in
+ * KVX_S_CAPACITY on the device.
+ */
+kvx_status kvx_plan_groups(const uint32_t *runs_per_lane, uint32_t table_lanes,
+                           const uint64_t *run_base, const int64_t *run_stride,
+                           const uint32_t *run_count, const uint64_t *num_runs,
+                           uint64_t run_capacity, uint32_t B,
+                           const uint32_t *seg_len, const uint32_t *numa,
+                           uint32_t template_lanes, uint64_t pool_bytes,
+                           kvx_group *groups, uint64_t group_capacity,
+                           kvx_desc *descs, uint64_t desc_capacity,
+                           uint32_t *lane_first, uint32_t *run_block,
+                           uint32_t *run_group, uint64_t *run_off,
+                           uint64_t *counts, uint32_t *status,
+                           void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------- rebuild */
+
+/*
+ * Rebuild every segment's slab pointer arithmetically (Requester step 5):
+ * local(b, l) = G.local + (b - G.block) * G.chunk + run_off[r], where r is
+ * the run of lane l covering block b and G its group.  For a dense group this
+ * is the page's group_local + (remote(b) - group_remote); for a non-dense
+ * group it addresses the dense local mirror.  Each pointer is checked: the
+ * group index is below counts[0], b lies in the group's block range, the
+ * segment [local, local + seg_len[l]) lies inside its block's chunk of the
+ * group carve, and the carve ends within slab_bytes.  A failing entry is set
+ * to UINT64_MAX and KVX_S_BOUNDS is raised.
+ *
+ * Inputs: lane_first [L + 1], run_block, run_group, run_off [run_capacity]
+ * and groups as kvx_plan_groups wrote them; counts (device, [0] = groups);
+ * seg_len [L]; slab_bytes (the slab buffer's size).
+ * Output: local [B][L] uint64 (block-major).
+ */
+kvx_status kvx_rebuild(const uint32_t *lane_first, const uint32_t *run_block,
+                       const uint32_t *run_group, const uint64_t *run_off,
+                       uint64_t run_capacity, const kvx_group *groups,
+                       uint64_t group_capacity, const uint64_t *counts,
+                       uint32_t B, uint32_t L, const uint32_t *seg_len,
+                       uint64_t slab_bytes, uint64_t *local,
+                       uint32_t *status, void *stream);
+
+/* ------------------------------------------------------------ pack/unpack */
+
+size_t kvx_copy_workspace_size(uint64_t slab_bytes);
+
+/*
+ * Pack: slab[d.local, +d.len) = pool[d.remote, +d.len) for every planned
+ * descriptor (the bytes of the page's coalesced reads).
+ *
+ *   pool, pool_bytes       holder pool (read).
+ *   descs, num_descs       descriptors as kvx_plan_groups wrote them;
+ *                          num_descs is a device pointer (counts + 1 of the
+ *                          plan); at most desc_capacity are read.
+ *   slab, slab_bytes       destination slab.
+ * The descriptors must tile the slab in order (each local == previous local
+ * + previous len, first local 0, every len > 0); otherwise KVX_S_DESC is
+ * raised and nothing is copied.  A descriptor whose range leaves the pool or
+ * the slab is skipped with KVX_S_BOUNDS; the others are copied.
+ */
+kvx_status kvx_pack(const uint8_t *pool, uint64_t pool_bytes,
+                    const kvx_desc *descs, const uint64_t *num_descs,
+                    uint64_t desc_capacity, uint8_t *slab, uint64_t slab_bytes,
+                    uint32_t *status, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Unpack, the inverse copy: dst_pool[d.remote, +d.len) = slab[d.local,
+ * +d.len).  Same descriptor rules as kvx_pack.  Destination ranges of
+ * different descriptors must not overlap (a valid plan of a table whose
+ * segments do not overlap guarantees it); overlapping ranges give undefined
+ * bytes in the overlap.  Pool bytes outside the descriptors are untouched.
+ */
+kvx_status kvx_unpack(const uint8_t *slab, uint64_t slab_bytes,
+                      const kvx_desc *descs, const uint64_t *num_descs,
+                      uint64_t desc_capacity, uint8_t *dst_pool,
+                      uint64_t pool_bytes, uint32_t *status,
+                      void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------- utility */
+
+/* Number of kernels this library has launched in this process. */
+uint64_t kvx_launch_count(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+uint32_t kvx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVX_H */

@@ -1,0 +1,182 @@
+// Internal helpers shared by the libkvx kernels (sm_103a).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kvx.h"
+
+namespace kvx {
+
+constexpr uint32_t kNone = 0xFFFFFFFFu;
+
+// ------------------------------------------------------------------ host side
+
+// Counts every kernel this library launches (reported by kvx_launch_count).
+void note_launch(uint32_t n = 1);
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count();
+
+inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+
+// Carves consecutive 256-byte aligned sub-buffers out of a workspace.  With a
+// null base it only measures.
+struct Carver {
+    char *base;
+    size_t off = 0;
+    explicit Carver(void *b) : base(static_cast<char *>(b)) {}
+    template <class T>
+    T *take(size_t n) {
+        off = align_up(off, 256);
+        T *p = base ? reinterpret_cast<T *>(base + off) : nullptr;
+        off += sizeof(T) * (n ? n : 1);
+        return p;
+    }
+};
+
+#define KVX_LAUNCHED()                                  \
+    do {                                                \
+        ::kvx::note_launch();                           \
+        if (cudaPeekAtLastError() != cudaSuccess) {     \
+            (void)cudaGetLastError();                   \
+            return KVX_ECUDA;                           \
+        }                                               \
+    } while (0)
+
+// ---------------------------------------------------------------- device side
+
+__device__ __forceinline__ void raise(uint32_t *st, uint32_t bits) {
+    if (bits) atomicOr(st, bits);
+}
+
+// Last-block ticket: every block of the grid calls this after its global
+// writes; it returns true in exactly one block, the last to arrive, which
+// then sees every other block's writes.  Nothing waits: blocks that are not
+// last simply go on (and exit).  The counter is left at zero.
+__device__ __forceinline__ bool last_block(uint32_t *ticket) {
+    __shared__ bool s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t total = gridDim.x * gridDim.y * gridDim.z;
+        const uint32_t t = atomicAdd(ticket, 1u);
+        s_last = (t == total - 1);
+        if (s_last) atomicExch(ticket, 0u);
+    }
+    __syncthreads();
+    if (s_last) __threadfence();
+    return s_last;
+}
+
+// Warp-level inclusive scans.
+template <class T>
+__device__ __forceinline__ T warp_incl_sum(T v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        T o = __shfl_up_sync(0xFFFFFFFFu, v, d);
+        if (lane >= d) v += o;
+    }
+    return v;
+}
+
+template <class T>
+__device__ __forceinline__ T warp_incl_max(T v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        T o = __shfl_up_sync(0xFFFFFFFFu, v, d);
+        if (lane >= d) v = o > v ? o : v;
+    }
+    return v;
+}
+
+// Block-wide exclusive sum over one value per thread; returns the exclusive
+// prefix and writes the block total.  `sh` holds >= 32 elements.
+template <class T>
+__device__ __forceinline__ T block_excl_sum(T v, T *sh, T *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = (blockDim.x + 31) >> 5;
+    T incl = warp_incl_sum(v);
+    __syncthreads();
+    if (lane == 31) sh[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        T w = lane < nwarps ? sh[lane] : T(0);
+        T wi = warp_incl_sum(w);
+        sh[lane] = wi - w;
+        if (lane == 31) sh[32] = wi;
+    }
+    __syncthreads();
+    T res = sh[warp] + incl - v;
+    *total = sh[32];
+    __syncthreads();
+    return res;
+}
+
+// Block-wide inclusive max (values are signed; identity = INT64_MIN).
+__device__ __forceinline__ int64_t block_incl_max(int64_t v, int64_t *sh) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = (blockDim.x + 31) >> 5;
+    int64_t incl = warp_incl_max(v);
+    __syncthreads();
+    if (lane == 31) sh[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int64_t w = lane < nwarps ? sh[lane] : INT64_MIN;
+        int64_t wi = warp_incl_max(w);
+        sh[lane] = wi;
+    }
+    __syncthreads();
+    int64_t prev = warp > 0 ? sh[warp - 1] : INT64_MIN;
+    __syncthreads();
+    return incl > prev ? incl : prev;
+}
+
+// Exclusive prefix sum, in place, of n uint64 values by one whole block
+// (used by last blocks on per-tile aggregates).  Returns the total.
+__device__ inline uint64_t block_scan_inplace_u64(uint64_t *a, uint64_t n) {
+    __shared__ uint64_t sh[33];
+    __shared__ uint64_t carry;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    for (uint64_t base = 0; base < n; base += blockDim.x) {
+        const uint64_t i = base + threadIdx.x;
+        uint64_t v = i < n ? __ldcg(a + i) : 0;
+        uint64_t tot;
+        uint64_t ex = block_excl_sum<uint64_t>(v, sh, &tot);
+        if (i < n) a[i] = carry + ex;
+        __syncthreads();
+        if (threadIdx.x == 0) carry += tot;
+        __syncthreads();
+    }
+    return carry;
+}
+
+// Exclusive prefix sum, in place, of n uint32 values where every thread owns
+// a contiguous span (large n, e.g. a digit histogram matrix).
+__device__ inline uint32_t block_scan_inplace_span_u32(uint32_t *a, uint64_t n) {
+    __shared__ uint64_t sh[33];
+    const uint64_t per = (n + blockDim.x - 1) / blockDim.x;
+    const uint64_t lo = per * threadIdx.x;
+    const uint64_t hi = lo + per < n ? lo + per : n;
+    uint64_t s = 0;
+    for (uint64_t i = lo; i < hi; i++) s += __ldcg(a + i);
+    uint64_t tot;
+    uint64_t ex = block_excl_sum<uint64_t>(s, sh, &tot);
+    for (uint64_t i = lo; i < hi; i++) {
+        uint32_t v = __ldcg(a + i);
+        a[i] = (uint32_t)ex;
+        ex += v;
+    }
+    __syncthreads();
+    return (uint32_t)tot;
+}
+
+}  // namespace kvx

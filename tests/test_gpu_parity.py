@@ -1,0 +1,267 @@
+"""CUDA path vs the CPU oracle, element by element (bit-exact: every output
+is integer or byte data).
+
+Small inputs: every output array and every slab / pool byte.  Full sizes of
+the five configurations (and the 64 KiB shape): every run-table, plan and
+rebuild array in full; the payload bytes by sampled segments against the
+seeded generator and by the pack-then-unpack identity over the whole pool.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_kvx_gb300 import kvx, workloads as W
+from tables import random_holder, random_lanes
+from gpu_helpers import (assert_plan_equal, assert_table_equal, check_all, gpu_plan,
+                         oracle_all)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("wl", W.small_variants(), ids=lambda w: w.name)
+def test_small_variants_bit_exact(wl):
+    check_all(wl.addr, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
+
+
+def test_random_holders_bit_exact():
+    rng = np.random.default_rng(2024)
+    for trial in range(60):
+        B = int(rng.integers(1, 40))
+        addr, seg_len, numa, pool = random_holder(rng, B, int(rng.integers(1, 9)), int(rng.integers(1, 4)))
+        check_all(addr, B, seg_len, numa, pool)
+
+
+def test_chunk_outgrows_stride_long_stretch():
+    """A long base-adjacent stretch whose blocks overlap: the fits cut runs
+    many times inside one stretch (the sequential walker)."""
+    B, L, seg = 3, 300, 16
+    addr = np.zeros((B, L), dtype=np.uint64)
+    for b in range(B):
+        addr[b] = b * 7 * seg + np.arange(L) * seg  # stride 112 < chunk
+    check_all(addr, B, np.full(L, seg, np.uint32), np.zeros(L, np.uint32), int(addr.max()) + seg)
+
+
+def test_random_lanes_many_tiles_all_radix_digits():
+    """Unstructured addresses over 40 bits, node ids in several bytes: R spans
+    several 2048-run tiles and every radix digit is active."""
+    rng = np.random.default_rng(77)
+    for B, L in ((777, 40), (1500, 9), (5, 1100)):
+        addr, seg_len, numa, pool = random_lanes(rng, B, L)
+        t, p, st, local = oracle_all(addr, B, seg_len, numa, pool)
+        tr = gpu_plan(addr, B, seg_len, numa, pool)
+        assert_table_equal(tr, t)
+        assert p.status == 0 and tr.read_status() == 0
+        assert_plan_equal(tr, p)
+        assert np.array_equal(tr.read_local(), local)
+
+
+@pytest.mark.parametrize("B,L", [(0, 4), (1, 2), (1, 7 * 2), (2, 2), (3, 50), (65, 34), (513, 2)])
+def test_edge_shapes(B, L):
+    rng = np.random.default_rng(B * 1000 + L)
+    slots = L // 2
+    if B == 0:
+        addr = np.zeros((0, L), dtype=np.uint64)
+        seg_len = np.full(L, 64, np.uint32)
+        tr = gpu_plan(addr, 0, seg_len, np.zeros(L, np.uint32), 4096)
+        assert tr.read_status() == 0 and tr.read_counts() == (0, 0, 0)
+        rpl, base, _, _ = tr.read_table()
+        assert np.all(rpl == 0) and base.size == 0
+        return
+    addr, seg_len, numa, pool = random_holder(rng, B, slots, 2)
+    check_all(addr, B, seg_len, numa, pool)
+
+
+def test_unaligned_segments_use_the_byte_path():
+    """Segment lengths that are not multiples of 16 bytes."""
+    rng = np.random.default_rng(5)
+    B, L = 9, 6
+    seg_len = np.array([3, 5, 7, 11, 13, 17], np.uint32)
+    addr = np.zeros((B, L), dtype=np.uint64)
+    pos = rng.permutation(B)
+    chunk = int(seg_len.sum()) + 1
+    for b in range(B):
+        off = 0
+        for l in range(L):
+            addr[b, l] = pos[b] * chunk + off
+            off += int(seg_len[l])
+    check_all(addr, B, seg_len, np.zeros(L, np.uint32), int(addr.max()) + 17)
+
+
+# --------------------------------------------------------- negative tables
+
+def _gpu_plan_table(B, seg_len, numa, pool, rpl, base, stride, count, num_runs=None,
+                    table_lanes=None, group_cap=None, desc_cap=None):
+    L = seg_len.size
+    tr = kvx.Transfer(B, seg_len, numa, pool)
+    R = base.size
+    assert R <= tr.run_cap
+    tr.runs_per_lane[: rpl.size].copy_(torch.from_numpy(rpl.astype(np.uint32).view(np.int32)))
+    if R:
+        tr.run_base[:R].copy_(torch.from_numpy(base.astype(np.uint64).view(np.int64)))
+        tr.run_stride[:R].copy_(torch.from_numpy(stride.astype(np.int64)))
+        tr.run_count[:R].copy_(torch.from_numpy(count.astype(np.uint32).view(np.int32)))
+    tr.num_runs.fill_(R if num_runs is None else num_runs)
+    tr.plan(table_lanes=table_lanes, group_cap=group_cap, desc_cap=desc_cap)
+    torch.cuda.synchronize()
+    return tr
+
+
+def test_validation_status_matches_oracle():
+    wl = W.tiny()
+    t = oracle.encode_runs(wl.addr)
+    cases = []
+    cases.append(("ok", dict()))
+    cases.append(("arrays", dict(num_runs=t.num_runs - 1)))
+    c = t.run_count.copy(); c[2] = 7
+    cases.append(("coverage", dict(count=c)))
+    c = t.run_count.copy(); c[1] = 0
+    cases.append(("zero_count", dict(count=c)))
+    sl = wl.seg_len.copy(); sl[2] = 0
+    cases.append(("zero_len", dict(seg_len=sl)))
+    cases.append(("span_pool", dict(pool=wl.pool_bytes - 1)))
+    s = t.run_stride.copy(); s[0] = 2**62
+    cases.append(("span_wrap", dict(stride=s)))
+    s = t.run_stride.copy(); s[3] = -(2**20)
+    cases.append(("span_negative", dict(stride=s)))
+    c = t.run_count.copy(); c[0] = 0
+    cases.append(("several", dict(count=c, seg_len=sl, pool=10)))
+    for name, kw in cases:
+        seg_len = kw.get("seg_len", wl.seg_len)
+        pool = kw.get("pool", wl.pool_bytes)
+        table = oracle.RunTable(t.runs_per_lane, t.run_base, kw.get("stride", t.run_stride),
+                                kw.get("count", t.run_count))
+        p = oracle.plan(table, wl.blocks, seg_len, wl.numa, pool, num_runs=kw.get("num_runs"))
+        tr = _gpu_plan_table(wl.blocks, seg_len, wl.numa, pool, table.runs_per_lane,
+                             table.run_base, table.run_stride, table.run_count,
+                             num_runs=kw.get("num_runs"))
+        assert tr.read_status() == p.status, name
+        assert tr.read_counts() == (p.groups.size, p.descs.size, p.slab_bytes), name
+    # wrong lane count
+    tr = _gpu_plan_table(wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes, t.runs_per_lane,
+                         t.run_base, t.run_stride, t.run_count, table_lanes=wl.lanes - 1)
+    assert tr.read_status() == kvx.S_LANES and tr.read_counts() == (0, 0, 0)
+    # one-block run with a stride
+    rpl = np.full(8, 2, np.uint32)
+    base = np.repeat(t.run_base, 2)
+    base[1::2] = t.run_base + 7 * t.run_stride.astype(np.uint64)
+    stride = np.repeat(t.run_stride, 2)
+    stride[1::2] = 0
+    count = np.tile(np.array([7, 1], np.uint32), 8)
+    tr = _gpu_plan_table(wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes, rpl, base, stride, count)
+    p = oracle.plan(oracle.RunTable(rpl, base, stride, count), wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
+    assert tr.read_status() == p.status == 0
+    assert_plan_equal(tr, p)
+    stride[1] = 5
+    tr = _gpu_plan_table(wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes, rpl, base, stride, count)
+    assert tr.read_status() == kvx.S_STRIDE1
+    # capacities
+    tr = _gpu_plan_table(wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes, t.runs_per_lane,
+                         t.run_base, t.run_stride, t.run_count, group_cap=1)
+    assert tr.read_status() == kvx.S_CAPACITY and tr.read_counts() == (0, 0, 0)
+    tr = _gpu_plan_table(wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes, t.runs_per_lane,
+                         t.run_base, t.run_stride, t.run_count, desc_cap=1)
+    assert tr.read_status() == kvx.S_CAPACITY and tr.read_counts() == (0, 0, 0)
+
+
+def test_rebuild_bounds_match_oracle():
+    wl = W.tiny()
+    t, p, st, local = oracle_all(wl.addr, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
+    tr = gpu_plan(wl.addr, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
+    g = p.groups.copy()
+    g["chunk"][0] -= 4096
+    tr.groups[: g.nbytes].copy_(torch.from_numpy(g.view(np.uint8)))
+    tr.status.zero_()
+    tr.rebuild()
+    torch.cuda.synchronize()
+    st, want = oracle.rebuild(t, p, wl.blocks, wl.lanes, wl.seg_len, groups=g)
+    assert tr.read_status() == st == oracle.S_BOUNDS
+    assert np.array_equal(tr.read_local(), want)
+    # slab one byte short: group 1's carve no longer fits
+    tr.groups[: p.groups.nbytes].copy_(torch.from_numpy(p.groups.view(np.uint8)))
+    tr.status.zero_()
+    tr.rebuild(slab_bytes=p.slab_bytes - 1)
+    torch.cuda.synchronize()
+    st, want = oracle.rebuild(t, p, wl.blocks, wl.lanes, wl.seg_len, slab_bytes=p.slab_bytes - 1)
+    assert tr.read_status() == st == oracle.S_BOUNDS
+    assert np.array_equal(tr.read_local(), want)
+
+
+def test_pack_descriptor_checks_match_oracle():
+    wl = W.tiny()
+    t, p, st, local = oracle_all(wl.addr, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
+    tr = gpu_plan(wl.addr, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
+    host_pool = W.holder_pool_np(wl)
+    pool = torch.from_numpy(host_pool).cuda()
+    for mutate in ("tiling", "bounds"):
+        d = p.descs.copy()
+        if mutate == "tiling":
+            d["local"][1] += 16
+        else:
+            d["remote"][1] = wl.pool_bytes - 8
+        tr.descs[: d.nbytes].copy_(torch.from_numpy(d.view(np.uint8)))
+        slab = torch.zeros(p.slab_bytes, dtype=torch.uint8, device="cuda")
+        tr.status.zero_()
+        tr.pack(pool, slab)
+        torch.cuda.synchronize()
+        want = np.zeros(p.slab_bytes, dtype=np.uint8)
+        stw = oracle.pack(host_pool, d, want)
+        assert tr.read_status() == stw, mutate
+        assert np.array_equal(slab.cpu().numpy(), want), mutate
+
+
+# ------------------------------------------------------------ full sizes
+
+FULL = ["tiny", "default", "worst", "mixed", "many_small", "wide64k"]
+
+
+def _used_positions(wl):
+    """Per region: (byte base, chunk, used-position mask) -- from the generator."""
+    out = []
+    for (first, nslots, base, npos), pos in zip(wl.regions, wl.pos):
+        used = np.zeros(npos, dtype=bool)
+        used[pos] = True
+        out.append((base, 2 * nslots * wl.seg, used))
+    return out
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_config(name):
+    wl = W.CONFIGS[name]()
+    t, p, st, local = oracle_all(wl.addr, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
+    assert p.status == 0 and st == 0
+    tr = gpu_plan(wl.addr, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
+    assert tr.read_status() == 0
+    assert_table_equal(tr, t)
+    assert_plan_equal(tr, p)
+    assert np.array_equal(tr.read_local(), local)
+
+    pool = torch.empty(wl.pool_bytes, dtype=torch.uint8, device="cuda")
+    W.fill_pool_torch(pool, wl.seed)
+    slab = torch.empty(tr.slab_bytes, dtype=torch.uint8, device="cuda")
+    tr.pack(pool, slab)
+    torch.cuda.synchronize()
+    assert tr.read_status() == 0
+    # sampled segments against the generator's bytes at their addresses
+    rng = np.random.default_rng(1)
+    B, L = wl.addr.shape
+    bs = rng.integers(0, B, size=400)
+    ls = rng.integers(0, L, size=400)
+    for b, l in zip(bs, ls):
+        a, lo, n = int(wl.addr[b, l]), int(local[b, l]), int(wl.seg_len[l])
+        got = slab[lo:lo + n].cpu().numpy()
+        assert np.array_equal(got, W.pool_bytes_np(wl.seed, a, n)), (b, l)
+    dst = torch.full((wl.pool_bytes,), W.CANARY, dtype=torch.uint8, device="cuda")
+    tr.unpack(slab, dst)
+    torch.cuda.synchronize()
+    assert tr.read_status() == 0
+    del slab
+    for base, chunk, used in _used_positions(wl):
+        n = used.size * chunk
+        a = pool[base:base + n].view(used.size, chunk)
+        d = dst[base:base + n].view(used.size, chunk)
+        u = torch.from_numpy(used).cuda()
+        assert torch.equal(a[u], d[u])
+        if (~used).any():
+            assert bool((d[~u] == W.CANARY).all())
+    assert wl.pool_bytes == sum(r[3] * 2 * r[1] * wl.seg for r in wl.regions)
