@@ -1,0 +1,435 @@
+#!/usr/bin/env python
+"""Benchmark of the paged KV block-transfer path on GB300.
+
+One step = one pass of the whole path over the default workload (1000 blocks
+x 288 slots x 2 x 4 KiB = 576k segments, 2250 MiB, bump-allocated holder in
+two NUMA regions): kvx_encode_runs, kvx_plan_groups, kvx_rebuild, kvx_pack,
+kvx_unpack, all on one stream with inputs resident in HBM.  The headline
+value is pack+unpack bytes (read + write: 4 N per step) over the step time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kvx|reference]
+
+--impl reference times the CPU oracle (the method as plain single-threaded
+C) on a bounded sample of the same workload.  Under torchrun every rank runs
+its own replica (independent transfers: weak scaling, no collective on the
+data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KV pack+unpack GB/s (fraction of HBM peak); run-encode Msegments/s"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0      # the ~8 TB/s nominal HBM3e figure
+FALLBACK_HBM_GBS = 6800.0     # profiling recipe's fallback when no measured peak exists
+WORKLOAD = ("default: 1000 blocks x 288 slots x 2 segments (K,V) x 4 KiB uint8 = 576,000 "
+            "segments, 2250 MiB, bump-allocated holder, slots 0-143 / 144-287 in two NUMA regions")
+COPY_SRC = os.path.join(ROOT, "paged_kv_cache_kvx_gb300", "csrc", "kvx_copy.cu")
+PROFILE = os.path.join(ROOT, "profiles", "copy_default.md")
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def copy_kernel_hash():
+    with open(COPY_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per copy launch from the committed ncu summary, only while
+    the copy kernel's source is the one that was profiled."""
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None
+    m = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
+    t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m or not t or m.group(1) != copy_kernel_hash():
+        return None
+    return float(t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="kvx_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- oracle arm
+
+def oracle_sample_step(wl, host_pool):
+    """One pass of the whole path through the CPU oracle; returns seconds."""
+    import oracle
+    t0 = time.perf_counter()
+    t = oracle.encode_runs(wl.addr)
+    p = oracle.plan(t, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
+    st, local = oracle.rebuild(t, p, wl.blocks, wl.lanes, wl.seg_len)
+    slab = np.empty(p.slab_bytes, dtype=np.uint8)
+    s1 = oracle.pack(host_pool, p.descs, slab)
+    dst = np.empty(wl.pool_bytes, dtype=np.uint8)
+    s2 = oracle.unpack(slab, p.descs, dst)
+    dt = time.perf_counter() - t0
+    if p.status or st or s1 or s2:
+        raise RuntimeError("oracle sample failed")
+    return dt
+
+
+def oracle_baseline(target_s: float, max_blocks: int = 100):
+    """Oracle on the first `blocks` blocks of the default workload, repeated
+    for about target_s seconds.  Returns (GB/s, description, steps)."""
+    from paged_kv_cache_kvx_gb300 import workloads as W
+    blocks = max_blocks
+    wl = W.bump("default_sample", blocks=blocks, slots=288, seg=4096, seed=2)
+    pool = W.holder_pool_np(wl)
+    first = oracle_sample_step(wl, pool)
+    n = max(1, int(target_s / max(first, 1e-6)))
+    times = [oracle_sample_step(wl, pool) for _ in range(n)]
+    per = statistics.median(times)
+    gbs = 4 * wl.payload_bytes / per / 1e9
+    desc = ("oracle encode+plan+rebuild+pack+unpack on the first %d of 1000 blocks of the default "
+            "workload (%d segments, %.0f MiB), median of %d passes, single thread"
+            % (blocks, wl.segments, wl.payload_bytes / 2**20, n))
+    return gbs, desc, n, per
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from paged_kv_cache_kvx_gb300 import workloads as W
+    import oracle
+    oracle.build()
+    # size the sample so warm-up + timed passes take about a minute
+    probe = W.bump("default_probe", blocks=20, slots=288, seg=4096, seed=2)
+    ppool = W.holder_pool_np(probe)
+    t_probe = oracle_sample_step(probe, ppool) / 20.0
+    budget = 60.0
+    blocks = int(max(2, min(1000, budget / max(1e-9, t_probe * (args.steps + args.warmup)))))
+    wl = W.bump("default_sample", blocks=blocks, slots=288, seg=4096, seed=2)
+    pool = W.holder_pool_np(wl)
+    for _ in range(args.warmup):
+        oracle_sample_step(wl, pool)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample_step(wl, pool)
+    dt = time.perf_counter() - t0
+    value = 4 * wl.payload_bytes * args.steps / dt / 1e9
+    sample = ("first %d of 1000 blocks of the default workload per step (%d segments, %.1f MiB), "
+              "single-threaded C oracle" % (blocks, wl.segments, wl.payload_bytes / 2**20))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample_blocks": blocks},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# -------------------------------------------------------------------- kvx arm
+
+def check_parity(tr, wl, pool, slab, dst, local_dev_np=None):
+    """The same process checks the CUDA path against the oracle first."""
+    import oracle
+    import torch
+    from paged_kv_cache_kvx_gb300 import workloads as W
+    t = oracle.encode_runs(wl.addr)
+    p = oracle.plan(t, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
+    st, local = oracle.rebuild(t, p, wl.blocks, wl.lanes, wl.seg_len)
+    assert p.status == 0 and st == 0
+    assert tr.read_status() == 0, "device status %#x" % tr.read_status()
+    rpl, base, stride, count = tr.read_table()
+    assert np.array_equal(rpl, t.runs_per_lane) and np.array_equal(base, t.run_base)
+    assert np.array_equal(stride, t.run_stride) and np.array_equal(count, t.run_count)
+    g = tr.read_plan()
+    assert g["groups"].tobytes() == p.groups.tobytes()
+    assert g["descs"].tobytes() == p.descs.tobytes()
+    assert np.array_equal(tr.read_local(), local)
+    rng = np.random.default_rng(0)
+    for b, l in zip(rng.integers(0, wl.blocks, 64), rng.integers(0, wl.lanes, 64)):
+        a, lo, n = int(wl.addr[b, l]), int(local[b, l]), int(wl.seg_len[l])
+        assert np.array_equal(slab[lo:lo + n].cpu().numpy(), W.pool_bytes_np(wl.seed, a, n))
+    # bump-allocated: every pool byte is a segment byte
+    assert torch.equal(pool, dst)
+    return len(p.descs), len(p.groups), t.num_runs
+
+
+def run_kvx(args):
+    import torch
+    import torch.distributed as dist
+    from paged_kv_cache_kvx_gb300 import kvx, workloads as W, build
+
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    build.build()
+    wl = W.default() if args.blocks == 1000 else W.bump("default", blocks=args.blocks, slots=288,
+                                                       seg=4096, nregions=2, seed=2)
+    N = wl.payload_bytes
+    S = wl.segments
+    tr = kvx.Transfer(wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes, device=dev)
+    tr.set_addr(wl.addr)
+    pool = torch.empty(wl.pool_bytes, dtype=torch.uint8, device=dev)
+    W.fill_pool_torch(pool, wl.seed)
+    slab = torch.empty(tr.slab_bytes, dtype=torch.uint8, device=dev)
+    dst = torch.full((wl.pool_bytes,), W.CANARY, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        tr.step(pool, slab, dst, stream=stream)
+    torch.cuda.synchronize()
+    ndescs, ngroups, nruns = check_parity(tr, wl, pool, slab, dst)
+
+    for _ in range(max(3, args.warmup)):
+        tr.step(pool, slab, dst, stream=stream)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    launches0 = kvx.kvx_launch_count()
+    start.record(stream)
+    for i in range(K):
+        e = ev[i]
+        e[0].record(stream)
+        tr.encode(stream=stream)
+        e[1].record(stream)
+        tr.plan(stream=stream)
+        e[2].record(stream)
+        tr.rebuild(stream=stream)
+        e[3].record(stream)
+        tr.pack(pool, slab, stream=stream)
+        e[4].record(stream)
+        tr.unpack(slab, dst, stream=stream)
+        e[5].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    launches = kvx.kvx_launch_count() - launches0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    total_ms = start.elapsed_time(end)
+    stage = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(5)] for e in ev])  # ms
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert tr.read_status() == 0
+    assert torch.equal(pool, dst)
+
+    # end to end through the same calls with host buffers
+    e2e = measure_e2e(tr, wl, pool, slab, dst, stream, args, dev) if not args.no_aux else None
+    # comparator: one plain device-to-device copy of N bytes
+    memcpy_gbs = measure_memcpy(pool, slab, N, stream) if not args.no_aux else None
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+    peak, peak_kind = load_peak()
+    ms_step = total_ms / K
+    value = 4.0 * N * K * world / (total_ms / 1e3) / 1e9
+    med = np.median(stage, axis=0)
+    mean = stage.mean(axis=0)
+    pack_gbs = 2.0 * N / (mean[3] / 1e3) / 1e9
+    unpack_gbs = 2.0 * N / (mean[4] / 1e3) / 1e9
+    dom = 3 if mean[3] >= mean[4] else 4
+    achieved = 2.0 * N / (mean[dom] / 1e3) / 1e9
+    traffic = profiled_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "bytes_moved_per_step": 4 * N,
+                   "l2": "inputs larger than L2 (2250 MiB pool and slab vs 129 MB), no flush",
+                   "runs": nruns, "groups": ngroups, "descs": ndescs},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "kvx_pack" if dom == 3 else "kvx_unpack",
+                     "peak_source": "%s hbm_gbs" % peak_kind},
+        "pack_gbs": pack_gbs, "unpack_gbs": unpack_gbs,
+        "pack_unpack_gbs": 4.0 * N / ((mean[3] + mean[4]) / 1e3) / 1e9,
+        "frac_of_%s_peak" % peak_kind: 4.0 * N / ((mean[3] + mean[4]) / 1e3) / 1e9 / peak,
+        "frac_of_nominal_8tbs": 4.0 * N / ((mean[3] + mean[4]) / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+        "encode_msegs_per_s": S / (mean[0] / 1e3) / 1e6,
+        "stage_ms_mean": dict(zip(["encode", "plan", "rebuild", "pack", "unpack"], map(float, mean))),
+        "stage_ms_median": dict(zip(["encode", "plan", "rebuild", "pack", "unpack"], map(float, med))),
+        "memcpy_d2d_gbs": memcpy_gbs,
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+    }
+    if blocks_note := (args.blocks != 1000):
+        line["config"]["workload"] = "reduced for profiling: %d of the default 1000 blocks" % args.blocks
+    if rank == 0 and world == 1 and not args.no_aux:
+        cb, desc, n, per = oracle_baseline(target_s=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": cb, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": desc}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_e2e(tr, wl, pool, slab, dst, stream, args, dev):
+    """Same metric through the same calls with HOST buffers: every step copies
+    the address table and the holder pool in from pinned memory and copies the
+    unpacked pool and the rebuilt pointers back out."""
+    import torch
+    h_addr = torch.from_numpy(wl.addr.reshape(-1).view(np.int64).copy()).pin_memory()
+    h_pool = torch.empty(wl.pool_bytes, dtype=torch.uint8).pin_memory()
+    h_pool.copy_(pool, non_blocking=False)
+    h_dst = torch.empty(wl.pool_bytes, dtype=torch.uint8).pin_memory()
+    h_local = torch.empty(wl.blocks * wl.lanes, dtype=torch.int64).pin_memory()
+    n_in = h_addr.numel() * 8 + h_pool.numel()
+    n_out = h_dst.numel() + h_local.numel() * 8
+
+    def one():
+        with torch.cuda.stream(stream):
+            tr.addr[: h_addr.numel()].copy_(h_addr, non_blocking=True)
+            pool.copy_(h_pool, non_blocking=True)
+            tr.step(pool, slab, dst, stream=stream)
+            h_dst.copy_(dst, non_blocking=True)
+            h_local.copy_(tr.local[: h_local.numel()], non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, 20))
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    ok = bool(torch.equal(h_dst, h_pool))
+    return {"value": 4.0 * wl.payload_bytes / (ms / 1e3) / 1e9, "unit": UNIT,
+            "h2d_bytes_per_step": int(n_in), "d2h_bytes_per_step": int(n_out),
+            "ms_per_step": ms, "steps": steps, "verified": ok}
+
+
+def measure_memcpy(pool, slab, N, stream):
+    import torch
+    src = pool[:N]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            slab.copy_(src, non_blocking=True)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    n = 20
+    with torch.cuda.stream(stream):
+        for _ in range(n):
+            slab.copy_(src, non_blocking=True)
+    b.record(stream)
+    torch.cuda.synchronize()
+    return 2.0 * N * n / (a.elapsed_time(b) / 1e3) / 1e9
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["kvx", "reference"], default="kvx")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU work for the oracle baseline leg of the kvx arm")
+    ap.add_argument("--blocks", type=int, default=1000,
+                    help="blocks of the default shape (1000; fewer only for profiler captures)")
+    ap.add_argument("--no-aux", action="store_true",
+                    help="skip the e2e, memcpy and CPU-baseline legs (profiler captures)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_kvx(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

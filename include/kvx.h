@@ -195,15 +195,15 @@ kvx_status kvx_plan_groups(const uint32_t *runs_per_lane, uint32_t table_lanes,
 /* ---------------------------------------------------------------- rebuild */
 
 /*
- * Rebuild every segment's slab pointer arithmetically (Requester step 5):
- * local(b, l) = G.local + (b - G.block) * G.chunk + run_off[r], where r is
- * the run of lane l covering block b and G its group.  For a dense group this
- * is the page's group_local + (remote(b) - group_remote); for a non-dense
- * group it addresses the dense local mirror.  Each pointer is checked: the
- * group index is below counts[0], b lies in the group's block range, the
- * segment [local, local + seg_len[l]) lies inside its block's chunk of the
- * group carve, and the carve ends within slab_bytes.  A failing entry is set
- * to UINT64_MAX and KVX_S_BOUNDS is raised.
+ * Rebuild every segment's slab pointer arithmetically (Requester step 5).
+ * With r the run of lane l covering block b, G its group and i = b - G.block:
+ * a dense group gives the page's local = group_local + (remote(b) -
+ * group_remote) = G.local + i * G.stride + run_off[r]; a non-dense group
+ * gives its dense local mirror, G.local + i * G.chunk + run_off[r].  Each
+ * pointer is checked: the group index is below counts[0], b lies in the
+ * group's block range, the segment [local, local + seg_len[l]) lies inside
+ * block i's chunk of the group carve, and the carve ends within slab_bytes.
+ * A failing entry is set to UINT64_MAX and KVX_S_BOUNDS is raised.
  *
  * Inputs: lane_first [L + 1], run_block, run_group, run_off [run_capacity]
  * and groups as kvx_plan_groups wrote them; counts (device, [0] = groups);

@@ -2,11 +2,14 @@
 // Requester step 5: local(b) = group_local + (remote(b) - group_remote),
 // every pointer bounds-checked).
 //
-// With run r of lane l covering block b and G = its group,
-//   local(b, l) = G.local + (b - G.block) * G.chunk + run_off[r].
-// For a dense group (chunk == stride) this is the page's formula, since
-// remote(b, l) - G.base = (b - G.block) * stride + run_off[r]; for a non-dense
-// group it addresses the dense local mirror of block b.
+// With run r of lane l covering block b, G = its group and i = b - G.block:
+//   dense group:     local = G.local + (remote(b) - G.base)
+//                          = G.local + i * G.stride + run_off[r]
+//   non-dense group: local = G.local + i * G.chunk + run_off[r]
+// (the page's formula, and its dense local mirror of each remote block).
+// The checks: the group index is valid, b is inside the group's block range,
+// [local, local + len) lies inside block i's slice [G.local + i*chunk,
+// G.local + (i+1)*chunk) of the carve, and the carve ends inside the slab.
 //
 // Thread layout as in the encoder: a CTA is 8 warps; lane t of warp w handles
 // lane l0 + t over K consecutive blocks, so each warp store is one coalesced
@@ -64,9 +67,9 @@ k_rebuild(const uint32_t *__restrict__ lane_first, const uint32_t *__restrict__ 
         r = a;
     }
     uint32_t bad = 0;
-    // current run's cached group
-    uint64_t cur_r = ~0ull, g_local = 0, g_chunk = 0, off = 0;
-    uint64_t g_block = 0, g_count = 0;
+    // cached per run: its group's fields and its offset inside the group
+    uint64_t cur_r = ~0ull, off = 0, g_block = 0, g_count = 0;
+    __int128 g_local = 0, g_chunk = 0, g_step = 0;
     bool run_ok = false;
     for (uint64_t b = b0; b < b1; b++) {
         uint64_t out = ~0ull;
@@ -78,20 +81,23 @@ k_rebuild(const uint32_t *__restrict__ lane_first, const uint32_t *__restrict__ 
                 run_ok = gi < ngroups;
                 if (run_ok) {
                     const kvx_group G = groups[gi];
-                    g_local = G.local;
-                    g_chunk = G.chunk;
+                    g_local = (__int128)G.local;
+                    g_chunk = (__int128)G.chunk;
+                    // dense: remote(b) - group_remote advances by the stride;
+                    // non-dense: the dense local mirror advances by the chunk
+                    g_step = G.dense ? (__int128)G.stride : (__int128)G.chunk;
                     g_block = G.block;
                     g_count = G.count;
                     off = run_off[r];
-                    // the segment lies inside its block's chunk, the carve in the slab
-                    const unsigned __int128 carve_end =
-                        (unsigned __int128)G.local + (unsigned __int128)G.count * G.chunk;
-                    run_ok = off <= G.chunk && len <= G.chunk - off &&
-                             carve_end <= (unsigned __int128)slab_bytes;
+                    run_ok = g_local + (__int128)G.count * g_chunk <= (__int128)slab_bytes;
                 }
             }
-            if (run_ok && b >= g_block && b - g_block < g_count && run_block[r] <= b)
-                out = g_local + (b - g_block) * g_chunk + off;
+            if (run_ok && b >= g_block && b - g_block < g_count && run_block[r] <= b) {
+                const __int128 i = (__int128)(b - g_block);
+                const __int128 loc = g_local + i * g_step + (__int128)off;
+                const __int128 slice = g_local + i * g_chunk;  // this block's part of the carve
+                if (loc >= slice && loc + (__int128)len <= slice + g_chunk) out = (uint64_t)loc;
+            }
         }
         if (out == ~0ull) bad = KVX_S_BOUNDS;
         local[b * L + l] = out;
