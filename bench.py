@@ -342,7 +342,7 @@ def run_kvx(args):
         "gpu_launches": int(launches),
         "clocks": clocks,
     }
-    if blocks_note := (args.blocks != 1000):
+    if args.blocks != 1000:
         line["config"]["workload"] = "reduced for profiling: %d of the default 1000 blocks" % args.blocks
     if rank == 0 and world == 1 and not args.no_aux:
         cb, desc, n, per = oracle_baseline(target_s=args.cpu_seconds)

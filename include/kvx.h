@@ -74,6 +74,8 @@ typedef enum kvx_status {
 #define KVX_S_BOUNDS     128u  /* a pointer or copy outside its slab/pool/group range */
 #define KVX_S_DESC       256u  /* descriptors do not tile the slab in order */
 #define KVX_S_CAPACITY   512u  /* a plan output exceeds its capacity, or the slab 2^63 bytes */
+#define KVX_S_TIMEOUT    1024u /* a copy kernel's bounded wait on its own bulk copy gave up
+                                  (the GPU did not deliver the bytes; the copy is incomplete) */
 
 /* READ splitting: planned descriptors are split into pieces of at most
  * MAX_RDMA_READ_BYTES = 32 MiB. */

@@ -4,17 +4,22 @@
 // holder-pool bytes into the dense slab; unpack is the inverse scatter.
 //
 // HBM-bound copy, no contraction.  The slab side is always contiguous (the
-// descriptors tile it), so the work is cut into fixed 32 KiB slab tiles:
-// a persistent grid walks the tiles round-robin, so at any moment the grid
-// streams one contiguous window of the slab and, per descriptor, of the pool.
-// A prep kernel checks the descriptors and records, for every tile, the
-// descriptor holding the tile's first byte.  Inside a tile:
-//   - one descriptor covers it (every tile of a dense 32 MiB read): each
-//     thread moves 8 x 16-byte vectors, all loads issued before the stores;
-//   - several descriptors, all 16-byte aligned (4 KiB / 512 B segment
-//     reads): the tile's descriptors are staged in shared memory and every
-//     16-byte vector finds its descriptor by binary search;
-//   - anything unaligned: byte copies (correct for any layout, slow).
+// descriptors tile it), so the work is cut into fixed 32 KiB slab tiles.  A
+// prep kernel checks the descriptors and sorts every tile into one of two
+// lists:
+//   - TMA jobs: tiles inside one 16-byte aligned descriptor (every tile of a
+//     dense 32 MiB read, most tiles of a 1 MiB per-block read).  One lane per
+//     SM streams them through a 6-stage shared-memory ring with bulk copies
+//     (cp.async.bulk global->shared, completion on an mbarrier, then
+//     cp.async.bulk shared->global): the SM's bulk-copy unit moves the
+//     bytes, no register staging, up to 192 KiB of loads in flight per SM.
+//   - vector tiles: tiles that hold several descriptors (4 KiB / 512 B
+//     segment reads) or unaligned ones.  256 threads per tile; the tile's
+//     descriptors are staged in shared memory and each 16-byte vector finds
+//     its descriptor by binary search (byte copies when anything is
+//     unaligned).
+// Both copy kernels walk their list round-robin over a persistent grid, so
+// the grid streams one window of the slab at a time.
 #include "kvx_common.cuh"
 
 namespace kvx {
@@ -24,23 +29,39 @@ constexpr int kThreads = 256;
 constexpr uint64_t kTileBytes = 32 * 1024;
 constexpr int kVecPerThread = (int)(kTileBytes / (kThreads * 16));  // 8
 constexpr int kCtasPerSm = 3;
+constexpr int kStages = 6;                  // TMA ring depth per SM
+constexpr uint32_t kSpinLimit = 1u << 26;   // bounded mbarrier wait (seconds at most)
 
 struct CopyCtl {
     unsigned long long used;  // end of the last descriptor (slab bytes in use)
     uint32_t bad;             // descriptors do not tile the slab
+    uint32_t n_tma;           // TMA jobs
+    uint32_t n_vec;           // vector tiles
+    uint32_t pad;
+};
+
+struct TmaJob {
+    uint64_t lo;      // slab offset of the tile
+    uint64_t delta;   // pool offset - slab offset inside the tile's descriptor
+    uint32_t len;     // bytes (multiple of 16)
     uint32_t pad;
 };
 
 struct Ws {
     CopyCtl *ctl;
-    uint32_t *tile_desc;  // [ceil(slab_bytes / kTileBytes)]
+    uint32_t *tile_desc;  // [ntiles]
+    TmaJob *jobs;         // [ntiles]
+    uint32_t *vec_tiles;  // [ntiles]
 };
 
 Ws carve(void *base, uint64_t slab_bytes, size_t *bytes) {
+    const uint64_t nt = ceil_div(slab_bytes, kTileBytes);
     Carver c(base);
     Ws w;
     w.ctl = c.take<CopyCtl>(1);
-    w.tile_desc = c.take<uint32_t>(ceil_div(slab_bytes, kTileBytes));
+    w.tile_desc = c.take<uint32_t>(nt);
+    w.jobs = c.take<TmaJob>(nt);
+    w.vec_tiles = c.take<uint32_t>(nt);
     *bytes = c.off;
     return w;
 }
@@ -49,16 +70,19 @@ __device__ __forceinline__ bool in_range(uint64_t off, uint64_t len, uint64_t si
     return off <= size && len <= size - off;
 }
 
-// One thread per descriptor: tiling check, bounds check, tile -> descriptor map.
+// Descriptor checks (one thread per descriptor: tiling, bounds), then one
+// thread per tile: the descriptor holding the tile's first byte (binary
+// search) and the tile's list.
 __global__ void __launch_bounds__(kThreads)
 k_copy_prep(const kvx_desc *__restrict__ descs, const uint64_t *__restrict__ num_descs,
-            uint64_t desc_cap, uint64_t pool_bytes, uint64_t slab_bytes,
-            uint32_t *__restrict__ tile_desc, CopyCtl *ctl, uint32_t *status) {
+            uint64_t desc_cap, uint64_t pool_bytes, uint64_t slab_bytes, bool bases_aligned,
+            uint32_t *__restrict__ tile_desc, TmaJob *__restrict__ jobs,
+            uint32_t *__restrict__ vec_tiles, CopyCtl *ctl, uint32_t *status) {
     const uint64_t n = *num_descs < desc_cap ? *num_descs : desc_cap;
-    const uint64_t ntiles = ceil_div(slab_bytes, kTileBytes);
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
     uint32_t bits = 0;
-    for (uint64_t k = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; k < n;
-         k += (uint64_t)gridDim.x * blockDim.x) {
+    for (uint64_t k = tid; k < n; k += stride) {
         const kvx_desc d = descs[k];
         uint64_t expect = 0;
         bool tiled = true;
@@ -76,13 +100,189 @@ k_copy_prep(const kvx_desc *__restrict__ descs, const uint64_t *__restrict__ num
         if (!in_range(d.remote, d.len, pool_bytes) || !in_range(d.local, d.len, slab_bytes))
             bits |= KVX_S_BOUNDS;
         if (k + 1 == n) ctl->used = d.local + d.len;
-        // tiles whose first byte lies in [local, local + len)
-        uint64_t t = ceil_div(d.local, kTileBytes);
-        const uint64_t t_end = (d.local + d.len - 1) / kTileBytes;
-        for (; t <= t_end && t < ntiles; t++) tile_desc[t] = (uint32_t)k;
     }
     if (bits) atomicOr(status, bits);
+    if (n == 0) return;
+    // The lists are only read when the descriptors tile the slab (else the
+    // copy kernels do nothing), so the last descriptor's end is the bytes in use.
+    const kvx_desc last = descs[n - 1];
+    const uint64_t used = last.local + last.len < slab_bytes ? last.local + last.len : slab_bytes;
+    const uint64_t ntiles = ceil_div(used, kTileBytes);
+    const uint32_t lane = threadIdx.x & 31;
+    for (uint64_t t0 = tid - lane; t0 < ntiles; t0 += stride) {  // warp-uniform loop
+        const uint64_t t = t0 + lane;
+        bool is_tma = false, is_vec = false;
+        TmaJob job{};
+        if (t < ntiles) {
+            const uint64_t lo = t * kTileBytes;
+            const uint64_t hi = lo + kTileBytes < used ? lo + kTileBytes : used;
+            uint64_t a = 0, z = n;  // last k with descs[k].local <= lo, in [a, z)
+            while (z - a > 1) {
+                const uint64_t m = (a + z) >> 1;
+                if (descs[m].local <= lo) a = m; else z = m;
+            }
+            tile_desc[t] = (uint32_t)a;
+            const kvx_desc d = descs[a];
+            const bool single = d.local <= lo && hi - d.local <= d.len;
+            const bool inb = in_range(d.remote, d.len, pool_bytes) && in_range(d.local, d.len, slab_bytes);
+            const uint64_t delta = d.remote - d.local;
+            if (single && !inb) {
+                // skipped: its descriptor leaves the pool or the slab
+            } else if (single && bases_aligned && ((lo | hi | delta) & 15) == 0) {
+                is_tma = true;
+                job = TmaJob{lo, delta, (uint32_t)(hi - lo), 0};
+            } else {
+                is_vec = true;
+            }
+        }
+        const uint32_t mt = __ballot_sync(0xFFFFFFFFu, is_tma);
+        const uint32_t mv = __ballot_sync(0xFFFFFFFFu, is_vec);
+        uint32_t bt = 0, bv = 0;
+        if (lane == 0) {
+            if (mt) bt = atomicAdd(&ctl->n_tma, __popc(mt));
+            if (mv) bv = atomicAdd(&ctl->n_vec, __popc(mv));
+        }
+        bt = __shfl_sync(0xFFFFFFFFu, bt, 0);
+        bv = __shfl_sync(0xFFFFFFFFu, bv, 0);
+        const uint32_t below = (1u << lane) - 1u;
+        if (is_tma) jobs[bt + __popc(mt & below)] = job;
+        if (is_vec) vec_tiles[bv + __popc(mv & below)] = (uint32_t)t;
+    }
 }
+
+// ------------------------------------------------------------- TMA path
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: false after kSpinLimit polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kSpinLimit; i++) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (i > 64) __nanosleep(32);
+    }
+    return false;
+}
+
+__device__ __forceinline__ void bulk_g2s(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(sdst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_s2g(void *gdst, const void *ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+                 "r"(smem_u32(ssrc)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// One warp per CTA, one CTA per SM; lane 0 drives the ring, the warp loads
+// job records 32 at a time.
+template <bool PACK>
+__global__ void __launch_bounds__(32, 1)
+k_copy_tma(const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r, uint8_t *slab_w,
+           const TmaJob *__restrict__ jobs, const CopyCtl *ctl, uint32_t *status) {
+    extern __shared__ __align__(128) uint8_t ring[];
+    __shared__ __align__(8) uint64_t bars[kStages];
+    const uint32_t lane = threadIdx.x;
+    if (ctl->bad) return;
+    const uint32_t n = ctl->n_tma;
+    const uint32_t G = gridDim.x;
+    const uint32_t count = n > blockIdx.x ? (n - blockIdx.x + G - 1) / G : 0;
+    if (count == 0) return;
+    if (lane == 0) {
+        for (int s = 0; s < kStages; s++) mbar_init(&bars[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    uint8_t *dst_ring[kStages];
+    uint32_t len_ring[kStages];
+    bool ok = true;
+    TmaJob mine{};  // job (base + lane) of the current batch of 32
+    uint32_t batch = ~0u;
+    uint32_t issued = 0;  // loads issued
+    uint32_t landed = 0;  // loads whose barrier completed (in order)
+    for (uint32_t i = 0; i < count + kStages - 1 && ok; i++) {
+        if (i < count) {
+            const uint32_t b = i / 32;
+            if (b != batch) {
+                batch = b;
+                const uint32_t j = b * 32 + lane;
+                if (j < count) mine = jobs[blockIdx.x + (uint64_t)j * G];
+            }
+            const uint32_t src_lane = i % 32;
+            const uint64_t lo = __shfl_sync(0xFFFFFFFFu, mine.lo, src_lane);
+            const uint64_t delta = __shfl_sync(0xFFFFFFFFu, mine.delta, src_lane);
+            const uint32_t len = __shfl_sync(0xFFFFFFFFu, mine.len, src_lane);
+            if (lane == 0) {
+                const int s = i % kStages;
+                if (i >= kStages) bulk_wait_read_all();  // buffer s: store i-kStages done reading
+                const uint8_t *src = PACK ? pool_r + lo + delta : slab_r + lo;
+                dst_ring[s] = PACK ? slab_w + lo : pool_w + lo + delta;
+                len_ring[s] = len;
+                mbar_arrive_expect_tx(&bars[s], len);
+                bulk_g2s(ring + (uint64_t)s * kTileBytes, src, len, &bars[s]);
+                issued++;
+            }
+        }
+        if (lane == 0 && i >= kStages - 1) {
+            const uint32_t k = i - (kStages - 1);
+            if (k < count) {
+                const int s = k % kStages;
+                if (!mbar_wait(&bars[s], (k / kStages) & 1u)) {
+                    ok = false;
+                } else {
+                    landed = k + 1;
+                    bulk_s2g(dst_ring[s], ring + (uint64_t)s * kTileBytes, len_ring[s]);
+                    bulk_commit();
+                }
+            }
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    }
+    if (lane == 0) {
+        if (!ok) {
+            atomicOr(status, KVX_S_TIMEOUT);
+            // let the loads still in flight (at most kStages) land before the
+            // ring is released; each barrier has one use outstanding
+            for (uint32_t k = landed; k < issued; k++) mbar_wait(&bars[k % kStages], (k / kStages) & 1u);
+        }
+        bulk_wait_all();
+    }
+    __syncwarp();
+}
+
+// ---------------------------------------------------------- vector path
 
 __device__ __forceinline__ uint4 ld_stream(const uint8_t *p) {
     return __ldcs(reinterpret_cast<const uint4 *>(p));
@@ -91,71 +291,28 @@ __device__ __forceinline__ void st_stream(uint8_t *p, uint4 v) {
     __stcs(reinterpret_cast<uint4 *>(p), v);
 }
 
-// Copy slab range [x0, x1) of one span; slab offset x maps to pool offset
-// x + delta.  PACK: pool -> slab; else slab -> pool.
-template <bool PACK>
-__device__ __forceinline__ void copy_span_vec(const uint8_t *pool_r, uint8_t *pool_w,
-                                              const uint8_t *slab_r, uint8_t *slab_w, uint64_t x0,
-                                              uint64_t x1, uint64_t delta) {
-    for (uint64_t x = x0 + (uint64_t)threadIdx.x * 16; x < x1;
-         x += (uint64_t)kThreads * 16 * kVecPerThread) {
-        uint4 v[kVecPerThread];
-#pragma unroll
-        for (int u = 0; u < kVecPerThread; u++) {
-            const uint64_t xx = x + (uint64_t)u * kThreads * 16;
-            if (xx < x1) v[u] = PACK ? ld_stream(pool_r + xx + delta) : ld_stream(slab_r + xx);
-        }
-#pragma unroll
-        for (int u = 0; u < kVecPerThread; u++) {
-            const uint64_t xx = x + (uint64_t)u * kThreads * 16;
-            if (xx < x1) {
-                if (PACK) st_stream(slab_w + xx, v[u]);
-                else st_stream(pool_w + xx + delta, v[u]);
-            }
-        }
-    }
-}
-
-template <bool PACK>
-__device__ __forceinline__ void copy_span_bytes(const uint8_t *pool_r, uint8_t *pool_w,
-                                                const uint8_t *slab_r, uint8_t *slab_w, uint64_t x0,
-                                                uint64_t x1, uint64_t delta) {
-    for (uint64_t x = x0 + threadIdx.x; x < x1; x += kThreads) {
-        if (PACK) slab_w[x] = pool_r[x + delta];
-        else pool_w[x + delta] = slab_r[x];
-    }
-}
-
 template <bool PACK>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
-k_copy(const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r, uint8_t *slab_w,
-       uint64_t pool_bytes, uint64_t slab_bytes, bool bases_aligned,
-       const kvx_desc *__restrict__ descs, const uint64_t *__restrict__ num_descs,
-       uint64_t desc_cap, const uint32_t *__restrict__ tile_desc, const CopyCtl *ctl) {
+k_copy_vec(const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r, uint8_t *slab_w,
+           uint64_t pool_bytes, uint64_t slab_bytes, bool bases_aligned,
+           const kvx_desc *__restrict__ descs, const uint64_t *__restrict__ num_descs,
+           uint64_t desc_cap, const uint32_t *__restrict__ tile_desc,
+           const uint32_t *__restrict__ vec_tiles, const CopyCtl *ctl) {
     __shared__ uint64_t s_lo[kThreads + 1];
     __shared__ uint64_t s_delta[kThreads];
     __shared__ uint8_t s_ok[kThreads];
     if (ctl->bad) return;
     const uint64_t n = *num_descs < desc_cap ? *num_descs : desc_cap;
     const uint64_t used = ctl->used < slab_bytes ? ctl->used : slab_bytes;
-    const uint64_t ntiles = ceil_div(used, kTileBytes);
-    for (uint64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const uint32_t nlist = ctl->n_vec;
+    for (uint32_t li = blockIdx.x; li < nlist; li += gridDim.x) {
+        const uint64_t t = vec_tiles[li];
         uint64_t lo = t * kTileBytes;
+        if (lo >= used) continue;
         const uint64_t hi = lo + kTileBytes < used ? lo + kTileBytes : used;
         uint64_t k = tile_desc[t];
         if (k >= n) continue;
-        const kvx_desc d0 = descs[k];
-        if (d0.local <= lo && hi - d0.local <= d0.len) {
-            // one descriptor covers the whole tile
-            if (!in_range(d0.remote, d0.len, pool_bytes) || !in_range(d0.local, d0.len, slab_bytes))
-                continue;
-            const uint64_t delta = d0.remote - d0.local;
-            const bool al = bases_aligned && ((lo | hi | delta) & 15) == 0;
-            if (al) copy_span_vec<PACK>(pool_r, pool_w, slab_r, slab_w, lo, hi, delta);
-            else copy_span_bytes<PACK>(pool_r, pool_w, slab_r, slab_w, lo, hi, delta);
-            continue;
-        }
-        // several descriptors: stage up to kThreads of them at a time
+        // stage up to kThreads descriptors at a time
         while (lo < hi) {
             const uint64_t kk = k + threadIdx.x;
             bool in = false, ok = false, aligned = true;
@@ -230,6 +387,18 @@ k_copy(const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r, uint8_t *s
     }
 }
 
+template <bool PACK>
+cudaError_t set_tma_smem() {
+    static bool done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(k_copy_tma<PACK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(kStages * kTileBytes));
+    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+    return e;
+}
+
 kvx_status launch(bool pack, const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r,
                   uint8_t *slab_w, uint64_t pool_bytes, uint64_t slab_bytes, const kvx_desc *descs,
                   const uint64_t *num_descs, uint64_t desc_cap, uint32_t *status, void *ws,
@@ -239,25 +408,31 @@ kvx_status launch(bool pack, const uint8_t *pool_r, uint8_t *pool_w, const uint8
     size_t need = 0;
     Ws w = carve(ws, slab_bytes, &need);
     if (ws_bytes < need) return KVX_EINVAL;
+    if ((pack ? set_tma_smem<true>() : set_tma_smem<false>()) != cudaSuccess) return KVX_ECUDA;
     cudaStream_t s = as_stream(stream);
     if (cudaMemsetAsync(w.ctl, 0, sizeof(CopyCtl), s) != cudaSuccess) return KVX_ECUDA;
-    const uint64_t prep_grid = ceil_div(desc_cap ? desc_cap : 1, kThreads);
-    const uint64_t prep_max = (uint64_t)sm_count() * kCtasPerSm;
-    const uint32_t pg = (uint32_t)(prep_grid < prep_max ? prep_grid : prep_max);
-    k_copy_prep<<<pg, kThreads, 0, s>>>(descs, num_descs, desc_cap, pool_bytes, slab_bytes,
-                                        w.tile_desc, w.ctl, status);
-    KVX_LAUNCHED();
     const uintptr_t pa = reinterpret_cast<uintptr_t>(pool_r ? (const void *)pool_r : pool_w);
     const uintptr_t sa = reinterpret_cast<uintptr_t>(slab_r ? (const void *)slab_r : slab_w);
     const bool aligned = ((pa | sa) & 15) == 0;
-    const uint32_t grid = (uint32_t)(sm_count() * kCtasPerSm);
+    const int sms = sm_count();
+    k_copy_prep<<<sms * 2, kThreads, 0, s>>>(descs, num_descs, desc_cap, pool_bytes, slab_bytes,
+                                              aligned, w.tile_desc, w.jobs, w.vec_tiles, w.ctl, status);
+    KVX_LAUNCHED();
+    const size_t smem = (size_t)kStages * kTileBytes;
     if (pack)
-        k_copy<true><<<grid, kThreads, 0, s>>>(pool_r, pool_w, slab_r, slab_w, pool_bytes, slab_bytes,
-                                               aligned, descs, num_descs, desc_cap, w.tile_desc, w.ctl);
+        k_copy_tma<true><<<sms, 32, smem, s>>>(pool_r, pool_w, slab_r, slab_w, w.jobs, w.ctl, status);
     else
-        k_copy<false><<<grid, kThreads, 0, s>>>(pool_r, pool_w, slab_r, slab_w, pool_bytes,
-                                                slab_bytes, aligned, descs, num_descs, desc_cap,
-                                                w.tile_desc, w.ctl);
+        k_copy_tma<false><<<sms, 32, smem, s>>>(pool_r, pool_w, slab_r, slab_w, w.jobs, w.ctl, status);
+    KVX_LAUNCHED();
+    const uint32_t grid = (uint32_t)(sms * kCtasPerSm);
+    if (pack)
+        k_copy_vec<true><<<grid, kThreads, 0, s>>>(pool_r, pool_w, slab_r, slab_w, pool_bytes,
+                                                   slab_bytes, aligned, descs, num_descs, desc_cap,
+                                                   w.tile_desc, w.vec_tiles, w.ctl);
+    else
+        k_copy_vec<false><<<grid, kThreads, 0, s>>>(pool_r, pool_w, slab_r, slab_w, pool_bytes,
+                                                    slab_bytes, aligned, descs, num_descs, desc_cap,
+                                                    w.tile_desc, w.vec_tiles, w.ctl);
     KVX_LAUNCHED();
     return KVX_OK;
 }

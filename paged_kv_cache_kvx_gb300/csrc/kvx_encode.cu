@@ -185,15 +185,25 @@ k_encode_tiles(const uint64_t *__restrict__ addr, uint32_t B, uint32_t L, Geomet
     }
     if (!last_block(&ctl->ticket)) return;
 
-    // Last block: per lane, tiles in order -> entry prefixes.
+    // Last block: per lane, tiles in order -> entry prefixes.  Records are
+    // loaded in batches before they are combined and overwritten, so the
+    // loads of a batch are in flight together.
+    constexpr uint32_t kBatch = 8;
     for (uint32_t lane = threadIdx.x; lane < L; lane += blockDim.x) {
         Prefix p{0u, 0u, kNone};
-        for (uint32_t r = 0; r < g.ntr; r++) {
-            TileRec *rec = tiles + (uint64_t)r * L + lane;
-            const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(rec));
-            const Xfer xr = unpack_xfer(TileRec{v.x, v.y, v.z, v.w});
-            *rec = TileRec{p.state, p.runs, p.prev, 0u};
-            p = prefix_then(p, xr);
+        for (uint32_t r0 = 0; r0 < g.ntr; r0 += kBatch) {
+            uint4 v[kBatch];
+#pragma unroll
+            for (uint32_t j = 0; j < kBatch; j++)
+                if (r0 + j < g.ntr)
+                    v[j] = __ldcg(reinterpret_cast<const uint4 *>(tiles + (uint64_t)(r0 + j) * L + lane));
+#pragma unroll
+            for (uint32_t j = 0; j < kBatch; j++) {
+                if (r0 + j >= g.ntr) break;
+                const Xfer xr = unpack_xfer(TileRec{v[j].x, v[j].y, v[j].z, v[j].w});
+                tiles[(uint64_t)(r0 + j) * L + lane] = TileRec{p.state, p.runs, p.prev, 0u};
+                p = prefix_then(p, xr);
+            }
         }
         runs_per_lane[lane] = p.runs;
         lane_base[lane] = p.runs;

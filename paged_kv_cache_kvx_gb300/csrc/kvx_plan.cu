@@ -254,8 +254,11 @@ k_plan_init(const uint32_t *__restrict__ rpl, uint32_t table_lanes, const uint64
             if (i < L) lane_first[i] = (uint32_t)(carry + ex);
             carry += tot;
         }
-        if (mybits) atomicOr(&s_bits, mybits);
-        atomicAdd((unsigned long long *)&s_len, (unsigned long long)lensum);
+        mybits = __reduce_or_sync(0xFFFFFFFFu, mybits);
+        if ((tid & 31) == 0 && mybits) atomicOr(&s_bits, mybits);
+        uint64_t lentot;
+        block_excl_sum<uint64_t>(lensum, sh, &lentot);
+        if (tid == 0) s_len = lentot;
         __syncthreads();
         if (tid == 0) lane_first[L] = (uint32_t)carry;
         R = *num_runs;
@@ -336,12 +339,21 @@ k_plan_decode(const uint32_t *__restrict__ lane_first, uint32_t L,
             an &= node;
         }
     }
-    // lanes with no valid item keep the identities
-    if (bits) atomicOr(&s_bits, bits);
-    atomicOr(&s_or, o);
-    atomicAnd(&s_and, a);
-    atomicOr(&s_orn, on);
-    atomicAnd(&s_andn, an);
+    // lanes with no valid item keep the identities; one shared atomic per warp
+    bits = __reduce_or_sync(0xFFFFFFFFu, bits);
+    on = __reduce_or_sync(0xFFFFFFFFu, on);
+    an = __reduce_and_sync(0xFFFFFFFFu, an);
+    const uint32_t o_lo = __reduce_or_sync(0xFFFFFFFFu, (uint32_t)o);
+    const uint32_t o_hi = __reduce_or_sync(0xFFFFFFFFu, (uint32_t)(o >> 32));
+    const uint32_t a_lo = __reduce_and_sync(0xFFFFFFFFu, (uint32_t)a);
+    const uint32_t a_hi = __reduce_and_sync(0xFFFFFFFFu, (uint32_t)(a >> 32));
+    if ((threadIdx.x & 31) == 0) {
+        if (bits) atomicOr(&s_bits, bits);
+        atomicOr(&s_or, ((unsigned long long)o_hi << 32) | o_lo);
+        atomicAnd(&s_and, ((unsigned long long)a_hi << 32) | a_lo);
+        atomicOr(&s_orn, on);
+        atomicAnd(&s_andn, an);
+    }
     Seg ex, tot;
     block_scan(agg, SegOp(), Seg{0, 0, 0}, sh, &ex, &tot);
     if (threadIdx.x == 0 && tile < nt) {
@@ -425,7 +437,17 @@ k_plan_keys(const uint32_t *__restrict__ lane_first, uint32_t L, uint32_t B,
             const uint64_t base = run_base[r];
             const uint32_t node = numa[l];
             items[r] = SortItem{base, node, (uint32_t)r};
-            if (nact) atomicAdd(&s_hist[digit_of(base, node, dig0)], 1u);
+        }
+    }
+    if (nact && tile < nt) {
+        // histogram of the first active digit, one shared atomic per distinct
+        // digit in each warp round
+        for (int j = 0; j < kIPT; j++) {
+            const uint64_t r = r0 + j;
+            const uint32_t d = r < R ? digit_of(run_base[r], numa[run_lane[r]], dig0) : kDigits;
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, d);
+            if (d < kDigits && (threadIdx.x & 31) == __ffs(peers) - 1)
+                atomicAdd(&s_hist[d], __popc(peers));
         }
     }
     if (bits) atomicOr(&s_bits, bits);

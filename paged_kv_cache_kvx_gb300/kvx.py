@@ -28,7 +28,7 @@ assert GROUP_DTYPE.itemsize == 48 and DESC_DTYPE.itemsize == 32
 
 KVX_OK, KVX_EINVAL, KVX_ECAPACITY, KVX_ECUDA = 0, 1, 3, 4
 S_LANES, S_ARRAYS, S_COVERAGE, S_ZERO_COUNT, S_ZERO_LEN = 1, 2, 4, 8, 16
-S_SPAN, S_STRIDE1, S_BOUNDS, S_DESC, S_CAPACITY = 32, 64, 128, 256, 512
+S_SPAN, S_STRIDE1, S_BOUNDS, S_DESC, S_CAPACITY, S_TIMEOUT = 32, 64, 128, 256, 512, 1024
 MAX_READ_BYTES = 32 * 1024 * 1024
 
 _ERR = {KVX_EINVAL: "KVX_EINVAL", KVX_ECAPACITY: "KVX_ECAPACITY", KVX_ECUDA: "KVX_ECUDA"}
