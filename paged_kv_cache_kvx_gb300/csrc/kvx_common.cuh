@@ -74,6 +74,68 @@ __device__ __forceinline__ bool last_block(uint32_t *ticket) {
     return s_last;
 }
 
+// Grid barrier for cooperative launches (every participating block is
+// resident).  Sense by generation: the last block to arrive resets the count
+// and bumps the generation; the others poll it.  The wait is bounded: after
+// kBarrierPolls polls (about half a second) a block gives up, raises the
+// shared abort flag and returns false, and so do the blocks still waiting.
+// With a single participating block it is a plain __syncthreads().
+struct GridSync {
+    uint32_t count;
+    uint32_t gen;
+    uint32_t abort;
+    uint32_t pad;
+};
+
+constexpr uint32_t kBarrierPolls = 1u << 22;
+
+__device__ __forceinline__ bool grid_barrier(GridSync *gs, uint32_t nblocks) {
+    __shared__ int s_ok;
+    if (nblocks <= 1) {
+        __syncthreads();
+        return true;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        volatile uint32_t *vgen = &gs->gen;
+        volatile uint32_t *vabort = &gs->abort;
+        const uint32_t g = *vgen;
+        __threadfence();
+        const uint32_t arrived = atomicAdd(&gs->count, 1u) + 1u;
+        if (arrived == nblocks) {
+            atomicExch(&gs->count, 0u);
+            __threadfence();
+            atomicAdd(&gs->gen, 1u);
+        } else {
+            for (uint32_t polls = 0; *vgen == g; polls++) {
+                if (*vabort || polls >= kBarrierPolls) {
+                    atomicExch(&gs->abort, 1u);
+                    ok = 0;
+                    break;
+                }
+                if (polls > 32) __nanosleep(100);
+            }
+        }
+        __threadfence();
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
+// Loads that bypass L1: data other blocks wrote earlier in the same kernel.
+template <class T>
+__device__ __forceinline__ T ld_cg(const T *p) {
+    static_assert(sizeof(T) % 8 == 0, "8-byte multiple");
+    T v;
+    const unsigned long long *src = reinterpret_cast<const unsigned long long *>(p);
+    unsigned long long *dst = reinterpret_cast<unsigned long long *>(&v);
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(T) / 8); i++) dst[i] = __ldcg(src + i);
+    return v;
+}
+
 // Warp-level inclusive scans.
 template <class T>
 __device__ __forceinline__ T warp_incl_sum(T v) {

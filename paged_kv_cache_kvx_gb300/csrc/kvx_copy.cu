@@ -4,15 +4,16 @@
 // holder-pool bytes into the dense slab; unpack is the inverse scatter.
 //
 // HBM-bound copy, no contraction.  The slab side is always contiguous (the
-// descriptors tile it), so the work is cut into fixed 32 KiB slab tiles.  A
+// descriptors tile it), so the work is cut into fixed 64 KiB slab tiles.  A
 // prep kernel checks the descriptors and sorts every tile into one of two
 // lists:
 //   - TMA jobs: tiles inside one 16-byte aligned descriptor (every tile of a
 //     dense 32 MiB read, most tiles of a 1 MiB per-block read).  One lane per
-//     SM streams them through a 6-stage shared-memory ring with bulk copies
+//     SM streams them through a 3-stage shared-memory ring with bulk copies
 //     (cp.async.bulk global->shared, completion on an mbarrier, then
 //     cp.async.bulk shared->global): the SM's bulk-copy unit moves the
-//     bytes, no register staging, up to 192 KiB of loads in flight per SM.
+//     bytes, no register staging, up to 192 KiB of loads in flight per SM (a
+//     sweep of 16-64 KiB tiles and 2-12 stages on GB300 put 3 x 64 KiB first).
 //   - vector tiles: tiles that hold several descriptors (4 KiB / 512 B
 //     segment reads) or unaligned ones.  256 threads per tile; the tile's
 //     descriptors are staged in shared memory and each 16-byte vector finds
@@ -26,10 +27,11 @@ namespace kvx {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr uint64_t kTileBytes = 32 * 1024;
-constexpr int kVecPerThread = (int)(kTileBytes / (kThreads * 16));  // 8
+constexpr uint64_t kTileBytes = 64 * 1024;
+constexpr int kVecPerThread = (int)(kTileBytes / (kThreads * 16));  // 16
 constexpr int kCtasPerSm = 3;
-constexpr int kStages = 6;                  // TMA ring depth per SM
+constexpr int kStages = 3;                  // TMA ring depth per CTA
+constexpr int kTmaCtasPerSm = 1;
 constexpr uint32_t kSpinLimit = 1u << 26;   // bounded mbarrier wait (seconds at most)
 
 struct CopyCtl {
@@ -209,7 +211,7 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // One warp per CTA, one CTA per SM; lane 0 drives the ring, the warp loads
 // job records 32 at a time.
 template <bool PACK>
-__global__ void __launch_bounds__(32, 1)
+__global__ void __launch_bounds__(32, kTmaCtasPerSm)
 k_copy_tma(const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r, uint8_t *slab_w,
            const TmaJob *__restrict__ jobs, const CopyCtl *ctl, uint32_t *status) {
     extern __shared__ __align__(128) uint8_t ring[];
@@ -420,9 +422,9 @@ kvx_status launch(bool pack, const uint8_t *pool_r, uint8_t *pool_w, const uint8
     KVX_LAUNCHED();
     const size_t smem = (size_t)kStages * kTileBytes;
     if (pack)
-        k_copy_tma<true><<<sms, 32, smem, s>>>(pool_r, pool_w, slab_r, slab_w, w.jobs, w.ctl, status);
+        k_copy_tma<true><<<sms * kTmaCtasPerSm, 32, smem, s>>>(pool_r, pool_w, slab_r, slab_w, w.jobs, w.ctl, status);
     else
-        k_copy_tma<false><<<sms, 32, smem, s>>>(pool_r, pool_w, slab_r, slab_w, w.jobs, w.ctl, status);
+        k_copy_tma<false><<<sms * kTmaCtasPerSm, 32, smem, s>>>(pool_r, pool_w, slab_r, slab_w, w.jobs, w.ctl, status);
     KVX_LAUNCHED();
     const uint32_t grid = (uint32_t)(sms * kCtasPerSm);
     if (pack)
