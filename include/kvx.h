@@ -256,6 +256,27 @@ kvx_status kvx_unpack(const uint8_t *slab, uint64_t slab_bytes,
                       uint64_t pool_bytes, uint32_t *status,
                       void *ws, size_t ws_bytes, void *stream);
 
+/*
+ * kvx_pack without a caller workspace, for callers that cannot allocate
+ * device memory (code where cudaMalloc is forbidden or would stall, such as
+ * an allocation-free serving loop, or a language binding with no device
+ * allocator).  The paper has no counterpart: it is a packaging variant of
+ * kvx_pack.  Same arguments and results as kvx_pack, minus ws / ws_bytes.
+ *
+ * Its scratch is a 4 MiB file-scope device array inside libkvx, held on
+ * every GPU that loads the library until the process exits.  That covers
+ * slabs up to 131,048 tiles of 64 KiB (about 8 GiB); a larger slab_bytes
+ * returns KVX_ECAPACITY and enqueues nothing.  The first call on a device
+ * looks up the array's device address (with that device current); make that
+ * first call before any stream capture.  Every call shares the array: calls
+ * that overlap on the GPU race and must be serialised by the caller.  The
+ * call allocates nothing and calls no allocating routine.
+ */
+kvx_status kvx_pack_noalloc(const uint8_t *pool, uint64_t pool_bytes,
+                            const kvx_desc *descs, const uint64_t *num_descs,
+                            uint64_t desc_capacity, uint8_t *slab, uint64_t slab_bytes,
+                            uint32_t *status, void *stream);
+
 /* ---------------------------------------------------------------- utility */
 
 /* Number of kernels this library has launched in this process. */

@@ -21,6 +21,8 @@
 //     unaligned).
 // Both copy kernels walk their list round-robin over a persistent grid, so
 // the grid streams one window of the slab at a time.
+#include <atomic>
+
 #include "kvx_common.cuh"
 
 namespace kvx {
@@ -464,4 +466,50 @@ extern "C" kvx_status kvx_unpack(const uint8_t *slab, uint64_t slab_bytes, const
                                  void *ws, size_t ws_bytes, void *stream) {
     return launch(false, nullptr, dst_pool, slab, nullptr, pool_bytes, slab_bytes, descs,
                   num_descs, desc_capacity, status, ws, ws_bytes, stream);
+}
+
+// ------------------------------------------------------------ no-allocation pack
+//
+// kvx_pack_noalloc: kvx_pack for callers that cannot allocate device memory
+// (for instance code running where cudaMalloc is forbidden or would stall:
+// an allocation-free serving loop, a host thread without its own allocator,
+// a binding to a language runtime that cannot hand out device buffers).  Its
+// scratch is this file-scope device array instead of a caller workspace.
+// Every GPU that loads the library holds the array until the process exits.
+// All calls share it, so calls that overlap on the GPU (two streams, or two
+// host threads) race on it and must be serialised by the caller; each call
+// clears the part that has to start at zero before using it.
+namespace {
+
+constexpr size_t kNoallocScratchBytes = (size_t)4 << 20;  // 4 MiB
+static __device__ __align__(256) unsigned char g_pack_scratch[kNoallocScratchBytes];
+
+// Device address of g_pack_scratch on the current device.  The name is only
+// a host-side stand-in, so the address is looked up once per device, with
+// that device current, on the first call there.
+void *pack_scratch_address() {
+    static std::atomic<void *> addr[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    void *p = addr[dev].load(std::memory_order_acquire);
+    if (p) return p;
+    if (cudaGetSymbolAddress(&p, g_pack_scratch) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    addr[dev].store(p, std::memory_order_release);
+    return p;
+}
+
+}  // namespace
+
+extern "C" kvx_status kvx_pack_noalloc(const uint8_t *pool, uint64_t pool_bytes,
+                                       const kvx_desc *descs, const uint64_t *num_descs,
+                                       uint64_t desc_capacity, uint8_t *slab, uint64_t slab_bytes,
+                                       uint32_t *status, void *stream) {
+    if (kvx_copy_workspace_size(slab_bytes) > kNoallocScratchBytes) return KVX_ECAPACITY;
+    void *scratch = pack_scratch_address();
+    if (!scratch) return KVX_ECUDA;
+    return launch(true, pool, nullptr, nullptr, slab, pool_bytes, slab_bytes, descs, num_descs,
+                  desc_capacity, status, scratch, kNoallocScratchBytes, stream);
 }

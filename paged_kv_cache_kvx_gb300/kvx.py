@@ -52,6 +52,7 @@ _SIGS = {
     "kvx_copy_workspace_size": (_SZ, [_U64]),
     "kvx_pack": (ctypes.c_int, [_P, _U64, _P, _P, _U64, _P, _U64, _P, _P, _SZ, _P]),
     "kvx_unpack": (ctypes.c_int, [_P, _U64, _P, _P, _U64, _P, _U64, _P, _P, _SZ, _P]),
+    "kvx_pack_noalloc": (ctypes.c_int, [_P, _U64, _P, _P, _U64, _P, _U64, _P, _P]),
     "kvx_launch_count": (_U64, []),
     "kvx_version": (_U32, []),
 }
@@ -164,6 +165,14 @@ def kvx_unpack(slab, slab_bytes, descs, num_descs, desc_capacity, dst_pool, pool
     _check(lib().kvx_unpack(_ptr(slab), slab_bytes, _ptr(descs), _ptr(num_descs), desc_capacity,
                             _ptr(dst_pool), pool_bytes, _ptr(status), _ptr(ws), ws.numel(),
                             _stream(stream)), "kvx_unpack")
+
+
+def kvx_pack_noalloc(pool, pool_bytes, descs, num_descs, desc_capacity, slab, slab_bytes, status,
+                     stream=None):
+    """kvx_pack with the library's own static scratch (no workspace argument)."""
+    _check(lib().kvx_pack_noalloc(_ptr(pool), pool_bytes, _ptr(descs), _ptr(num_descs),
+                                  desc_capacity, _ptr(slab), slab_bytes, _ptr(status),
+                                  _stream(stream)), "kvx_pack_noalloc")
 
 
 def kvx_launch_count() -> int:
