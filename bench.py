@@ -48,6 +48,23 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest of every rank's x (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def step_value(payload_bytes: int, steps: int, world: int, total_ms: float) -> float:
+    """Whole-job GB/s: every rank moves 4 N bytes per step (pack and unpack
+    each read and write N), over the slowest rank's time."""
+    return 4.0 * payload_bytes * steps * world / (total_ms / 1e3) / 1e9
+
+
 def load_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -293,10 +310,7 @@ def run_kvx(args):
     clocks = sampler.stop() if sampler else None
     total_ms = start.elapsed_time(end)
     stage = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(5)] for e in ev])  # ms
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, device=dev)
     assert tr.read_status() == 0
     assert torch.equal(pool, dst)
 
@@ -311,7 +325,7 @@ def run_kvx(args):
         return 0
     peak, peak_kind = load_peak()
     ms_step = total_ms / K
-    value = 4.0 * N * K * world / (total_ms / 1e3) / 1e9
+    value = step_value(N, K, world, total_ms)
     med = np.median(stage, axis=0)
     mean = stage.mean(axis=0)
     pack_gbs = 2.0 * N / (mean[3] / 1e3) / 1e9
