@@ -24,10 +24,10 @@
 // Runs are cut into tiles of 2048 (8 per thread of a 256-thread block); only
 // as many blocks as there are tiles take part, each owning tiles b, b+P, ...
 // A block gets the carry for its tile by an ordered reduction of the earlier
-// tiles' aggregates, so scans cost no extra barrier.  With one tile (up to
-// 2048 runs: every bump-allocated holder of up to 1024 slots) a single
-// block runs every phase and the barriers are __syncthreads().  Every read
-// of data another block wrote in this kernel bypasses L1.
+// tiles' aggregates, so scans cost no extra barrier.  Every read of data
+// another block wrote in this kernel bypasses L1.  Tables of up to 2048 runs
+// (every bump-allocated holder of up to 1024 slots) go to k_plan_small, one
+// block with the table in shared memory, and this kernel returns at once.
 #include "kvx_common.cuh"
 
 namespace kvx {
@@ -300,17 +300,40 @@ __device__ void phase_decode(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
     for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
         Seg agg{0, 0, 0};
         const uint64_t r0 = (uint64_t)tile * kTile + (uint64_t)threadIdx.x * kIPT;
+        // all loads of this thread's runs first, then the checks
+        uint32_t lanes[kIPT], cnts[kIPT], lens[kIPT], nodes[kIPT];
+        uint64_t bases[kIPT];
+        int64_t strides[kIPT];
+#pragma unroll
         for (int j = 0; j < kIPT; j++) {
             const uint64_t r = r0 + j;
-            if (r >= R) break;
-            const uint32_t l = lf_smem ? lane_of([&](uint32_t i) { return s_lf[i]; }, L, r)
-                                       : lane_of([&](uint32_t i) { return __ldcg(a.lane_first + i); }, L, r);
+            lanes[j] = 0;
+            if (r < R) {
+                lanes[j] = lf_smem ? lane_of([&](uint32_t i) { return s_lf[i]; }, L, r)
+                                   : lane_of([&](uint32_t i) { return __ldcg(a.lane_first + i); }, L, r);
+                bases[j] = a.run_base[r];
+                strides[j] = a.run_stride[r];
+                cnts[j] = a.run_count[r];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kIPT; j++) {
+            if (r0 + j < R) {
+                lens[j] = __ldg(a.seg_len + lanes[j]);
+                nodes[j] = __ldg(a.numa + lanes[j]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kIPT; j++) {
+            const uint64_t r = r0 + j;
+            if (r >= R) continue;
+            const uint32_t l = lanes[j];
             a.run_lane[r] = l;
-            const uint64_t base = a.run_base[r];
-            const int64_t stride = a.run_stride[r];
-            const uint32_t cnt = a.run_count[r];
-            const uint32_t len = a.seg_len[l];
-            const uint32_t node = a.numa[l];
+            const uint64_t base = bases[j];
+            const int64_t stride = strides[j];
+            const uint32_t cnt = cnts[j];
+            const uint32_t len = lens[j];
+            const uint32_t node = nodes[j];
             if (cnt == 0) bits |= KVX_S_ZERO_COUNT;
             if (cnt == 1 && stride != 0) bits |= KVX_S_STRIDE1;
             if (cnt >= 1) {
@@ -384,16 +407,25 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
         const Seg carry = reduce_prefix(a.seg, tile, SegOp(), Seg{0, 0, 0}, sm.seg);
         const uint64_t r0 = (uint64_t)tile * kTile + (uint64_t)threadIdx.x * kIPT;
         Seg agg{0, 0, 0};
-        uint32_t cnts[kIPT];
-        uint32_t lanes[kIPT];
+        uint32_t cnts[kIPT], lanes[kIPT], nodes[kIPT];
+        uint64_t bases[kIPT];
         uint32_t heads = 0;
+#pragma unroll
         for (int j = 0; j < kIPT; j++) {
             const uint64_t r = r0 + j;
             cnts[j] = 0;
             lanes[j] = 0;
+            if (r < R) {
+                lanes[j] = __ldcg(a.run_lane + r);
+                cnts[j] = a.run_count[r];
+                bases[j] = a.run_base[r];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kIPT; j++) {
+            const uint64_t r = r0 + j;
             if (r >= R) continue;
-            lanes[j] = __ldcg(a.run_lane + r);
-            cnts[j] = a.run_count[r];
+            nodes[j] = __ldg(a.numa + lanes[j]);
             const bool head = r == (lf_smem ? s_lf[lanes[j]] : __ldcg(a.lane_first + lanes[j]));
             if (head) heads |= 1u << j;
             agg = SegOp()(agg, Seg{cnts[j], head ? 1u : 0u, 0});
@@ -401,23 +433,25 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
         Seg ex, tot;
         block_scan(agg, SegOp(), Seg{0, 0, 0}, sm.seg, &ex, &tot);
         uint64_t blk = SegOp()(carry, ex).sum;  // blocks before this thread's first run
+#pragma unroll
         for (int j = 0; j < kIPT; j++) {
             const uint64_t r = r0 + j;
-            if (r >= R) break;
+            if (r >= R) continue;
             if (heads >> j & 1u) blk = 0;
             const uint32_t l = lanes[j];
             a.run_block[r] = (uint32_t)blk;
             blk += cnts[j];
             const uint32_t next_first = lf_smem ? s_lf[l + 1] : __ldcg(a.lane_first + l + 1);
             if (r + 1 == (uint64_t)next_first && blk != a.B) bits |= KVX_S_COVERAGE;
-            a.items0[r] = SortItem{a.run_base[r], a.numa[l], (uint32_t)r};
+            a.items0[r] = SortItem{bases[j], nodes[j], (uint32_t)r};
         }
         if (nact) {
             // histogram of the first active digit; one shared atomic per distinct
             // digit in each warp round
+#pragma unroll
             for (int j = 0; j < kIPT; j++) {
                 const uint64_t r = r0 + j;
-                const uint32_t d = r < R ? digit_of(a.run_base[r], a.numa[lanes[j]], dig0) : kDigits;
+                const uint32_t d = r < R ? digit_of(bases[j], nodes[j], dig0) : kDigits;
                 const uint32_t peers = __match_any_sync(0xFFFFFFFFu, d);
                 if (d < kDigits && (threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1))
                     atomicAdd(&s_hist[d], __popc(peers));
@@ -533,13 +567,18 @@ __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint
             __syncthreads();
 #pragma unroll
             for (int j = 0; j < kIPT; j++) {
-                if (d[j] >= kDigits) continue;
-                const uint64_t dst = (uint64_t)s_base[d[j]] + s_off[slot][d[j]] + wcnt[w][d[j]] + pos[j];
-                if (dst >= R) continue;  // never taken: the offsets are a permutation of [0, R)
-                out[dst] = it[j];
-                if (has_next) {
-                    const uint32_t nd = digit_of(it[j].base, it[j].node, ndig);
-                    atomicAdd(&Hn[(uint64_t)(dst / kTile) * kDigits + nd], 1u);
+                uint64_t key = ~0ull;  // next-histogram bin of this item
+                if (d[j] < kDigits) {
+                    const uint64_t dst = (uint64_t)s_base[d[j]] + s_off[slot][d[j]] + wcnt[w][d[j]] + pos[j];
+                    if (dst < R) {  // always: the offsets are a permutation of [0, R)
+                        out[dst] = it[j];
+                        if (has_next)
+                            key = (dst / kTile) * kDigits + digit_of(it[j].base, it[j].node, ndig);
+                    }
+                }
+                if (has_next) {  // one atomic per distinct bin in the warp
+                    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, key);
+                    if (key != ~0ull && lane == (uint32_t)(__ffs(peers) - 1)) atomicAdd(&Hn[key], __popc(peers));
                 }
             }
             __syncthreads();
@@ -575,12 +614,40 @@ __device__ void phase_adjacent(const PlanArgs &a, uint64_t R, uint32_t nt, uint3
         }
         SortItem its[kIPT];
 #pragma unroll
+        for (int j = 0; j < kIPT; j++) {
+            its[j].r = 0;
+            if (p0 + j < R) {
+                its[j] = ld_cg(sorted + p0 + j);
+                if (its[j].r >= R) its[j].r = 0;  // never taken: a permutation of the runs
+            }
+        }
+        int64_t strides[kIPT];
+        uint32_t counts[kIPT], blocks[kIPT], lanes[kIPT], lens[kIPT];
+#pragma unroll
+        for (int j = 0; j < kIPT; j++) {
+            if (p0 + j >= R) continue;
+            const uint32_t r = its[j].r;
+            strides[j] = a.run_stride[r];
+            counts[j] = a.run_count[r];
+            blocks[j] = __ldcg(a.run_block + r);
+            lanes[j] = __ldcg(a.run_lane + r);
+        }
+#pragma unroll
         for (int j = 0; j < kIPT; j++)
-            if (p0 + j < R) its[j] = ld_cg(sorted + p0 + j);
+            if (p0 + j < R) lens[j] = __ldg(a.seg_len + lanes[j]);
+#pragma unroll
         for (int j = 0; j < kIPT; j++) {
             const uint64_t p = p0 + j;
-            if (p >= R) break;
-            const Rec x = make_rec(a, its[j], R);
+            if (p >= R) continue;
+            Rec x;
+            x.base = its[j].base;
+            x.node = its[j].node;
+            x.r = its[j].r;
+            x.stride = strides[j];
+            x.count = counts[j];
+            x.block = blocks[j];
+            x.len = lens[j];
+            x.pad = 0;
             a.rec[p] = x;
             const bool c = have_prev && compatible(prev, x);
             a.compat[p] = c ? 1 : 0;
@@ -778,12 +845,464 @@ __device__ void on_abort(const PlanArgs &a) {
         }                                        \
     } while (0)
 
-__global__ void __launch_bounds__(kT) k_plan(const __grid_constant__ PlanArgs a) {
+
+// ------------------------------------------------- single-block planner
+//
+// Tables of up to 2048 runs (every bump-allocated holder with up to 1024
+// slots) are planned by one block of 1024 threads, 2 runs each, with the
+// whole run table in shared memory: the same steps as the phases above, each
+// a few shared-memory passes and warp-shuffle scans instead of global round
+// trips.  The cooperative kernel returns at once for these tables.
+constexpr uint32_t kSmallRuns = 2048;
+constexpr int kST = 1024;
+constexpr int kSW = kST / 32;
+
+__device__ __forceinline__ bool plan_is_small(const PlanArgs &a, uint64_t R) {
+    return R <= kSmallRuns && R <= a.run_cap && a.table_lanes == a.template_lanes &&
+           a.table_lanes + 1 <= kLaneSmem;
+}
+
+struct SmallSmem {
+    uint64_t base[kSmallRuns];
+    int64_t stride[kSmallRuns];
+    uint32_t lf[kLaneSmem];
+    uint32_t count[kSmallRuns];
+    uint32_t lane[kSmallRuns];
+    uint32_t block[kSmallRuns];
+    uint32_t node[kSmallRuns];
+    uint32_t len[kSmallRuns];
+    uint16_t idx[2][kSmallRuns];
+    uint16_t wcnt[kSW][kDigits];
+    uint32_t dbase[kDigits];
+    uint8_t flag[kSmallRuns + 1];
+    uint8_t compat[kSmallRuns];
+};
+
+template <class T>
+__device__ __forceinline__ T shfl_up_any(T v, int d) {
+    static_assert(sizeof(T) % 4 == 0, "4-byte multiple");
+    T o;
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(&v);
+    uint32_t *dst = reinterpret_cast<uint32_t *>(&o);
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(T) / 4); i++) dst[i] = __shfl_up_sync(0xFFFFFFFFu, src[i], d);
+    return o;
+}
+
+// Block-wide inclusive scan (1024 threads), warp shuffles + one warp over the
+// warp totals.  *excl / *total as in block_scan.
+template <class T, class Op>
+__device__ T small_scan(T v, Op op, T identity, T *wtot, T *excl, T *total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    T x = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const T o = shfl_up_any(x, d);
+        if (lane >= d) x = op(o, x);
+    }
+    __syncthreads();
+    if (lane == 31) wtot[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        T t = wtot[lane];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const T o = shfl_up_any(t, d);
+            if (lane >= d) t = op(o, t);
+        }
+        wtot[lane] = t;
+    }
+    __syncthreads();
+    const T before = w > 0 ? wtot[w - 1] : identity;
+    const T incl = op(before, x);
+    const T ex_in_warp = shfl_up_any(x, 1);
+    *excl = lane > 0 ? op(before, ex_in_warp) : before;
+    *total = wtot[kSW - 1];
+    __syncthreads();
+    return incl;
+}
+
+struct SumOp64 {
+    __device__ uint64_t operator()(uint64_t a, uint64_t b) const { return a + b; }
+};
+struct MaxOp32 {
+    __device__ int32_t operator()(int32_t a, int32_t b) const { return a > b ? a : b; }
+};
+
+__global__ void __launch_bounds__(kST, 1) k_plan_small(const __grid_constant__ PlanArgs a) {
+    extern __shared__ __align__(16) unsigned char sraw[];
+    SmallSmem &S = *reinterpret_cast<SmallSmem *>(sraw);
+    __shared__ uint64_t w64[kSW];
+    __shared__ Seg wseg[kSW];
+    __shared__ int32_t w32[kSW];
+    __shared__ CAgg wc[kSW];
+    __shared__ uint32_t s_bits;
+    __shared__ unsigned long long s_or, s_and;
+    __shared__ uint32_t s_orn, s_andn;
+    const uint64_t R = *a.num_runs;
+    if (!plan_is_small(a, R)) return;
+    const uint32_t tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const uint32_t L = a.table_lanes;
+    if (tid == 0) {
+        s_bits = 0;
+        s_or = 0;
+        s_and = ~0ull;
+        s_orn = 0;
+        s_andn = ~0u;
+        a.counts[0] = a.counts[1] = a.counts[2] = 0;
+    }
+    __syncthreads();
+
+    // ---- step 1, table level: lane_first, zero-size slots, empty lanes
+    uint64_t carry = 0, lensum = 0;
+    uint32_t bits = 0;
+    for (uint32_t b0 = 0; b0 < L; b0 += kST) {
+        const uint32_t i = b0 + tid;
+        uint64_t v = 0;
+        if (i < L) {
+            v = a.rpl[i];
+            const uint32_t len = a.seg_len[i];
+            if (len == 0) bits |= KVX_S_ZERO_LEN;
+            if (v == 0 && a.B > 0) bits |= KVX_S_COVERAGE;
+            lensum += len;
+        }
+        uint64_t ex, tot;
+        small_scan(v, SumOp64(), (uint64_t)0, w64, &ex, &tot);
+        if (i < L) {
+            S.lf[i] = (uint32_t)(carry + ex);
+            a.lane_first[i] = (uint32_t)(carry + ex);
+        }
+        carry += tot;
+    }
+    {
+        uint64_t ex, lentot;
+        small_scan(lensum, SumOp64(), (uint64_t)0, w64, &ex, &lentot);
+        if (tid == 0) {
+            S.lf[L] = (uint32_t)carry;
+            a.lane_first[L] = (uint32_t)carry;
+        }
+        bits = __reduce_or_sync(0xFFFFFFFFu, bits);
+        if (lane == 0 && bits) atomicOr(&s_bits, bits);
+        __syncthreads();
+        uint32_t st = s_bits;
+        bool stop = false;
+        if (carry != R) {
+            st |= KVX_S_ARRAYS;
+            stop = true;
+        } else if ((unsigned __int128)a.B * (unsigned __int128)lentot >= ((unsigned __int128)1 << 63)) {
+            st |= KVX_S_CAPACITY;
+            stop = true;
+        }
+        if (stop) {
+            if (tid == 0) atomicOr(a.status, st);
+            return;
+        }
+    }
+    __syncthreads();
+
+    // ---- step 1 per run + step 2 decode (runs 2*tid, 2*tid + 1)
+    const uint32_t r0 = 2 * tid;
+    bits = 0;
+    unsigned long long o = 0, an = ~0ull;
+    uint32_t on = 0, ann = ~0u;
+    Seg agg{0, 0, 0};
+#pragma unroll
+    for (int j = 0; j < 2; j++) {
+        const uint32_t r = r0 + j;
+        if (r >= R) continue;
+        uint32_t lo = 0, hi = L;  // lane: largest l with lf[l] <= r
+        while (hi - lo > 1) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (S.lf[mid] <= r) lo = mid; else hi = mid;
+        }
+        const uint32_t l = lo;
+        const uint64_t base = a.run_base[r];
+        const int64_t stride = a.run_stride[r];
+        const uint32_t cnt = a.run_count[r];
+        const uint32_t len = __ldg(a.seg_len + l);
+        const uint32_t node = __ldg(a.numa + l);
+        S.base[r] = base;
+        S.stride[r] = stride;
+        S.count[r] = cnt;
+        S.lane[r] = l;
+        S.len[r] = len;
+        S.node[r] = node;
+        if (cnt == 0) bits |= KVX_S_ZERO_COUNT;
+        if (cnt == 1 && stride != 0) bits |= KVX_S_STRIDE1;
+        if (cnt >= 1) {
+            const __int128 first = (__int128)base;
+            const __int128 last = first + (__int128)(cnt - 1) * (__int128)stride;
+            const __int128 hi2 = last > first ? last : first;
+            if (last < 0 || hi2 + (__int128)len > (__int128)a.pool_bytes) bits |= KVX_S_SPAN;
+        }
+        agg = SegOp()(agg, Seg{cnt, r == S.lf[l] ? 1u : 0u, 0});
+        o |= base;
+        an &= base;
+        on |= node;
+        ann &= node;
+    }
+    {
+        Seg ex, tot;
+        small_scan(agg, SegOp(), Seg{0, 0, 0}, wseg, &ex, &tot);
+        uint64_t blk = ex.sum;
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            const uint32_t r = r0 + j;
+            if (r >= R) continue;
+            const uint32_t l = S.lane[r];
+            if (r == S.lf[l]) blk = 0;
+            S.block[r] = (uint32_t)blk;
+            a.run_block[r] = (uint32_t)blk;
+            blk += S.count[r];
+            if (r + 1 == S.lf[l + 1] && blk != a.B) bits |= KVX_S_COVERAGE;
+        }
+    }
+    bits = __reduce_or_sync(0xFFFFFFFFu, bits);
+    on = __reduce_or_sync(0xFFFFFFFFu, on);
+    ann = __reduce_and_sync(0xFFFFFFFFu, ann);
+    {
+        const uint32_t o_lo = __reduce_or_sync(0xFFFFFFFFu, (uint32_t)o);
+        const uint32_t o_hi = __reduce_or_sync(0xFFFFFFFFu, (uint32_t)(o >> 32));
+        const uint32_t a_lo = __reduce_and_sync(0xFFFFFFFFu, (uint32_t)an);
+        const uint32_t a_hi = __reduce_and_sync(0xFFFFFFFFu, (uint32_t)(an >> 32));
+        if (lane == 0) {
+            if (bits) atomicOr(&s_bits, bits);
+            atomicOr(&s_or, ((unsigned long long)o_hi << 32) | o_lo);
+            atomicAnd(&s_and, ((unsigned long long)a_hi << 32) | a_lo);
+            atomicOr(&s_orn, on);
+            atomicAnd(&s_andn, ann);
+        }
+    }
+    __syncthreads();
+    if (s_bits) {
+        if (tid == 0) atomicOr(a.status, s_bits);
+        return;
+    }
+
+    // ---- step 2: stable LSD radix sort of run indices on (node, base)
+    uint32_t act[12], nact = 0;
+    if (R > 1) {
+        const unsigned long long db = s_or ^ s_and;
+        const uint32_t dn = s_orn ^ s_andn;
+        for (uint32_t d = 0; d < 8; d++)
+            if ((db >> (8 * d)) & 0xFFu) act[nact++] = d;
+        for (uint32_t d = 0; d < 4; d++)
+            if ((dn >> (8 * d)) & 0xFFu) act[nact++] = 8 + d;
+    }
+    for (uint32_t r = tid; r < R; r += kST) S.idx[0][r] = (uint16_t)r;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (uint32_t k = 0; k < nact; k++) {
+        const uint16_t *in = S.idx[k & 1];
+        uint16_t *out = S.idx[(k + 1) & 1];
+        const uint32_t dig = act[k];
+        for (uint32_t i = tid; i < kSW * kDigits; i += kST) (&S.wcnt[0][0])[i] = 0;
+        __syncthreads();
+        uint32_t item[2], d[2], pos[2];
+#pragma unroll
+        for (int j = 0; j < 2; j++) {  // warp-contiguous: position w*64 + j*32 + lane
+            const uint32_t p = w * 64 + j * 32 + lane;
+            d[j] = kDigits;
+            item[j] = 0;
+            if (p < R) {
+                item[j] = in[p];
+                d[j] = digit_of(S.base[item[j]], S.node[item[j]], dig);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, d[j]);
+            const uint32_t rank = __popc(peers & lt_mask);
+            const uint32_t before = d[j] < kDigits ? S.wcnt[w][d[j]] : 0;
+            __syncwarp();
+            if (d[j] < kDigits && rank == 0) S.wcnt[w][d[j]] = (uint16_t)(before + __popc(peers));
+            __syncwarp();
+            pos[j] = before + rank;
+        }
+        __syncthreads();
+        uint64_t dtot = 0;
+        if (tid < kDigits) {
+            uint32_t acc = 0;
+            for (int ww = 0; ww < kSW; ww++) {
+                const uint32_t c = S.wcnt[ww][tid];
+                S.wcnt[ww][tid] = (uint16_t)acc;
+                acc += c;
+            }
+            dtot = acc;
+        }
+        {
+            uint64_t ex, tot;
+            small_scan(dtot, SumOp64(), (uint64_t)0, w64, &ex, &tot);
+            if (tid < kDigits) S.dbase[tid] = (uint32_t)ex;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            if (d[j] >= kDigits) continue;
+            const uint32_t dst = S.dbase[d[j]] + S.wcnt[w][d[j]] + pos[j];
+            if (dst < R) out[dst] = (uint16_t)item[j];  // always: a permutation
+        }
+        __syncthreads();
+    }
+    const uint16_t *sorted = S.idx[nact & 1];
+
+    // ---- step 3: compat, stretch starts, group starts (positions 2*tid, +1)
+    int32_t mx = -1;
+#pragma unroll
+    for (int j = 0; j < 2; j++) {
+        const uint32_t p = r0 + j;
+        if (p >= R) continue;
+        bool c = false;
+        if (p > 0) {
+            const uint32_t x = sorted[p], y = sorted[p - 1];
+            c = S.node[x] == S.node[y] && S.block[x] == S.block[y] && S.count[x] == S.count[y] &&
+                S.stride[x] == S.stride[y] && S.base[x] == S.base[y] + S.len[y];
+        }
+        S.compat[p] = c ? 1 : 0;
+        if (!c) mx = (int32_t)p;
+    }
+    {
+        int32_t ex, tot;
+        small_scan(mx, MaxOp32(), (int32_t)-1, w32, &ex, &tot);
+        int32_t st = ex;  // stretch start before this thread's first position
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            const uint32_t p = r0 + j;
+            if (p >= R) continue;
+            const bool c = S.compat[p] != 0;
+            if (!c) st = (int32_t)p;
+            const uint32_t x = sorted[p];
+            const uint32_t cnt = S.count[x];
+            const int64_t stride = S.stride[x];
+            if (cnt == 1) {
+                S.flag[p] = c ? 0 : 1;
+                continue;
+            }
+            if (stride <= 0) {
+                S.flag[p] = 1;  // a non-positive stride never fits: one run per group
+                continue;
+            }
+            const uint64_t ustride = (uint64_t)stride;
+            const uint64_t O = S.base[x] - S.base[sorted[st > 0 ? st : 0]];
+            const uint64_t E = O + S.len[x];
+            if (E <= ustride) {
+                S.flag[p] = c ? 0 : 1;
+            } else if (O <= ustride) {
+                // first run that outgrows the stretch's first group: walk the rest
+                S.flag[p] = 1;
+                uint64_t cur = S.base[x];
+                for (uint32_t q = p + 1; q < R && S.compat[q]; q++) {
+                    const uint32_t y = sorted[q];
+                    if (S.base[y] + S.len[y] - cur > ustride) {
+                        S.flag[q] = 1;
+                        cur = S.base[y];
+                    } else {
+                        S.flag[q] = 0;
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- group numbering, records, carve and reads
+    uint64_t gcount = 0;
+    int32_t glast = -1;
+#pragma unroll
+    for (int j = 0; j < 2; j++) {
+        const uint32_t p = r0 + j;
+        if (p < R && S.flag[p]) {
+            gcount++;
+            glast = (int32_t)p;
+        }
+    }
+    uint64_t gex, gtot;
+    small_scan(gcount, SumOp64(), (uint64_t)0, w64, &gex, &gtot);
+    int32_t lex, ltot;
+    small_scan(glast, MaxOp32(), (int32_t)-1, w32, &lex, &ltot);
+    if (gtot > a.group_cap) {
+        if (tid == 0) atomicOr(a.status, KVX_S_CAPACITY);
+        return;
+    }
+    uint64_t gid_run = gex;
+    int32_t gs = lex;
+    kvx_group G[2];
+    bool is_end[2] = {false, false};
+    uint32_t gids[2] = {0, 0};
+    CAgg c{0, 0};
+#pragma unroll
+    for (int j = 0; j < 2; j++) {
+        const uint32_t p = r0 + j;
+        if (p >= R) continue;
+        if (S.flag[p]) {
+            gid_run++;
+            gs = (int32_t)p;
+        }
+        const uint32_t gid = (uint32_t)(gid_run - 1);
+        const uint32_t x = sorted[p];
+        const uint32_t x0 = sorted[gs > 0 ? gs : 0];
+        const uint64_t off = S.base[x] - S.base[x0];
+        a.run_group[x] = gid;
+        a.run_off[x] = off;
+        gids[j] = gid;
+        if (p + 1 == R || S.flag[p + 1]) {
+            is_end[j] = true;
+            kvx_group &g = G[j];
+            g.base = S.base[x0];
+            g.stride = S.stride[x0];
+            g.chunk = off + S.len[x];
+            g.local = 0;
+            g.block = S.block[x0];
+            g.count = S.count[x0];
+            g.node = S.node[x0];
+            g.dense = group_dense(g.count, g.stride, g.chunk) ? 1u : 0u;
+            c.bytes += (uint64_t)g.count * g.chunk;
+            c.descs += group_pieces(g);
+        }
+    }
+    CAgg cex, ctot;
+    small_scan(c, COp(), CAgg{0, 0}, wc, &cex, &ctot);
+    if (ctot.descs > a.desc_cap) {
+        if (tid == 0) atomicOr(a.status, KVX_S_CAPACITY);
+        return;
+    }
+    CAgg cur = cex;
+    const uint64_t M = KVX_MAX_READ_BYTES;
+#pragma unroll
+    for (int j = 0; j < 2; j++) {
+        if (!is_end[j]) continue;
+        kvx_group g = G[j];
+        g.local = cur.bytes;
+        a.groups[gids[j]] = g;
+        uint64_t dd = cur.descs;
+        if (g.dense) {
+            const uint64_t total = (uint64_t)g.count * g.chunk;
+            for (uint64_t off = 0; off < total; off += M, dd++)
+                a.descs[dd] = kvx_desc{g.base + off, g.local + off, total - off < M ? total - off : M, gids[j], 0};
+        } else {
+            for (uint64_t i = 0; i < g.count; i++) {
+                const uint64_t rb = g.base + i * (uint64_t)g.stride;
+                const uint64_t lb = g.local + i * g.chunk;
+                for (uint64_t off = 0; off < g.chunk; off += M, dd++)
+                    a.descs[dd] = kvx_desc{rb + off, lb + off, g.chunk - off < M ? g.chunk - off : M, gids[j], 0};
+            }
+        }
+        cur.bytes += (uint64_t)g.count * g.chunk;
+        cur.descs += group_pieces(g);
+    }
+    if (tid == 0) {
+        a.counts[0] = gtot;
+        a.counts[1] = ctot.descs;
+        a.counts[2] = ctot.bytes;
+    }
+}
+
+__global__ void __launch_bounds__(kT, 2) k_plan(const __grid_constant__ PlanArgs a) {
     __shared__ ScanSmem sm;
     __shared__ uint32_t s_act[12];
     __shared__ uint32_t s_nact;
     __shared__ uint32_t s_lf[kLaneSmem];
     const uint64_t R_in = *a.num_runs;
+    if (plan_is_small(a, R_in)) return;  // planned by k_plan_small
     const uint64_t R = R_in <= a.run_cap ? R_in : 0;
     const uint32_t nt = (uint32_t)ceil_div(R, kTile);
     const uint32_t P = nt < gridDim.x ? (nt ? nt : 1) : gridDim.x;
@@ -969,6 +1488,18 @@ extern "C" kvx_status kvx_plan_groups(const uint32_t *runs_per_lane, uint32_t ta
     a.segmax = w.segmax;
     a.gagg = w.gagg;
     a.cagg = w.cagg;
+    static bool small_ready[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return KVX_ECUDA;
+    if (!small_ready[dev]) {
+        if (cudaFuncSetAttribute(k_plan_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)sizeof(SmallSmem)) != cudaSuccess)
+            return KVX_ECUDA;
+        small_ready[dev] = true;
+    }
+    k_plan_small<<<1, kST, sizeof(SmallSmem), s>>>(a);
+    KVX_LAUNCHED();
     if (cudaMemsetAsync(w.ctl, 0, sizeof(PlanCtl), s) != cudaSuccess) return KVX_ECUDA;
     const uint64_t ntc = ceil_div(run_capacity ? run_capacity : 1, kTile);
     const int maxb = plan_max_blocks();

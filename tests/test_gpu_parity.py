@@ -107,9 +107,59 @@ def _gpu_plan_table(B, seg_len, numa, pool, rpl, base, stride, count, num_runs=N
     return tr
 
 
+def _validation_cases_match(B, seg_len0, numa, pool0, t):
+    """Corrupt the table one class at a time; the CUDA planner must report
+    exactly the oracle's status bits and plan nothing."""
+    cases = [("ok", dict()), ("arrays", dict(num_runs=t.num_runs - 1))]
+    c = t.run_count.copy(); c[2] = 7
+    cases.append(("coverage", dict(count=c)))
+    c = t.run_count.copy(); c[1] = 0
+    cases.append(("zero_count", dict(count=c)))
+    sl = seg_len0.copy(); sl[2] = 0
+    cases.append(("zero_len", dict(seg_len=sl)))
+    cases.append(("span_pool", dict(pool=pool0 - 1)))
+    st = t.run_stride.copy(); st[0] = 2**62
+    cases.append(("span_wrap", dict(stride=st)))
+    st = t.run_stride.copy(); st[3] = -(2**50)
+    cases.append(("span_negative", dict(stride=st)))
+    c = t.run_count.copy(); c[0] = 0
+    cases.append(("several", dict(count=c, seg_len=sl, pool=10)))
+    for name, kw in cases:
+        seg_len = kw.get("seg_len", seg_len0)
+        pool = kw.get("pool", pool0)
+        table = oracle.RunTable(t.runs_per_lane, t.run_base, kw.get("stride", t.run_stride),
+                                kw.get("count", t.run_count))
+        p = oracle.plan(table, B, seg_len, numa, pool, num_runs=kw.get("num_runs"))
+        tr = _gpu_plan_table(B, seg_len, numa, pool, table.runs_per_lane, table.run_base,
+                             table.run_stride, table.run_count, num_runs=kw.get("num_runs"))
+        assert tr.read_status() == p.status, name
+        assert tr.read_counts() == (p.groups.size, p.descs.size, p.slab_bytes), name
+        if p.status == 0:
+            assert_plan_equal(tr, p)
+    tr = _gpu_plan_table(B, seg_len0, numa, pool0, t.runs_per_lane, t.run_base, t.run_stride,
+                         t.run_count, table_lanes=seg_len0.size - 1)
+    assert tr.read_status() == kvx.S_LANES and tr.read_counts() == (0, 0, 0)
+    tr = _gpu_plan_table(B, seg_len0, numa, pool0, t.runs_per_lane, t.run_base, t.run_stride,
+                         t.run_count, group_cap=1)
+    assert tr.read_status() == kvx.S_CAPACITY and tr.read_counts() == (0, 0, 0)
+    tr = _gpu_plan_table(B, seg_len0, numa, pool0, t.runs_per_lane, t.run_base, t.run_stride,
+                         t.run_count, desc_cap=1)
+    assert tr.read_status() == kvx.S_CAPACITY and tr.read_counts() == (0, 0, 0)
+
+
+def test_validation_status_matches_oracle_multi_tile():
+    """The same corruptions on a 3000-run table (the multi-block planner)."""
+    rng = np.random.default_rng(31)
+    addr, seg_len, numa, pool = random_lanes(rng, 300, 20)
+    t = oracle.encode_runs(addr)
+    assert t.num_runs > 2048
+    _validation_cases_match(300, seg_len, numa, pool, t)
+
+
 def test_validation_status_matches_oracle():
     wl = W.tiny()
     t = oracle.encode_runs(wl.addr)
+    _validation_cases_match(wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes, t)
     cases = []
     cases.append(("ok", dict()))
     cases.append(("arrays", dict(num_runs=t.num_runs - 1)))
