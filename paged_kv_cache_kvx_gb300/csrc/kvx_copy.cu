@@ -12,8 +12,11 @@
 //     SM streams them through a 3-stage shared-memory ring with bulk copies
 //     (cp.async.bulk global->shared, completion on an mbarrier, then
 //     cp.async.bulk shared->global): the SM's bulk-copy unit moves the
-//     bytes, no register staging, up to 192 KiB of loads in flight per SM (a
-//     sweep of 16-64 KiB tiles and 2-12 stages on GB300 put 3 x 64 KiB first).
+//     bytes, no register staging, up to 192 KiB of loads in flight per SM.
+//     Rings claim their jobs dynamically, so the copy ends when the bytes
+//     are done rather than when the slowest ring is.  Sweeps on GB300 (16-96
+//     KiB tiles, 2-12 stages, 38-304 rings, static or claimed work, claims of
+//     1-8 jobs) put one ring per SM, 3 x 64 KiB, claims of 2 first.
 //   - vector tiles: tiles that hold several descriptors (4 KiB / 512 B
 //     segment reads) or unaligned ones.  256 threads per tile; the tile's
 //     descriptors are staged in shared memory and each 16-byte vector finds
@@ -41,7 +44,7 @@ struct CopyCtl {
     uint32_t bad;             // descriptors do not tile the slab
     uint32_t n_tma;           // TMA jobs
     uint32_t n_vec;           // vector tiles
-    uint32_t pad;
+    uint32_t next_job;        // next unclaimed TMA job
 };
 
 struct TmaJob {
@@ -210,76 +213,92 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// One warp per CTA, one CTA per SM; lane 0 drives the ring, the warp loads
-// job records 32 at a time.
+// One warp per CTA, one CTA per SM; lane 0 drives the ring.  Jobs are handed
+// out dynamically: a ring claims kGrab consecutive jobs at a time from an
+// atomic counter (the warp loads their records, one per lane) and claims its
+// next batch while it works through the current one, so a ring that happens
+// to sit on a busier part of the chip simply takes fewer tiles and the copy
+// ends when the bytes are done, not when the slowest ring is.
+constexpr uint32_t kGrab = 2;
+
+struct Grab {
+    uint32_t pos, n;  // warp-uniform
+    TmaJob rec;       // lane j holds job j of the batch
+};
+
 template <bool PACK>
 __global__ void __launch_bounds__(32, kTmaCtasPerSm)
 k_copy_tma(const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r, uint8_t *slab_w,
-           const TmaJob *__restrict__ jobs, const CopyCtl *ctl, uint32_t *status) {
+           const TmaJob *__restrict__ jobs, CopyCtl *ctl, uint32_t *status) {
     extern __shared__ __align__(128) uint8_t ring[];
     __shared__ __align__(8) uint64_t bars[kStages];
     const uint32_t lane = threadIdx.x;
     if (ctl->bad) return;
     const uint32_t n = ctl->n_tma;
-    const uint32_t G = gridDim.x;
-    const uint32_t count = n > blockIdx.x ? (n - blockIdx.x + G - 1) / G : 0;
-    if (count == 0) return;
+    if (n == 0) return;
     if (lane == 0) {
         for (int s = 0; s < kStages; s++) mbar_init(&bars[s], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
+    auto claim = [&](Grab &g) {
+        uint32_t b = 0;
+        if (lane == 0) b = atomicAdd(&ctl->next_job, kGrab);
+        b = __shfl_sync(0xFFFFFFFFu, b, 0);
+        g.pos = 0;
+        g.n = b < n ? (n - b < kGrab ? n - b : kGrab) : 0;
+        if (lane < g.n) g.rec = jobs[b + lane];
+    };
+    Grab cur, nxt;
+    claim(cur);
+    claim(nxt);
     uint8_t *dst_ring[kStages];
     uint32_t len_ring[kStages];
     bool ok = true;
-    TmaJob mine{};  // job (base + lane) of the current batch of 32
-    uint32_t batch = ~0u;
-    uint32_t issued = 0;  // loads issued
-    uint32_t landed = 0;  // loads whose barrier completed (in order)
-    for (uint32_t i = 0; i < count + kStages - 1 && ok; i++) {
-        if (i < count) {
-            const uint32_t b = i / 32;
-            if (b != batch) {
-                batch = b;
-                const uint32_t j = b * 32 + lane;
-                if (j < count) mine = jobs[blockIdx.x + (uint64_t)j * G];
-            }
-            const uint32_t src_lane = i % 32;
-            const uint64_t lo = __shfl_sync(0xFFFFFFFFu, mine.lo, src_lane);
-            const uint64_t delta = __shfl_sync(0xFFFFFFFFu, mine.delta, src_lane);
-            const uint32_t len = __shfl_sync(0xFFFFFFFFu, mine.len, src_lane);
-            if (lane == 0) {
-                const int s = i % kStages;
-                if (i >= kStages) bulk_wait_read_all();  // buffer s: store i-kStages done reading
-                const uint8_t *src = PACK ? pool_r + lo + delta : slab_r + lo;
-                dst_ring[s] = PACK ? slab_w + lo : pool_w + lo + delta;
-                len_ring[s] = len;
-                mbar_arrive_expect_tx(&bars[s], len);
-                bulk_g2s(ring + (uint64_t)s * kTileBytes, src, len, &bars[s]);
-                issued++;
-            }
+    uint32_t issued = 0, stored = 0;  // loads issued, tiles stored (uniform)
+    for (;;) {
+        if (cur.pos == cur.n && cur.n != 0) {
+            cur = nxt;
+            claim(nxt);
         }
-        if (lane == 0 && i >= kStages - 1) {
-            const uint32_t k = i - (kStages - 1);
-            if (k < count) {
-                const int s = k % kStages;
-                if (!mbar_wait(&bars[s], (k / kStages) & 1u)) {
+        const bool have = cur.pos < cur.n;
+        if (stored < issued && (issued - stored == (uint32_t)kStages || !have)) {
+            if (lane == 0) {
+                const int s = stored % kStages;
+                if (!mbar_wait(&bars[s], (stored / kStages) & 1u)) {
                     ok = false;
                 } else {
-                    landed = k + 1;
                     bulk_s2g(dst_ring[s], ring + (uint64_t)s * kTileBytes, len_ring[s]);
                     bulk_commit();
                 }
             }
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) break;
+            stored++;
+            continue;
         }
-        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!have) break;  // every job claimed and stored
+        const uint64_t lo = __shfl_sync(0xFFFFFFFFu, cur.rec.lo, cur.pos);
+        const uint64_t delta = __shfl_sync(0xFFFFFFFFu, cur.rec.delta, cur.pos);
+        const uint32_t len = __shfl_sync(0xFFFFFFFFu, cur.rec.len, cur.pos);
+        cur.pos++;
+        if (lane == 0) {
+            const int s = issued % kStages;
+            if (issued >= (uint32_t)kStages) bulk_wait_read_all();  // store issued-kStages read its buffer
+            const uint8_t *src = PACK ? pool_r + lo + delta : slab_r + lo;
+            dst_ring[s] = PACK ? slab_w + lo : pool_w + lo + delta;
+            len_ring[s] = len;
+            mbar_arrive_expect_tx(&bars[s], len);
+            bulk_g2s(ring + (uint64_t)s * kTileBytes, src, len, &bars[s]);
+        }
+        issued++;
     }
     if (lane == 0) {
         if (!ok) {
             atomicOr(status, KVX_S_TIMEOUT);
             // let the loads still in flight (at most kStages) land before the
             // ring is released; each barrier has one use outstanding
-            for (uint32_t k = landed; k < issued; k++) mbar_wait(&bars[k % kStages], (k / kStages) & 1u);
+            for (uint32_t k = stored; k < issued; k++) mbar_wait(&bars[k % kStages], (k / kStages) & 1u);
         }
         bulk_wait_all();
     }
