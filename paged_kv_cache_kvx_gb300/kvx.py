@@ -265,13 +265,27 @@ class Transfer:
         kvx_unpack(slab, slab.numel(), self.descs, self.counts[1:], self.desc_cap, dst_pool,
                    dst_pool.numel(), self.status, self.copy_ws, stream)
 
-    def step(self, pool, slab, dst_pool, stream=None):
-        """One pass of the whole path: encode, plan, rebuild, pack, unpack."""
-        self.encode(stream=stream)
-        self.plan(stream=stream)
-        self.rebuild(stream=stream)
-        self.pack(pool, slab, stream=stream)
-        self.unpack(slab, dst_pool, stream=stream)
+    def step(self, pool, slab, dst_pool, stream=None, side=None):
+        """One pass of the whole path: encode, plan, rebuild, pack, unpack.
+        With a side stream, rebuild (which needs only the plan) runs there
+        alongside pack and joins before the step ends."""
+        main = torch.cuda.current_stream(self.device) if stream is None else stream
+        self.encode(stream=main)
+        self.plan(stream=main)
+        if side is None:
+            self.rebuild(stream=main)
+            self.pack(pool, slab, stream=main)
+            self.unpack(slab, dst_pool, stream=main)
+            return
+        planned = torch.cuda.Event()
+        planned.record(main)
+        side.wait_event(planned)
+        self.rebuild(stream=side)
+        rebuilt = torch.cuda.Event()
+        rebuilt.record(side)
+        self.pack(pool, slab, stream=main)
+        self.unpack(slab, dst_pool, stream=main)
+        main.wait_event(rebuilt)
 
     def set_addr(self, addr_np: np.ndarray):
         a = np.ascontiguousarray(addr_np, dtype=np.uint64).reshape(-1)
