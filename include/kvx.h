@@ -277,6 +277,16 @@ kvx_status kvx_pack_noalloc(const uint8_t *pool, uint64_t pool_bytes,
                             uint64_t desc_capacity, uint8_t *slab, uint64_t slab_bytes,
                             uint32_t *status, void *stream);
 
+/*
+ * Diagnostic, no counterpart in the paper: shows that the library's bounded
+ * waits give up instead of hanging.  Launches a grid barrier that waits for
+ * one block more than is launched and an mbarrier wait for bytes no copy
+ * will deliver; each polls to its limit (about one second), then ORs
+ * KVX_S_TIMEOUT into *status (device word) and returns.  Nothing is copied
+ * and nothing faults.
+ */
+kvx_status kvx_selftest_timeouts(uint32_t *status, void *stream);
+
 /* ---------------------------------------------------------------- utility */
 
 /* Number of kernels this library has launched in this process. */

@@ -77,8 +77,8 @@ __device__ __forceinline__ bool last_block(uint32_t *ticket) {
 // Grid barrier for cooperative launches (every participating block is
 // resident).  Sense by generation: the last block to arrive resets the count
 // and bumps the generation; the others poll it.  The wait is bounded: after
-// kBarrierPolls polls (about half a second) a block gives up, raises the
-// shared abort flag and returns false, and so do the blocks still waiting.
+// about a second a block gives up, raises the shared abort flag and returns
+// false, and so do the blocks still waiting.
 // With a single participating block it is a plain __syncthreads().
 struct GridSync {
     uint32_t count;
@@ -87,7 +87,16 @@ struct GridSync {
     uint32_t pad;
 };
 
-constexpr uint32_t kBarrierPolls = 1u << 22;
+// Waits are bounded in time (%globaltimer nanoseconds) with a poll-count
+// backstop.
+constexpr uint64_t kWaitNs = 1000000000ull;  // one second
+constexpr uint32_t kBarrierPolls = 1u << 26;
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 __device__ __forceinline__ bool grid_barrier(GridSync *gs, uint32_t nblocks) {
     __shared__ int s_ok;
@@ -108,8 +117,9 @@ __device__ __forceinline__ bool grid_barrier(GridSync *gs, uint32_t nblocks) {
             __threadfence();
             atomicAdd(&gs->gen, 1u);
         } else {
+            const uint64_t t0 = global_ns();
             for (uint32_t polls = 0; *vgen == g; polls++) {
-                if (*vabort || polls >= kBarrierPolls) {
+                if (*vabort || polls >= kBarrierPolls || global_ns() - t0 > kWaitNs) {
                     atomicExch(&gs->abort, 1u);
                     ok = 0;
                     break;
@@ -240,5 +250,66 @@ __device__ inline uint32_t block_scan_inplace_span_u32(uint32_t *a, uint64_t n) 
     __syncthreads();
     return (uint32_t)tot;
 }
+
+// ------------------------------------------------- mbarrier and bulk copies
+
+constexpr uint32_t kSpinLimit = 1u << 28;  // backstop; the time bound ends waits first
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: false after about a second (try_wait itself may suspend the
+// thread for a while, so the bound is time, not a poll count).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0; i < kSpinLimit; i++) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitNs) return false;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void bulk_g2s(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(sdst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_s2g(void *gdst, const void *ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+                 "r"(smem_u32(ssrc)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 }  // namespace kvx

@@ -53,6 +53,7 @@ _SIGS = {
     "kvx_pack": (ctypes.c_int, [_P, _U64, _P, _P, _U64, _P, _U64, _P, _P, _SZ, _P]),
     "kvx_unpack": (ctypes.c_int, [_P, _U64, _P, _P, _U64, _P, _U64, _P, _P, _SZ, _P]),
     "kvx_pack_noalloc": (ctypes.c_int, [_P, _U64, _P, _P, _U64, _P, _U64, _P, _P]),
+    "kvx_selftest_timeouts": (ctypes.c_int, [_P, _P]),
     "kvx_launch_count": (_U64, []),
     "kvx_version": (_U32, []),
 }
@@ -173,6 +174,10 @@ def kvx_pack_noalloc(pool, pool_bytes, descs, num_descs, desc_capacity, slab, sl
     _check(lib().kvx_pack_noalloc(_ptr(pool), pool_bytes, _ptr(descs), _ptr(num_descs),
                                   desc_capacity, _ptr(slab), slab_bytes, _ptr(status),
                                   _stream(stream)), "kvx_pack_noalloc")
+
+
+def kvx_selftest_timeouts(status, stream=None):
+    _check(lib().kvx_selftest_timeouts(_ptr(status), _stream(stream)), "kvx_selftest_timeouts")
 
 
 def kvx_launch_count() -> int:

@@ -1,0 +1,82 @@
+"""Bounded waits, graph capture of the whole path, and byte-exact slabs at
+full size where the plan maps remote offsets 1:1 onto slab offsets."""
+import time
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_kvx_gb300 import kvx, workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def test_bounded_waits_report_a_timeout():
+    """A grid barrier and an mbarrier that nothing will release give up
+    within seconds and say so; the context stays usable afterwards."""
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.time()
+    kvx.kvx_selftest_timeouts(status)
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 30
+    assert int(status.item()) == kvx.S_TIMEOUT
+    x = torch.arange(10, device="cuda")
+    assert int(x.sum().item()) == 45
+
+
+def test_captured_step_replays_bit_exact():
+    """One step captured as a CUDA graph (counts stay on the device) replays
+    to the same plan and the same bytes as the step launched call by call;
+    rebuild on a side stream joins before the step ends."""
+    wl = W.worst(blocks=61, slots=18, npos=128, seed=3)
+    tr = kvx.Transfer(wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
+    tr.set_addr(wl.addr)
+    pool = torch.empty(wl.pool_bytes, dtype=torch.uint8, device="cuda")
+    W.fill_pool_torch(pool, wl.seed)
+    slab = torch.empty(tr.slab_bytes, dtype=torch.uint8, device="cuda")
+    dst = torch.full((wl.pool_bytes,), W.CANARY, dtype=torch.uint8, device="cuda")
+    tr.step(pool, slab, dst)
+    torch.cuda.synchronize()
+    assert tr.read_status() == 0
+    want_plan = tr.read_plan()
+    want_local = tr.read_local()
+    want_slab = slab.clone()
+    want_dst = dst.clone()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    slab.zero_()
+    dst.fill_(W.CANARY)
+    tr.local.zero_()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        tr.step(pool, slab, dst, side=side)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert tr.read_status() == 0
+    got = tr.read_plan()
+    for k in ("groups", "descs"):
+        assert got[k].tobytes() == want_plan[k].tobytes()
+    assert np.array_equal(tr.read_local(), want_local)
+    assert torch.equal(slab, want_slab) and torch.equal(dst, want_dst)
+
+
+@pytest.mark.parametrize("name", ["default", "wide64k"])
+def test_identity_plans_copy_every_byte(name):
+    """Bump-allocated holders: every dense group's slab offset equals its
+    remote base, so the whole slab must equal the pool byte for byte."""
+    wl = W.CONFIGS[name]()
+    tr = kvx.Transfer(wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
+    tr.set_addr(wl.addr)
+    pool = torch.empty(wl.pool_bytes, dtype=torch.uint8, device="cuda")
+    W.fill_pool_torch(pool, wl.seed)
+    slab = torch.zeros(tr.slab_bytes, dtype=torch.uint8, device="cuda")
+    tr.encode()
+    tr.plan()
+    tr.pack(pool, slab)
+    torch.cuda.synchronize()
+    plan = tr.read_plan()
+    assert tr.read_status() == 0
+    assert np.array_equal(plan["groups"]["local"], plan["groups"]["base"])
+    assert tr.slab_bytes == wl.pool_bytes
+    assert torch.equal(slab, pool)
