@@ -33,10 +33,12 @@
  *   - Data-dependent problems are OR-ed as KVX_S_* bits into the caller's
  *     device word `status` (never cleared by the library; the caller zeroes it
  *     and reads it after synchronising).  A nonzero status means the outputs
- *     of that call are undefined, except as stated per call.  No call traps,
- *     asserts or waits on another thread block: bad input cannot hang or
- *     fault the GPU; every global access is checked against the capacities
- *     passed in.
+ *     of that call are undefined, except as stated per call.  No call traps
+ *     or asserts.  Thread blocks wait on one another only at the grid
+ *     barriers of cooperative launches (encode, plan), each bounded by one
+ *     second of wall time, after which the kernel ORs KVX_S_TIMEOUT and
+ *     returns: bad input cannot hang or fault the GPU; every global access
+ *     is checked against the capacities passed in.
  *   - Outputs must not alias inputs.
  *
  * Layouts: the address table and the rebuilt local pointers are block-major,
@@ -129,14 +131,18 @@ size_t kvx_encode_workspace_size(uint32_t B, uint32_t L);
  *                  difference), blocks covered.
  *   run_capacity   must be >= kvx_run_capacity(B, L) (else KVX_ECAPACITY).
  *   num_runs       [1] out: total runs R (device).
+ *   status         [1] device word; encoding cannot fail on data, so the
+ *                  only bit it can OR in is KVX_S_TIMEOUT (a grid barrier
+ *                  of the one cooperative launch waited more than a
+ *                  second; the run table is then invalid).
  *   ws, ws_bytes   scratch, >= kvx_encode_workspace_size(B, L).
- * Encoding cannot fail on data; it writes no status.
  */
 kvx_status kvx_encode_runs(const uint64_t *addr, uint32_t B, uint32_t L,
                            uint32_t *runs_per_lane, uint64_t *run_base,
                            int64_t *run_stride, uint32_t *run_count,
                            uint64_t run_capacity, uint64_t *num_runs,
-                           void *ws, size_t ws_bytes, void *stream);
+                           uint32_t *status, void *ws, size_t ws_bytes,
+                           void *stream);
 
 /* ------------------------------------------------------------------ plan */
 

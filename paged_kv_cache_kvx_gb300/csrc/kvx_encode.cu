@@ -11,6 +11,14 @@
 // (entry state, runs before, last start before), and an emit pass writes
 // each run at its lane-major index.
 //
+// One cooperative kernel, four phases separated by bounded grid barriers:
+//   1. per tile (32 lanes x 8K blocks): the tile's effect on each lane;
+//   2. one warp per lane: a warp-shuffle scan of its tiles' effects gives
+//      every tile's entry prefix and the lane's run count;
+//   3. one warp per 32-lane tile: the tile's run total;
+//   4. per tile: lane offsets (totals of earlier lane tiles plus a warp
+//      scan), then every thread re-walks its slice from its entry prefix
+//      and writes its runs.
 // Thread layout: a CTA is 8 warps; lane t of warp w handles table lane
 // l0 + t over blocks [tile_b0 + w*K, +K), so every warp load is one
 // coalesced 256-byte row segment of the block-major table.
@@ -39,15 +47,21 @@ __device__ __forceinline__ Xfer xfer_identity() {
     return x;
 }
 
+// Entry e of a two-entry field, by select (keeps Xfer in registers).
+__device__ __forceinline__ uint32_t pick(const uint32_t (&v)[2], uint32_t e) {
+    return e ? v[1] : v[0];
+}
+
 // a then b
 __device__ __forceinline__ Xfer xfer_then(const Xfer &a, const Xfer &b) {
     Xfer c;
 #pragma unroll
     for (int e = 0; e < 2; e++) {
         const uint32_t e1 = a.fin[e];
-        c.cnt[e] = a.cnt[e] + b.cnt[e1];
-        c.last[e] = b.last[e1] != kNone ? b.last[e1] : a.last[e];
-        c.fin[e] = b.fin[e1];
+        const uint32_t bl = pick(b.last, e1);
+        c.cnt[e] = a.cnt[e] + pick(b.cnt, e1);
+        c.last[e] = bl != kNone ? bl : a.last[e];
+        c.fin[e] = pick(b.fin, e1);
     }
     return c;
 }
@@ -62,14 +76,15 @@ struct Prefix {
 
 __device__ __forceinline__ Prefix prefix_then(const Prefix &p, const Xfer &x) {
     Prefix q;
-    q.state = x.fin[p.state];
-    q.runs = p.runs + x.cnt[p.state];
-    q.prev = x.last[p.state] != kNone ? x.last[p.state] : p.prev;
+    const uint32_t xl = pick(x.last, p.state);
+    q.state = pick(x.fin, p.state);
+    q.runs = p.runs + pick(x.cnt, p.state);
+    q.prev = xl != kNone ? xl : p.prev;
     return q;
 }
 
 // Per-lane tile records in the workspace: first the tile's Xfer, then (after
-// the last block's scan) the tile's entry Prefix.
+// the per-lane scan) the tile's entry Prefix.
 struct TileRec {
     uint32_t a, b, c, d;
 };
@@ -89,7 +104,7 @@ __device__ __forceinline__ Xfer unpack_xfer(const TileRec &t) {
 }
 
 struct EncodeCtl {
-    uint32_t ticket;
+    GridSync gs;
 };
 
 __device__ __forceinline__ uint64_t ld_addr(const uint64_t *addr, uint64_t b, uint32_t L, uint32_t l) {
@@ -146,7 +161,7 @@ Geometry geometry(uint32_t B, uint32_t L) {
 struct Ws {
     EncodeCtl *ctl;
     TileRec *tiles;       // [ntr][L]
-    uint64_t *lane_base;  // [L]
+    uint64_t *tile_runs;  // [ntl]
 };
 
 Ws carve(void *base, uint32_t B, uint32_t L, size_t *bytes) {
@@ -155,128 +170,223 @@ Ws carve(void *base, uint32_t B, uint32_t L, size_t *bytes) {
     Ws w;
     w.ctl = c.take<EncodeCtl>(1);
     w.tiles = c.take<TileRec>((size_t)g.ntr * L);
-    w.lane_base = c.take<uint64_t>(L);
+    w.tile_runs = c.take<uint64_t>(g.ntl);
     *bytes = c.off;
     return w;
 }
 
-// Pass 1: per-(tile, lane) Xfer; the last block scans tiles per lane into
-// entry prefixes, writes runs_per_lane, scans lanes into run offsets.
-__global__ void __launch_bounds__(kThreads)
-k_encode_tiles(const uint64_t *__restrict__ addr, uint32_t B, uint32_t L, Geometry g,
-               TileRec *__restrict__ tiles, uint64_t *__restrict__ lane_base,
-               uint32_t *__restrict__ runs_per_lane, uint64_t *__restrict__ num_runs,
-               EncodeCtl *ctl) {
-    __shared__ Xfer sx[kRows][32];
-    const uint32_t tl = blockIdx.x % g.ntl, tr = blockIdx.x / g.ntl;
-    const uint32_t t = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const uint32_t l = tl * 32 + t;
-    const uint64_t tb0 = (uint64_t)tr * kRows * g.K;
-    const uint64_t b0 = tb0 + (uint64_t)w * g.K;
-    const uint64_t b1 = b0 + g.K < B ? b0 + g.K : B;
-    Xfer x = xfer_identity();
-    if (l < L && b0 < B) x = slice_xfer(addr, L, l, b0, b1);
-    sx[w][t] = x;
-    __syncthreads();
-    if (w == 0 && l < L) {
-        Xfer acc = sx[0][t];
-        for (int r = 1; r < kRows; r++) acc = xfer_then(acc, sx[r][t]);
-        tiles[(uint64_t)tr * L + l] = pack_xfer(acc);
-    }
-    if (!last_block(&ctl->ticket)) return;
-
-    // Last block: per lane, tiles in order -> entry prefixes.  Records are
-    // loaded in batches before they are combined and overwritten, so the
-    // loads of a batch are in flight together.
-    constexpr uint32_t kBatch = 8;
-    for (uint32_t lane = threadIdx.x; lane < L; lane += blockDim.x) {
-        Prefix p{0u, 0u, kNone};
-        for (uint32_t r0 = 0; r0 < g.ntr; r0 += kBatch) {
-            uint4 v[kBatch];
+__device__ __forceinline__ Xfer shfl_up_xfer(const Xfer &v, int d) {
+    Xfer o;
 #pragma unroll
-            for (uint32_t j = 0; j < kBatch; j++)
-                if (r0 + j < g.ntr)
-                    v[j] = __ldcg(reinterpret_cast<const uint4 *>(tiles + (uint64_t)(r0 + j) * L + lane));
-#pragma unroll
-            for (uint32_t j = 0; j < kBatch; j++) {
-                if (r0 + j >= g.ntr) break;
-                const Xfer xr = unpack_xfer(TileRec{v[j].x, v[j].y, v[j].z, v[j].w});
-                tiles[(uint64_t)(r0 + j) * L + lane] = TileRec{p.state, p.runs, p.prev, 0u};
-                p = prefix_then(p, xr);
-            }
-        }
-        runs_per_lane[lane] = p.runs;
-        lane_base[lane] = p.runs;
+    for (int e = 0; e < 2; e++) {
+        o.cnt[e] = __shfl_up_sync(0xFFFFFFFFu, v.cnt[e], d);
+        o.last[e] = __shfl_up_sync(0xFFFFFFFFu, v.last[e], d);
+        o.fin[e] = __shfl_up_sync(0xFFFFFFFFu, v.fin[e], d);
     }
-    __syncthreads();
-    const uint64_t total = block_scan_inplace_u64(lane_base, L);
-    if (threadIdx.x == 0) *num_runs = total;
+    return o;
 }
 
-// Pass 2: recompute each thread's slice, resolve its entry prefix from the
-// tile prefix, and write the runs that start inside the slice.  The count of
-// a run is written by the thread that meets the next start (or the lane's
-// end).
-__global__ void __launch_bounds__(kThreads)
-k_encode_emit(const uint64_t *__restrict__ addr, uint32_t B, uint32_t L, Geometry g,
-              const TileRec *__restrict__ tiles, const uint64_t *__restrict__ lane_base,
-              uint64_t *__restrict__ run_base, int64_t *__restrict__ run_stride,
-              uint32_t *__restrict__ run_count, uint64_t run_cap) {
+__device__ __forceinline__ Xfer shfl_xfer(const Xfer &v, int src) {
+    Xfer o;
+#pragma unroll
+    for (int e = 0; e < 2; e++) {
+        o.cnt[e] = __shfl_sync(0xFFFFFFFFu, v.cnt[e], src);
+        o.last[e] = __shfl_sync(0xFFFFFFFFu, v.last[e], src);
+        o.fin[e] = __shfl_sync(0xFFFFFFFFu, v.fin[e], src);
+    }
+    return o;
+}
+
+// Sum of v[0..n) by the whole block (every thread gets the result).
+__device__ uint64_t block_sum_tiles(const uint64_t *v, uint32_t n, uint64_t *s_red) {
+    const uint32_t t = threadIdx.x & 31, w = threadIdx.x >> 5;
+    uint64_t sum = 0;
+    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) sum += __ldcg(v + i);
+    for (int d = 16; d > 0; d >>= 1) sum += __shfl_down_sync(0xFFFFFFFFu, sum, d);
+    __syncthreads();  // s_red may still be read from the previous call
+    if (t == 0) s_red[w] = sum;
+    __syncthreads();
+    uint64_t tot = 0;
+    for (int i = 0; i < kRows; i++) tot += s_red[i];
+    return tot;
+}
+
+struct EncodeArgs {
+    const uint64_t *addr;
+    uint32_t B, L;
+    Geometry g;
+    TileRec *tiles;
+    uint32_t *runs_per_lane;
+    uint64_t *tile_runs;
+    uint64_t *num_runs;
+    uint64_t *run_base;
+    int64_t *run_stride;
+    uint32_t *run_count;
+    uint64_t run_cap;
+    EncodeCtl *ctl;
+    uint32_t *status;
+};
+
+__global__ void __launch_bounds__(kThreads) k_encode(const __grid_constant__ EncodeArgs a) {
     __shared__ Xfer sx[kRows][32];
     __shared__ Prefix sp[kRows][32];
-    const uint32_t tl = blockIdx.x % g.ntl, tr = blockIdx.x / g.ntl;
+    __shared__ uint64_t s_lb[32];
+    __shared__ uint64_t s_red[kRows];
+    const uint32_t B = a.B, L = a.L;
+    const Geometry g = a.g;
     const uint32_t t = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const uint32_t l = tl * 32 + t;
-    const uint64_t tb0 = (uint64_t)tr * kRows * g.K;
-    const uint64_t b0 = tb0 + (uint64_t)w * g.K;
-    const uint64_t b1 = b0 + g.K < B ? b0 + g.K : B;
-    const bool active = l < L && b0 < B;
-    sx[w][t] = active ? slice_xfer(addr, L, l, b0, b1) : xfer_identity();
-    __syncthreads();
-    if (w == 0 && l < L) {
-        const TileRec tp = tiles[(uint64_t)tr * L + l];
-        Prefix p{tp.a, tp.b, tp.c};
-        for (int r = 0; r < kRows; r++) {
-            sp[r][t] = p;
-            p = prefix_then(p, sx[r][t]);
-        }
-    }
-    __syncthreads();
-    if (!active) return;
+    const uint32_t ntiles = g.ntl * g.ntr;
+    const uint32_t G = gridDim.x;
 
-    Prefix p = sp[w][t];
-    const uint64_t lb = lane_base[l];
-    uint64_t p2 = b0 >= 2 ? ld_addr(addr, b0 - 2, L, l) : 0;
-    uint64_t p1 = b0 >= 1 ? ld_addr(addr, b0 - 1, L, l) : 0;
-    uint64_t a = ld_addr(addr, b0, L, l);
-    uint32_t s = p.state;
-    uint32_t runs = p.runs;
-    uint32_t prev = p.prev;
-    for (uint64_t i = b0; i < b1; i++) {
-        const uint64_t nx = i + 1 < B ? ld_addr(addr, i + 1, L, l) : 0;
-        uint32_t n;
-        if (i == 0)
-            n = 0;
-        else if (i == 1 || a - p1 == p1 - p2)
-            n = 1;
-        else
-            n = s ^ 1u;
-        if (n == 0) {
-            const uint64_t idx = lb + runs;
-            if (idx < run_cap) {  // always true: runs per lane <= ceil(B/2)
-                run_base[idx] = a;
-                run_stride[idx] = i + 1 < B ? (int64_t)(nx - a) : 0;
-            }
-            if (prev != kNone && idx - 1 < run_cap) run_count[idx - 1] = (uint32_t)(i - prev);
-            prev = (uint32_t)i;
-            runs++;
+    // ---- phase 1: each tile's effect on each of its lanes
+    for (uint32_t tile = blockIdx.x; tile < ntiles; tile += G) {
+        const uint32_t tl = tile % g.ntl, tr = tile / g.ntl;
+        const uint32_t l = tl * 32 + t;
+        const uint64_t b0 = (uint64_t)tr * kRows * g.K + (uint64_t)w * g.K;
+        const uint64_t b1 = b0 + g.K < B ? b0 + g.K : B;
+        sx[w][t] = (l < L && b0 < B) ? slice_xfer(a.addr, L, l, b0, b1) : xfer_identity();
+        __syncthreads();
+        if (w == 0 && l < L) {
+            Xfer acc = sx[0][t];
+            for (int r = 1; r < kRows; r++) acc = xfer_then(acc, sx[r][t]);
+            a.tiles[(uint64_t)tr * L + l] = pack_xfer(acc);
         }
-        s = n;
-        p2 = p1;
-        p1 = a;
-        a = nx;
+        __syncthreads();
     }
-    if (b1 == B && lb + runs - 1 < run_cap) run_count[lb + runs - 1] = (uint32_t)(B - prev);
+    if (!grid_barrier(&a.ctl->gs, G)) {
+        if (threadIdx.x == 0) atomicOr(a.status, KVX_S_TIMEOUT);
+        return;
+    }
+
+    // ---- phase 2: one warp per lane, warp-shuffle scan over its tiles
+    for (uint32_t l = blockIdx.x * kRows + w; l < L; l += G * kRows) {
+        Prefix carry{0u, 0u, kNone};
+        for (uint32_t c0 = 0; c0 < g.ntr; c0 += 32) {
+            const uint32_t r = c0 + t;
+            TileRec* slot = a.tiles + (uint64_t)r * L + l;
+            Xfer x = xfer_identity();
+            if (r < g.ntr) {
+                const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(slot));
+                x = unpack_xfer(TileRec{v.x, v.y, v.z, v.w});
+            }
+            Xfer incl = x;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const Xfer o = shfl_up_xfer(incl, d);
+                if ((int)t >= d) incl = xfer_then(o, incl);
+            }
+            Xfer excl = shfl_up_xfer(incl, 1);
+            if (t == 0) excl = xfer_identity();
+            const Prefix mine = prefix_then(carry, excl);
+            if (r < g.ntr) *slot = TileRec{mine.state, mine.runs, mine.prev, 0u};
+            carry = prefix_then(carry, shfl_xfer(incl, 31));
+        }
+        if (t == 0) a.runs_per_lane[l] = carry.runs;
+    }
+    if (!grid_barrier(&a.ctl->gs, G)) {
+        if (threadIdx.x == 0) atomicOr(a.status, KVX_S_TIMEOUT);
+        return;
+    }
+
+    // ---- phase 3: runs of each 32-lane tile, one warp per lane tile
+    for (uint32_t tl = blockIdx.x * kRows + w; tl < g.ntl; tl += G * kRows) {
+        const uint32_t l = tl * 32 + t;
+        uint64_t v = l < L ? __ldcg(a.runs_per_lane + l) : 0;
+        for (int d = 16; d > 0; d >>= 1) v += __shfl_down_sync(0xFFFFFFFFu, v, d);
+        if (t == 0) a.tile_runs[tl] = v;
+    }
+    if (!grid_barrier(&a.ctl->gs, G)) {
+        if (threadIdx.x == 0) atomicOr(a.status, KVX_S_TIMEOUT);
+        return;
+    }
+
+    // ---- phase 4: lane offsets, then every slice writes its runs
+    if (blockIdx.x == 0) {  // total runs
+        const uint64_t tot = block_sum_tiles(a.tile_runs, g.ntl, s_red);
+        if (threadIdx.x == 0) *a.num_runs = tot;
+    }
+    for (uint32_t tile = blockIdx.x; tile < ntiles; tile += G) {
+        const uint32_t tl = tile % g.ntl, tr = tile / g.ntl;
+        const uint32_t l0 = tl * 32, l = l0 + t;
+        {   // runs of every lane tile before tl, then a warp scan over the tile's lanes
+            const uint64_t base0 = block_sum_tiles(a.tile_runs, tl, s_red);
+            if (w == 0) {
+                const uint64_t mine = l < L ? __ldcg(a.runs_per_lane + l) : 0;
+                uint64_t incl = mine;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const uint64_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                    if ((int)t >= d) incl += o;
+                }
+                s_lb[t] = base0 + incl - mine;
+            }
+        }
+        const uint64_t b0 = (uint64_t)tr * kRows * g.K + (uint64_t)w * g.K;
+        const uint64_t b1 = b0 + g.K < B ? b0 + g.K : B;
+        const bool active = l < L && b0 < B;
+        sx[w][t] = active ? slice_xfer(a.addr, L, l, b0, b1) : xfer_identity();
+        __syncthreads();
+        if (w == 0 && l < L) {
+            const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(a.tiles + (uint64_t)tr * L + l));
+            Prefix p{v.x, v.y, v.z};
+            for (int r = 0; r < kRows; r++) {
+                sp[r][t] = p;
+                p = prefix_then(p, sx[r][t]);
+            }
+        }
+        __syncthreads();
+        if (active) {
+            const Prefix p = sp[w][t];
+            const uint64_t lb = s_lb[t];
+            uint64_t p2 = b0 >= 2 ? ld_addr(a.addr, b0 - 2, L, l) : 0;
+            uint64_t p1 = b0 >= 1 ? ld_addr(a.addr, b0 - 1, L, l) : 0;
+            uint64_t av = ld_addr(a.addr, b0, L, l);
+            uint32_t s = p.state;
+            uint32_t runs = p.runs;
+            uint32_t prev = p.prev;
+            for (uint64_t i = b0; i < b1; i++) {
+                const uint64_t nx = i + 1 < B ? ld_addr(a.addr, i + 1, L, l) : 0;
+                uint32_t n;
+                if (i == 0)
+                    n = 0;
+                else if (i == 1 || av - p1 == p1 - p2)
+                    n = 1;
+                else
+                    n = s ^ 1u;
+                if (n == 0) {
+                    const uint64_t idx = lb + runs;
+                    if (idx < a.run_cap) {  // always true: runs per lane <= ceil(B/2)
+                        a.run_base[idx] = av;
+                        a.run_stride[idx] = i + 1 < B ? (int64_t)(nx - av) : 0;
+                    }
+                    if (prev != kNone && idx - 1 < a.run_cap) a.run_count[idx - 1] = (uint32_t)(i - prev);
+                    prev = (uint32_t)i;
+                    runs++;
+                }
+                s = n;
+                p2 = p1;
+                p1 = av;
+                av = nx;
+            }
+            if (b1 == B && lb + runs - 1 < a.run_cap) a.run_count[lb + runs - 1] = (uint32_t)(B - prev);
+        }
+        __syncthreads();
+    }
+}
+
+// Blocks of k_encode that can be resident at once (cooperative launch limit).
+uint32_t encode_max_blocks() {
+    static int cached[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return (uint32_t)cached[dev];
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_encode, kThreads, 0) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const int n = per_sm * sm_count();
+    if (dev >= 0 && dev < 64) cached[dev] = n;
+    return (uint32_t)n;
 }
 
 }  // namespace
@@ -297,9 +407,10 @@ extern "C" size_t kvx_encode_workspace_size(uint32_t B, uint32_t L) {
 extern "C" kvx_status kvx_encode_runs(const uint64_t *addr, uint32_t B, uint32_t L,
                                       uint32_t *runs_per_lane, uint64_t *run_base,
                                       int64_t *run_stride, uint32_t *run_count,
-                                      uint64_t run_capacity, uint64_t *num_runs, void *ws,
-                                      size_t ws_bytes, void *stream) {
-    if (!num_runs || !ws || (L && !runs_per_lane) || ((uint64_t)B * L && !addr))
+                                      uint64_t run_capacity, uint64_t *num_runs,
+                                      uint32_t *status, void *ws, size_t ws_bytes,
+                                      void *stream) {
+    if (!num_runs || !status || !ws || (L && !runs_per_lane) || ((uint64_t)B * L && !addr))
         return KVX_EINVAL;
     if (kvx_run_capacity(B, L) && (!run_base || !run_stride || !run_count)) return KVX_EINVAL;
     if (run_capacity < kvx_run_capacity(B, L)) return KVX_ECAPACITY;
@@ -309,14 +420,30 @@ extern "C" kvx_status kvx_encode_runs(const uint64_t *addr, uint32_t B, uint32_t
     const Geometry g = geometry(B, L);
     cudaStream_t s = as_stream(stream);
     if (cudaMemsetAsync(w.ctl, 0, sizeof(EncodeCtl), s) != cudaSuccess) return KVX_ECUDA;
-    const uint32_t grid = g.ntl * g.ntr;
-    k_encode_tiles<<<grid, kThreads, 0, s>>>(addr, B, L, g, w.tiles, w.lane_base, runs_per_lane,
-                                             num_runs, w.ctl);
-    KVX_LAUNCHED();
-    if (B && L) {
-        k_encode_emit<<<grid, kThreads, 0, s>>>(addr, B, L, g, w.tiles, w.lane_base, run_base,
-                                                run_stride, run_count, run_capacity);
-        KVX_LAUNCHED();
+    EncodeArgs a;
+    a.addr = addr;
+    a.B = B;
+    a.L = L;
+    a.g = g;
+    a.tiles = w.tiles;
+    a.runs_per_lane = runs_per_lane;
+    a.tile_runs = w.tile_runs;
+    a.num_runs = num_runs;
+    a.run_base = run_base;
+    a.run_stride = run_stride;
+    a.run_count = run_count;
+    a.run_cap = run_capacity;
+    a.ctl = w.ctl;
+    a.status = status;
+    const uint32_t ntiles = g.ntl * g.ntr;
+    const uint32_t maxb = encode_max_blocks();
+    const uint32_t grid = ntiles < maxb ? ntiles : maxb;
+    void *args[] = {&a};
+    if (cudaLaunchCooperativeKernel((const void *)k_encode, dim3(grid), dim3(kThreads), args, 0, s) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        return KVX_ECUDA;
     }
+    note_launch();
     return KVX_OK;
 }

@@ -42,7 +42,7 @@ _SZ = ctypes.c_size_t
 _SIGS = {
     "kvx_run_capacity": (_U64, [_U32, _U32]),
     "kvx_encode_workspace_size": (_SZ, [_U32, _U32]),
-    "kvx_encode_runs": (ctypes.c_int, [_P, _U32, _U32, _P, _P, _P, _P, _U64, _P, _P, _SZ, _P]),
+    "kvx_encode_runs": (ctypes.c_int, [_P, _U32, _U32, _P, _P, _P, _P, _U64, _P, _P, _P, _SZ, _P]),
     "kvx_desc_capacity": (_U64, [_U32, _U32, _U64]),
     "kvx_plan_workspace_size": (_SZ, [_U32, _U64, _U64]),
     "kvx_plan_groups": (ctypes.c_int, [_P, _U32, _P, _P, _P, _P, _U64, _U32, _P, _P, _U32, _U64,
@@ -115,10 +115,11 @@ def kvx_encode_workspace_size(B: int, L: int) -> int:
 
 
 def kvx_encode_runs(addr, B, L, runs_per_lane, run_base, run_stride, run_count, run_capacity,
-                    num_runs, ws, stream=None):
+                    num_runs, status, ws, stream=None):
     _check(lib().kvx_encode_runs(_ptr(addr), B, L, _ptr(runs_per_lane), _ptr(run_base),
                                  _ptr(run_stride), _ptr(run_count), run_capacity, _ptr(num_runs),
-                                 _ptr(ws), ws.numel(), _stream(stream)), "kvx_encode_runs")
+                                 _ptr(status), _ptr(ws), ws.numel(), _stream(stream)),
+           "kvx_encode_runs")
 
 
 def kvx_desc_capacity(B: int, L: int, seg_bytes_sum: int) -> int:
@@ -245,7 +246,8 @@ class Transfer:
     def encode(self, addr=None, stream=None):
         a = self.addr if addr is None else addr
         kvx_encode_runs(a, self.B, self.L, self.runs_per_lane, self.run_base, self.run_stride,
-                        self.run_count, self.run_cap, self.num_runs, self.enc_ws, stream)
+                        self.run_count, self.run_cap, self.num_runs, self.status, self.enc_ws,
+                        stream)
 
     def plan(self, stream=None, table_lanes=None, group_cap=None, desc_cap=None):
         kvx_plan_groups(self.runs_per_lane, self.L if table_lanes is None else table_lanes,
