@@ -74,6 +74,17 @@ def _setup(handle):
         f = getattr(_lib, name)
         f.restype = ctypes.c_uint32
         f.argtypes = [u32p, ctypes.c_uint64, u32p, ctypes.c_uint64, u32p, ctypes.c_uint64]
+    _lib.kvxo_verify_encode.restype = ctypes.c_uint64
+    _lib.kvxo_verify_encode.argtypes = [u32p, u32p, u32p, ctypes.c_uint32, ctypes.c_uint32,
+                                        u32p, u32p, u32p, u32p, ctypes.c_uint64, u32p]
+    _lib.kvxo_seal_blocks.restype = ctypes.c_uint32
+    _lib.kvxo_seal_blocks.argtypes = ([u32p] * 6 + [ctypes.c_uint64, ctypes.c_uint32,
+                                                    ctypes.c_uint32, u32p, u32p, ctypes.c_uint64,
+                                                    u32p, u32p, ctypes.c_uint64])
+    _lib.kvxo_paged_writes.restype = ctypes.c_uint32
+    _lib.kvxo_paged_writes.argtypes = [ctypes.c_uint64, u32p, ctypes.c_uint64, u32p,
+                                       ctypes.c_uint64, ctypes.c_uint64, u32p, ctypes.c_uint64,
+                                       u32p, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64]
 
 
 def _p(a: np.ndarray):
@@ -196,3 +207,67 @@ def unpack(slab: np.ndarray, descs: np.ndarray, dst_pool: np.ndarray) -> int:
     d = np.ascontiguousarray(descs if descs.size else np.zeros(1, DESC_DTYPE))
     return int(lib().kvxo_unpack(_p(slab), slab.size, _p(d), int(descs.size), _p(dst_pool),
                                  dst_pool.size))
+
+
+def _nz(a: np.ndarray, dtype) -> np.ndarray:
+    """A contiguous array of dtype, never empty (ctypes wants a real pointer)."""
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a if a.size else np.zeros(1, dtype=dtype)
+
+
+def verify_encode(addr: np.ndarray, size: np.ndarray, tmpl_len: np.ndarray):
+    """Holder prefix scan with the slot-template check.  Returns (prefix
+    blocks, RunTable of those blocks)."""
+    addr = np.ascontiguousarray(addr, dtype=np.uint64)
+    B, L = addr.shape
+    size = np.ascontiguousarray(size, dtype=np.uint32)
+    assert size.shape == (B, L)
+    cap = max(1, run_capacity(B, L))
+    rpl = np.zeros(max(1, L), dtype=np.uint32)
+    base = np.zeros(cap, dtype=np.uint64)
+    stride = np.zeros(cap, dtype=np.int64)
+    count = np.zeros(cap, dtype=np.uint32)
+    prefix = np.zeros(1, dtype=np.uint32)
+    R = lib().kvxo_verify_encode(_p(_nz(addr, np.uint64)), _p(_nz(size, np.uint32)),
+                                 _p(_nz(tmpl_len, np.uint32)), B, L, _p(rpl), _p(base),
+                                 _p(stride), _p(count), cap, _p(prefix))
+    if R == 2**64 - 1:
+        raise RuntimeError("oracle verify_encode: run capacity exceeded")
+    return int(prefix[0]), RunTable(rpl[:L].copy(), base[:R].copy(), stride[:R].copy(),
+                                    count[:R].copy())
+
+
+def seal_blocks(table: RunTable, p: Plan, B: int, L: int, seg_len: np.ndarray,
+                slab: np.ndarray, dst_addr: np.ndarray, dst: np.ndarray,
+                groups: np.ndarray | None = None, run_group: np.ndarray | None = None,
+                slab_bytes: int | None = None) -> int:
+    """Install every segment from the slab at dst[dst_addr[b][l]] (in place on
+    dst).  Returns the status bitmask."""
+    groups = p.groups if groups is None else groups
+    run_group = p.run_group if run_group is None else run_group
+    slab_bytes = slab.size if slab_bytes is None else slab_bytes
+    assert slab_bytes <= slab.size
+    dst_addr = np.ascontiguousarray(dst_addr, dtype=np.uint64)
+    assert dst_addr.shape == (B, L)
+    return int(lib().kvxo_seal_blocks(
+        _p(_nz(table.runs_per_lane, np.uint32)), _p(_nz(table.run_base, np.uint64)),
+        _p(_nz(table.run_stride, np.int64)), _p(_nz(table.run_count, np.uint32)),
+        _p(_nz(run_group, np.uint32)), _p(_nz(groups, GROUP_DTYPE)), int(groups.size), B, L,
+        _p(_nz(seg_len, np.uint32)), _p(_nz(slab, np.uint8)), slab_bytes,
+        _p(_nz(dst_addr, np.uint64)), _p(dst), dst.size))
+
+
+def paged_writes(page_len: int, src: np.ndarray, src_idx: np.ndarray, src_stride: int,
+                 src_offset: int, dst: np.ndarray, dst_idx: np.ndarray, dst_stride: int,
+                 dst_offset: int) -> int:
+    """Copy page i of the source page set to page i of the destination set
+    (in place on dst).  Returns the status bitmask."""
+    src_idx = np.ascontiguousarray(src_idx, dtype=np.uint32)
+    dst_idx = np.ascontiguousarray(dst_idx, dtype=np.uint32)
+    assert src_idx.size == dst_idx.size
+    assert dst.flags["C_CONTIGUOUS"] and dst.dtype == np.uint8
+    return int(lib().kvxo_paged_writes(page_len, _p(_nz(src, np.uint8)), src.size,
+                                       _p(_nz(src_idx, np.uint32)), src_stride, src_offset,
+                                       _p(dst if dst.size else np.zeros(1, np.uint8)), dst.size,
+                                       _p(_nz(dst_idx, np.uint32)), dst_stride, dst_offset,
+                                       int(src_idx.size)))

@@ -22,6 +22,17 @@
  *                        (remote(b) - group_remote), every pointer checked.
  *   kvxo_pack/unpack  -- the data movement ("data itself moves"), one memcpy
  *                        per descriptor; unpack is the inverse copy.
+ *   kvxo_verify_encode -- Holder paragraph: the prefix scan checks each block
+ *                        against the slot template before its addresses
+ *                        enter the run accumulators (two-phase per block).
+ *   kvxo_seal_blocks  -- the follow-up the PR names after its stage
+ *                        breakdown (seal from template metadata): every
+ *                        segment is installed from the slab at its rebuilt
+ *                        offset, with no per-segment pointer table kept.
+ *   kvxo_paged_writes -- "RDMA point-to-point communication for LLM
+ *                        systems" (Perplexity), TransferEngine API listing:
+ *                        pages named by {indices, stride, offset}, the
+ *                        paged-write call copying page_len bytes per page.
  *
  * Readings where the page is silent (each is also listed in the design notes):
  *   - stride is the uint64 wrapping difference addr(s+1) - addr(s), stored as
@@ -432,6 +443,115 @@ uint32_t kvxo_unpack(const uint8_t *slab, uint64_t slab_bytes, const kvxo_desc *
             continue;
         }
         memcpy(dst_pool + d[k].remote, slab + d[k].local, d[k].len);
+    }
+    return st;
+}
+
+/* ------------------------------------------------ holder verify + encode */
+
+/*
+ * Holder prefix scan with the slot-template check (Holder paragraph): blocks
+ * are taken in order; a block is first checked as a whole -- every lane's
+ * segment size equals the template's length for that lane -- and only a
+ * block that passes contributes its addresses, so a mismatch in the middle
+ * of a block leaves nothing of that block in the table.  The scan stops at
+ * the first block that fails; *prefix receives the number of blocks taken.
+ * The run table is the greedy encoding (kvxo_encode_runs) of those blocks:
+ * addr is block-major, so they are its first *prefix rows.
+ */
+uint64_t kvxo_verify_encode(const uint64_t *addr, const uint32_t *size,
+                            const uint32_t *tmpl_len, uint32_t B, uint32_t L,
+                            uint32_t *runs_per_lane, uint64_t *run_base,
+                            int64_t *run_stride, uint32_t *run_count,
+                            uint64_t cap, uint32_t *prefix)
+{
+    uint32_t taken = 0;
+    for (uint32_t b = 0; b < B; b++) {
+        int ok = 1;                              /* phase 1: the whole block */
+        for (uint32_t l = 0; l < L && ok; l++)
+            if (size[(uint64_t)b * L + l] != tmpl_len[l])
+                ok = 0;
+        if (!ok)
+            break;
+        taken = b + 1;                           /* phase 2: its addresses join */
+    }
+    *prefix = taken;
+    return kvxo_encode_runs(addr, taken, L, runs_per_lane, run_base, run_stride,
+                            run_count, cap);
+}
+
+/* ------------------------------------------------------------------ seal */
+
+/*
+ * Seal from template metadata: segment (b, l) is copied from the slab at its
+ * rebuilt offset local(b, l) (kvxo_rebuild) to dst[dst_addr[b][l] ..
+ * + seg_len[l]), the receiver's own placement of that segment.  A segment
+ * whose rebuilt offset failed its checks, or whose destination range leaves
+ * dst, is not copied and raises KVXO_S_BOUNDS.  dst_addr is block-major
+ * [B][L].  Returns the status bitmask (0 on a clean run; UINT32_MAX when the
+ * scratch table cannot be allocated).
+ */
+uint32_t kvxo_seal_blocks(const uint32_t *runs_per_lane, const uint64_t *run_base,
+                          const int64_t *run_stride, const uint32_t *run_count,
+                          const uint32_t *run_group, const kvxo_group *groups,
+                          uint64_t num_groups, uint32_t B, uint32_t L,
+                          const uint32_t *seg_len, const uint8_t *slab,
+                          uint64_t slab_bytes, const uint64_t *dst_addr,
+                          uint8_t *dst, uint64_t dst_bytes)
+{
+    uint64_t n = (uint64_t)B * L;
+    uint64_t *local = (uint64_t *)malloc((n ? n : 1) * sizeof(uint64_t));
+    if (!local)
+        return UINT32_MAX;
+    uint32_t st = kvxo_rebuild(runs_per_lane, run_base, run_stride, run_count, run_group,
+                               groups, num_groups, B, L, seg_len, slab_bytes, local);
+    for (uint32_t b = 0; b < B; b++) {
+        for (uint32_t l = 0; l < L; l++) {
+            uint64_t k = (uint64_t)b * L + l;
+            if (local[k] == UINT64_MAX)
+                continue;                        /* flagged by the rebuild */
+            if (!in_range(dst_addr[k], seg_len[l], dst_bytes)) {
+                st |= KVXO_S_BOUNDS;
+                continue;
+            }
+            memcpy(dst + dst_addr[k], slab + local[k], seg_len[l]);
+        }
+    }
+    free(local);
+    return st;
+}
+
+/* ---------------------------------------------------------- paged writes */
+
+/*
+ * Paged write (TransferEngine API listing): a page set is {indices, stride,
+ * offset}; page i of the source set begins at src_offset + src_idx[i] *
+ * src_stride and is copied, page_len bytes, to page i of the destination set
+ * at dst_offset + dst_idx[i] * dst_stride.  Addresses are computed exactly;
+ * a page that does not lie inside its buffer is not copied (KVXO_S_SPAN for
+ * the source side, KVXO_S_BOUNDS for the destination side).  Destination
+ * pages are expected not to overlap.
+ */
+uint32_t kvxo_paged_writes(uint64_t page_len, const uint8_t *src, uint64_t src_bytes,
+                           const uint32_t *src_idx, uint64_t src_stride, uint64_t src_offset,
+                           uint8_t *dst, uint64_t dst_bytes, const uint32_t *dst_idx,
+                           uint64_t dst_stride, uint64_t dst_offset, uint64_t n)
+{
+    uint32_t st = 0;
+    for (uint64_t i = 0; i < n; i++) {
+        i128 s = (i128)src_offset + (i128)src_idx[i] * (i128)src_stride;
+        i128 d = (i128)dst_offset + (i128)dst_idx[i] * (i128)dst_stride;
+        int ok = 1;
+        if (s + (i128)page_len > (i128)src_bytes) {
+            st |= KVXO_S_SPAN;
+            ok = 0;
+        }
+        if (d + (i128)page_len > (i128)dst_bytes) {
+            st |= KVXO_S_BOUNDS;
+            ok = 0;
+        }
+        if (ok)
+            memcpy(dst + (uint64_t)d, src + (uint64_t)s, page_len);
     }
     return st;
 }

@@ -2,9 +2,10 @@
 
 Each mutant below is one plausible slip in the oracle (a dropped term, a wrong
 sign, index or operand, an off-by-one, a transposed copy).  It is planted in a
-temporary copy of the C source on the CPU, compiled, and the pin suite
-(test_oracle_pins.py) is run against it in a child process; every mutant must
-make at least one pin fail (or crash the child).
+temporary copy of the C source on the CPU, compiled, and the pin suites
+(test_oracle_pins.py, test_oracle_pins_next.py) are run against it in a
+child process; every mutant must make at least one pin fail (or crash the
+child).
 """
 import os
 import subprocess
@@ -57,6 +58,20 @@ MUTANTS = [
     ("unpack_transposed", "memcpy(dst_pool + d[k].remote, slab + d[k].local, d[k].len);",
      "memcpy(dst_pool + d[k].local, slab + d[k].remote, d[k].len);"),
     ("tiling_check_dropped", "if (d[k].local != expect || d[k].len == 0)", "if (d[k].len == 0)"),
+    ("verify_skips_instead_of_stopping", "        if (!ok)\n            break;", "        if (!ok)\n            continue;"),
+    ("verify_checks_lane0_only", "for (uint32_t l = 0; l < L && ok; l++)", "for (uint32_t l = 0; l < 1 && ok; l++)"),
+    ("verify_prefix_off_by_one", "taken = b + 1;", "taken = b;"),
+    ("seal_drops_dst_check", "if (!in_range(dst_addr[k], seg_len[l], dst_bytes)) {", "if (0) {"),
+    ("seal_lane0_length", "memcpy(dst + dst_addr[k], slab + local[k], seg_len[l]);",
+     "memcpy(dst + dst_addr[k], slab + local[k], seg_len[0] - 1);"),
+    ("seal_ignores_rebuild_flag", "            if (local[k] == UINT64_MAX)\n                continue;",
+     "            if (local[k] == UINT64_MAX)\n                local[k] = 0;"),
+    ("paged_src_uses_dst_stride", "(i128)src_idx[i] * (i128)src_stride;", "(i128)src_idx[i] * (i128)dst_stride;"),
+    ("paged_drops_dst_offset", "i128 d = (i128)dst_offset + ", "i128 d = "),
+    ("paged_64bit_arithmetic", "i128 s = (i128)src_offset + (i128)src_idx[i] * (i128)src_stride;",
+     "i128 s = (uint64_t)(src_offset + (uint64_t)src_idx[i] * src_stride);"),
+    ("paged_bounds_off_by_one", "if (d + (i128)page_len > (i128)dst_bytes) {", "if (d + (i128)page_len >= (i128)dst_bytes) {"),
+    ("paged_indices_swapped", "(i128)dst_idx[i] * (i128)dst_stride;", "(i128)src_idx[i] * (i128)dst_stride;"),
 ]
 
 
@@ -71,6 +86,7 @@ def test_mutant_is_caught(name, old, new, tmp_path):
     subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-w", "-o", str(so), str(c)])
     env = dict(os.environ, KVX_ORACLE_LIB=str(so))
     res = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                          os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                          os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                          os.path.join(ROOT, "tests", "test_oracle_pins_next.py")],
                          env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert res.returncode != 0, f"mutant {name} survived the pins:\n{res.stdout[-2000:]}"
