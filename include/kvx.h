@@ -20,6 +20,18 @@
  *   kvx_unpack       the inverse copy: slab -> a pool with the holder's layout
  *                    (not on the page; it closes the round trip)
  *
+ * and the steps around it that the pages name next:
+ *
+ *   kvx_verify_encode  the holder's prefix scan with its two-phase check of
+ *                    each block against the slot template, fused with the
+ *                    run encoding (Holder paragraph)
+ *   kvx_seal_blocks  seal from template metadata: fetched segments installed
+ *                    at the receiver's addresses straight from the slab, the
+ *                    local offsets computed on the fly (the PR's follow-up)
+ *   kvx_paged_writes page-index driven copies, the paged write of the
+ *                    TransferEngine API ("RDMA point-to-point communication
+ *                    for LLM systems", Perplexity)
+ *
  * Conventions for every call:
  *   - Array arguments are DEVICE pointers, allocated and owned by the caller.
  *     The library allocates nothing; scratch memory is the caller's `ws`
@@ -144,6 +156,34 @@ kvx_status kvx_encode_runs(const uint64_t *addr, uint32_t B, uint32_t L,
                            uint32_t *status, void *ws, size_t ws_bytes,
                            void *stream);
 
+/*
+ * The holder's prefix scan with its slot-template check, fused with the run
+ * encoding (Holder paragraph: each block is verified against the slot
+ * template first and only then feeds its addresses to the per-lane run
+ * accumulators, two-phase per block, so a mid-block mismatch never leaks
+ * part of a block into the table).  Block b passes when seg_size[b][l] ==
+ * seg_len[l] for every lane l; the prefix is the blocks before the first
+ * block that fails (all B when every block passes), and the run table is
+ * exactly what kvx_encode_runs writes for those blocks.
+ *
+ *   seg_size       [B][L] uint32, the sizes the holder's blocks actually
+ *                  have (block-major, like addr).
+ *   seg_len        [L] uint32, the slot template's segment lengths.
+ *   prefix_blocks  [1] out (device): blocks in the prefix, B' <= B.  The
+ *                  plan of this table takes B' as its block count.
+ * Every other argument as for kvx_encode_runs (workspace:
+ * kvx_encode_workspace_size(B, L); runs of blocks >= B' are never written).
+ * One cooperative launch; a template mismatch is not an error (it only ends
+ * the prefix), so status gets KVX_S_TIMEOUT at most.
+ */
+kvx_status kvx_verify_encode(const uint64_t *addr, const uint32_t *seg_size,
+                             const uint32_t *seg_len, uint32_t B, uint32_t L,
+                             uint32_t *prefix_blocks, uint32_t *runs_per_lane,
+                             uint64_t *run_base, int64_t *run_stride,
+                             uint32_t *run_count, uint64_t run_capacity,
+                             uint64_t *num_runs, uint32_t *status, void *ws,
+                             size_t ws_bytes, void *stream);
+
 /* ------------------------------------------------------------------ plan */
 
 /* Bound on descriptors for a valid table: at most one span per segment
@@ -261,6 +301,61 @@ kvx_status kvx_unpack(const uint8_t *slab, uint64_t slab_bytes,
                       uint64_t desc_capacity, uint8_t *dst_pool,
                       uint64_t pool_bytes, uint32_t *status,
                       void *ws, size_t ws_bytes, void *stream);
+
+/* -------------------------------------------- seal from template metadata */
+
+/*
+ * Seal the fetched blocks into the receiver's cache (pegaflow PR #350: the
+ * follow-up named after the stage breakdown, "seal from template metadata",
+ * which removes the per-segment pointer construction of step 5).  For every
+ * block b < B and lane l < L: dst[dst_addr[b][l], + seg_len[l]) =
+ * slab[local(b, l), + seg_len[l]), where local(b, l) is computed on the fly
+ * exactly as kvx_rebuild defines it (same arithmetic, same checks) and never
+ * stored.  A segment whose local offset fails a check, or whose destination
+ * range leaves [0, dst_bytes), is not copied and raises KVX_S_BOUNDS; the
+ * others are copied.  dst_addr = the holder table gives the bytes kvx_unpack
+ * writes.
+ *
+ * Inputs: the plan outputs as for kvx_rebuild; the slab (read, slab_bytes);
+ * dst_addr [B][L] uint64 byte offsets into dst (block-major); dst, dst_bytes.
+ * Destination ranges must not overlap each other (else the overlap holds
+ * undefined bytes) and must not overlap the slab.  No workspace; one launch.
+ */
+kvx_status kvx_seal_blocks(const uint32_t *lane_first, const uint32_t *run_block,
+                           const uint32_t *run_group, const uint64_t *run_off,
+                           uint64_t run_capacity, const kvx_group *groups,
+                           uint64_t group_capacity, const uint64_t *counts,
+                           uint32_t B, uint32_t L, const uint32_t *seg_len,
+                           const uint8_t *slab, uint64_t slab_bytes,
+                           const uint64_t *dst_addr, uint8_t *dst,
+                           uint64_t dst_bytes, uint32_t *status, void *stream);
+
+/* ------------------------------------------------------------ paged writes */
+
+/*
+ * Paged write by page indices ("RDMA point-to-point communication for LLM
+ * systems", Perplexity: the TransferEngine API's page sets {indices, stride,
+ * offset} and its paged-write call), as a device-to-device copy.  For i in
+ * [0, num_pages): page_len bytes from src at src_offset + src_indices[i] *
+ * src_stride go to dst at dst_offset + dst_indices[i] * dst_stride.
+ * Addresses are computed exactly (no 64-bit wrap).  A page whose source
+ * range leaves [0, src_bytes) raises KVX_S_SPAN, one whose destination range
+ * leaves [0, dst_bytes) raises KVX_S_BOUNDS; such a page is not copied, the
+ * others are.  Pages are copied in no particular order; destination pages
+ * must not overlap each other or the source (else undefined bytes there).
+ *
+ *   src_indices, dst_indices  [num_pages] uint32 (device).
+ *   src, dst                  device buffers of src_bytes / dst_bytes.
+ * No workspace; one launch.  num_pages == 0 enqueues nothing.
+ */
+kvx_status kvx_paged_writes(uint64_t page_len,
+                            const uint8_t *src, uint64_t src_bytes,
+                            const uint32_t *src_indices, uint64_t src_stride,
+                            uint64_t src_offset,
+                            uint8_t *dst, uint64_t dst_bytes,
+                            const uint32_t *dst_indices, uint64_t dst_stride,
+                            uint64_t dst_offset,
+                            uint64_t num_pages, uint32_t *status, void *stream);
 
 /*
  * kvx_pack without a caller workspace, for callers that cannot allocate

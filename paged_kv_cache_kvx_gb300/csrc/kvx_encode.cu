@@ -105,6 +105,7 @@ __device__ __forceinline__ Xfer unpack_xfer(const TileRec &t) {
 
 struct EncodeCtl {
     GridSync gs;
+    uint32_t cut;  // template check: B - (first failing block), 0 when every block passes
 };
 
 __device__ __forceinline__ uint64_t ld_addr(const uint64_t *addr, uint64_t b, uint32_t L, uint32_t l) {
@@ -213,6 +214,9 @@ __device__ uint64_t block_sum_tiles(const uint64_t *v, uint32_t n, uint64_t *s_r
 
 struct EncodeArgs {
     const uint64_t *addr;
+    const uint32_t *seg_size;  // optional [B][L]: observed segment sizes (template check)
+    const uint32_t *tmpl_len;  // [L] template segment lengths (with seg_size)
+    uint32_t *prefix;          // [1] out: blocks that pass (with seg_size)
     uint32_t B, L;
     Geometry g;
     TileRec *tiles;
@@ -238,13 +242,42 @@ __global__ void __launch_bounds__(kThreads) k_encode(const __grid_constant__ Enc
     const uint32_t ntiles = g.ntl * g.ntr;
     const uint32_t G = gridDim.x;
 
+    // ---- phase 0 (holder prefix scan): the first block whose segment sizes
+    // differ from the template ends the prefix; blocks from it on add nothing
+    uint32_t Bv = B;
+    if (a.prefix) {
+        uint32_t cut = 0;
+        for (uint32_t tile = blockIdx.x; tile < ntiles; tile += G) {
+            const uint32_t tl = tile % g.ntl, tr = tile / g.ntl;
+            const uint32_t l = tl * 32 + t;
+            const uint64_t b0 = (uint64_t)tr * kRows * g.K + (uint64_t)w * g.K;
+            const uint64_t b1 = b0 + g.K < B ? b0 + g.K : B;
+            if (l < L) {
+                const uint32_t want = __ldg(a.tmpl_len + l);
+                for (uint64_t b = b0; b < b1; b++)
+                    if (__ldg(a.seg_size + b * L + l) != want) {
+                        cut = max(cut, (uint32_t)(B - b));
+                        break;
+                    }
+            }
+        }
+        for (int d = 16; d > 0; d >>= 1) cut = max(cut, __shfl_xor_sync(0xFFFFFFFFu, cut, d));
+        if (t == 0 && cut) atomicMax(&a.ctl->cut, cut);
+        if (!grid_barrier(&a.ctl->gs, G)) {
+            if (threadIdx.x == 0) atomicOr(a.status, KVX_S_TIMEOUT);
+            return;
+        }
+        Bv = B - *(volatile uint32_t *)&a.ctl->cut;
+        if (blockIdx.x == 0 && threadIdx.x == 0) *a.prefix = Bv;
+    }
+
     // ---- phase 1: each tile's effect on each of its lanes
     for (uint32_t tile = blockIdx.x; tile < ntiles; tile += G) {
         const uint32_t tl = tile % g.ntl, tr = tile / g.ntl;
         const uint32_t l = tl * 32 + t;
         const uint64_t b0 = (uint64_t)tr * kRows * g.K + (uint64_t)w * g.K;
-        const uint64_t b1 = b0 + g.K < B ? b0 + g.K : B;
-        sx[w][t] = (l < L && b0 < B) ? slice_xfer(a.addr, L, l, b0, b1) : xfer_identity();
+        const uint64_t b1 = b0 + g.K < Bv ? b0 + g.K : Bv;
+        sx[w][t] = (l < L && b0 < Bv) ? slice_xfer(a.addr, L, l, b0, b1) : xfer_identity();
         __syncthreads();
         if (w == 0 && l < L) {
             Xfer acc = sx[0][t];
@@ -322,8 +355,8 @@ __global__ void __launch_bounds__(kThreads) k_encode(const __grid_constant__ Enc
             }
         }
         const uint64_t b0 = (uint64_t)tr * kRows * g.K + (uint64_t)w * g.K;
-        const uint64_t b1 = b0 + g.K < B ? b0 + g.K : B;
-        const bool active = l < L && b0 < B;
+        const uint64_t b1 = b0 + g.K < Bv ? b0 + g.K : Bv;
+        const bool active = l < L && b0 < Bv;
         sx[w][t] = active ? slice_xfer(a.addr, L, l, b0, b1) : xfer_identity();
         __syncthreads();
         if (w == 0 && l < L) {
@@ -345,7 +378,7 @@ __global__ void __launch_bounds__(kThreads) k_encode(const __grid_constant__ Enc
             uint32_t runs = p.runs;
             uint32_t prev = p.prev;
             for (uint64_t i = b0; i < b1; i++) {
-                const uint64_t nx = i + 1 < B ? ld_addr(a.addr, i + 1, L, l) : 0;
+                const uint64_t nx = i + 1 < Bv ? ld_addr(a.addr, i + 1, L, l) : 0;
                 uint32_t n;
                 if (i == 0)
                     n = 0;
@@ -357,7 +390,7 @@ __global__ void __launch_bounds__(kThreads) k_encode(const __grid_constant__ Enc
                     const uint64_t idx = lb + runs;
                     if (idx < a.run_cap) {  // always true: runs per lane <= ceil(B/2)
                         a.run_base[idx] = av;
-                        a.run_stride[idx] = i + 1 < B ? (int64_t)(nx - av) : 0;
+                        a.run_stride[idx] = i + 1 < Bv ? (int64_t)(nx - av) : 0;
                     }
                     if (prev != kNone && idx - 1 < a.run_cap) a.run_count[idx - 1] = (uint32_t)(i - prev);
                     prev = (uint32_t)i;
@@ -368,7 +401,7 @@ __global__ void __launch_bounds__(kThreads) k_encode(const __grid_constant__ Enc
                 p1 = av;
                 av = nx;
             }
-            if (b1 == B && lb + runs - 1 < a.run_cap) a.run_count[lb + runs - 1] = (uint32_t)(B - prev);
+            if (b1 == Bv && lb + runs - 1 < a.run_cap) a.run_count[lb + runs - 1] = (uint32_t)(Bv - prev);
         }
         __syncthreads();
     }
@@ -404,12 +437,14 @@ extern "C" size_t kvx_encode_workspace_size(uint32_t B, uint32_t L) {
     return bytes;
 }
 
-extern "C" kvx_status kvx_encode_runs(const uint64_t *addr, uint32_t B, uint32_t L,
-                                      uint32_t *runs_per_lane, uint64_t *run_base,
-                                      int64_t *run_stride, uint32_t *run_count,
-                                      uint64_t run_capacity, uint64_t *num_runs,
-                                      uint32_t *status, void *ws, size_t ws_bytes,
-                                      void *stream) {
+namespace kvx {
+namespace {
+
+kvx_status launch_encode(const uint64_t *addr, const uint32_t *seg_size, const uint32_t *tmpl_len,
+                         uint32_t *prefix, uint32_t B, uint32_t L, uint32_t *runs_per_lane,
+                         uint64_t *run_base, int64_t *run_stride, uint32_t *run_count,
+                         uint64_t run_capacity, uint64_t *num_runs, uint32_t *status, void *ws,
+                         size_t ws_bytes, void *stream) {
     if (!num_runs || !status || !ws || (L && !runs_per_lane) || ((uint64_t)B * L && !addr))
         return KVX_EINVAL;
     if (kvx_run_capacity(B, L) && (!run_base || !run_stride || !run_count)) return KVX_EINVAL;
@@ -422,6 +457,9 @@ extern "C" kvx_status kvx_encode_runs(const uint64_t *addr, uint32_t B, uint32_t
     if (cudaMemsetAsync(w.ctl, 0, sizeof(EncodeCtl), s) != cudaSuccess) return KVX_ECUDA;
     EncodeArgs a;
     a.addr = addr;
+    a.seg_size = seg_size;
+    a.tmpl_len = tmpl_len;
+    a.prefix = prefix;
     a.B = B;
     a.L = L;
     a.g = g;
@@ -446,4 +484,31 @@ extern "C" kvx_status kvx_encode_runs(const uint64_t *addr, uint32_t B, uint32_t
     }
     note_launch();
     return KVX_OK;
+}
+
+}  // namespace
+}  // namespace kvx
+
+extern "C" kvx_status kvx_encode_runs(const uint64_t *addr, uint32_t B, uint32_t L,
+                                      uint32_t *runs_per_lane, uint64_t *run_base,
+                                      int64_t *run_stride, uint32_t *run_count,
+                                      uint64_t run_capacity, uint64_t *num_runs,
+                                      uint32_t *status, void *ws, size_t ws_bytes,
+                                      void *stream) {
+    return launch_encode(addr, nullptr, nullptr, nullptr, B, L, runs_per_lane, run_base,
+                         run_stride, run_count, run_capacity, num_runs, status, ws, ws_bytes,
+                         stream);
+}
+
+extern "C" kvx_status kvx_verify_encode(const uint64_t *addr, const uint32_t *seg_size,
+                                        const uint32_t *seg_len, uint32_t B, uint32_t L,
+                                        uint32_t *prefix_blocks, uint32_t *runs_per_lane,
+                                        uint64_t *run_base, int64_t *run_stride,
+                                        uint32_t *run_count, uint64_t run_capacity,
+                                        uint64_t *num_runs, uint32_t *status, void *ws,
+                                        size_t ws_bytes, void *stream) {
+    if (!prefix_blocks || (L && !seg_len) || ((uint64_t)B * L && !seg_size)) return KVX_EINVAL;
+    return launch_encode(addr, seg_size, seg_len, prefix_blocks, B, L, runs_per_lane, run_base,
+                         run_stride, run_count, run_capacity, num_runs, status, ws, ws_bytes,
+                         stream);
 }

@@ -53,6 +53,12 @@ _SIGS = {
     "kvx_pack": (ctypes.c_int, [_P, _U64, _P, _P, _U64, _P, _U64, _P, _P, _SZ, _P]),
     "kvx_unpack": (ctypes.c_int, [_P, _U64, _P, _P, _U64, _P, _U64, _P, _P, _SZ, _P]),
     "kvx_pack_noalloc": (ctypes.c_int, [_P, _U64, _P, _P, _U64, _P, _U64, _P, _P]),
+    "kvx_verify_encode": (ctypes.c_int, [_P, _P, _P, _U32, _U32, _P, _P, _P, _P, _P, _U64, _P, _P,
+                                         _P, _SZ, _P]),
+    "kvx_seal_blocks": (ctypes.c_int, [_P, _P, _P, _P, _U64, _P, _U64, _P, _U32, _U32, _P, _P, _U64,
+                                       _P, _P, _U64, _P, _P]),
+    "kvx_paged_writes": (ctypes.c_int, [_U64, _P, _U64, _P, _U64, _U64, _P, _U64, _P, _U64, _U64,
+                                        _U64, _P, _P]),
     "kvx_selftest_timeouts": (ctypes.c_int, [_P, _P]),
     "kvx_launch_count": (_U64, []),
     "kvx_version": (_U32, []),
@@ -177,6 +183,32 @@ def kvx_pack_noalloc(pool, pool_bytes, descs, num_descs, desc_capacity, slab, sl
                                   _stream(stream)), "kvx_pack_noalloc")
 
 
+def kvx_verify_encode(addr, seg_size, seg_len, B, L, prefix_blocks, runs_per_lane, run_base,
+                      run_stride, run_count, run_capacity, num_runs, status, ws, stream=None):
+    _check(lib().kvx_verify_encode(_ptr(addr), _ptr(seg_size), _ptr(seg_len), B, L,
+                                   _ptr(prefix_blocks), _ptr(runs_per_lane), _ptr(run_base),
+                                   _ptr(run_stride), _ptr(run_count), run_capacity, _ptr(num_runs),
+                                   _ptr(status), _ptr(ws), ws.numel(), _stream(stream)),
+           "kvx_verify_encode")
+
+
+def kvx_seal_blocks(lane_first, run_block, run_group, run_off, run_capacity, groups,
+                    group_capacity, counts, B, L, seg_len, slab, slab_bytes, dst_addr, dst,
+                    dst_bytes, status, stream=None):
+    _check(lib().kvx_seal_blocks(_ptr(lane_first), _ptr(run_block), _ptr(run_group), _ptr(run_off),
+                                 run_capacity, _ptr(groups), group_capacity, _ptr(counts), B, L,
+                                 _ptr(seg_len), _ptr(slab), slab_bytes, _ptr(dst_addr), _ptr(dst),
+                                 dst_bytes, _ptr(status), _stream(stream)), "kvx_seal_blocks")
+
+
+def kvx_paged_writes(page_len, src, src_bytes, src_indices, src_stride, src_offset, dst, dst_bytes,
+                     dst_indices, dst_stride, dst_offset, num_pages, status, stream=None):
+    _check(lib().kvx_paged_writes(page_len, _ptr(src), src_bytes, _ptr(src_indices), src_stride,
+                                  src_offset, _ptr(dst), dst_bytes, _ptr(dst_indices), dst_stride,
+                                  dst_offset, num_pages, _ptr(status), _stream(stream)),
+           "kvx_paged_writes")
+
+
 def kvx_selftest_timeouts(status, stream=None):
     _check(lib().kvx_selftest_timeouts(_ptr(status), _stream(stream)), "kvx_selftest_timeouts")
 
@@ -249,6 +281,15 @@ class Transfer:
                         self.run_count, self.run_cap, self.num_runs, self.status, self.enc_ws,
                         stream)
 
+    def verify_encode(self, seg_size, prefix, addr=None, stream=None):
+        """Holder prefix scan: blocks checked against the template (seg_size
+        [B][L] observed sizes), then the passing prefix run-encoded.  The
+        prefix length lands in prefix (a device uint32)."""
+        a = self.addr if addr is None else addr
+        kvx_verify_encode(a, seg_size, self.seg_len, self.B, self.L, prefix, self.runs_per_lane,
+                          self.run_base, self.run_stride, self.run_count, self.run_cap,
+                          self.num_runs, self.status, self.enc_ws, stream)
+
     def plan(self, stream=None, table_lanes=None, group_cap=None, desc_cap=None):
         kvx_plan_groups(self.runs_per_lane, self.L if table_lanes is None else table_lanes,
                         self.run_base, self.run_stride, self.run_count, self.num_runs,
@@ -271,6 +312,13 @@ class Transfer:
     def unpack(self, slab, dst_pool, stream=None):
         kvx_unpack(slab, slab.numel(), self.descs, self.counts[1:], self.desc_cap, dst_pool,
                    dst_pool.numel(), self.status, self.copy_ws, stream)
+
+    def seal(self, slab, dst_addr, dst, stream=None):
+        """Install every segment from the slab at dst[dst_addr[b][l]] (seal
+        from template metadata; no local table is written)."""
+        kvx_seal_blocks(self.lane_first, self.run_block, self.run_group, self.run_off, self.run_cap,
+                        self.groups, self.group_cap, self.counts, self.B, self.L, self.seg_len,
+                        slab, slab.numel(), dst_addr, dst, dst.numel(), self.status, stream)
 
     def step(self, pool, slab, dst_pool, stream=None, side=None):
         """One pass of the whole path: encode, plan, rebuild, pack, unpack.

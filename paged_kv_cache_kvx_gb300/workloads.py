@@ -204,6 +204,54 @@ def small_variants():
     ]
 
 
+# ------------------------------------------------------------ paged writes
+
+@dataclass
+class PagedWorkload:
+    """Two page pools and the page tables of one paged write ("RDMA
+    point-to-point communication for LLM systems": page sets {indices,
+    stride, offset}, KvCache pages moved between a prefill and a decode
+    instance).  Page i goes from source page src_idx[i] to destination page
+    dst_idx[i]; each table lists distinct pages in a seeded random order, as
+    a paged cache's block tables do after some churn."""
+
+    name: str
+    page_len: int
+    num_pages: int
+    src_idx: np.ndarray         # uint32 [num_pages]
+    src_stride: int
+    src_offset: int
+    src_bytes: int
+    dst_idx: np.ndarray         # uint32 [num_pages]
+    dst_stride: int
+    dst_offset: int
+    dst_bytes: int
+    seed: int
+
+    @property
+    def bytes_moved(self) -> int:
+        return self.num_pages * self.page_len
+
+
+def paged(name, num_pages, page_len, src_pages, dst_pages, src_stride=None, src_offset=0,
+          dst_stride=None, dst_offset=0, seed=6):
+    rng = np.random.default_rng(seed)
+    src_stride = page_len if src_stride is None else src_stride
+    dst_stride = page_len if dst_stride is None else dst_stride
+    src_idx = rng.permutation(src_pages)[:num_pages].astype(np.uint32)
+    dst_idx = rng.permutation(dst_pages)[:num_pages].astype(np.uint32)
+    return PagedWorkload(name, page_len, num_pages, src_idx, src_stride, src_offset,
+                         src_offset + (src_pages - 1) * src_stride + page_len, dst_idx,
+                         dst_stride, dst_offset, dst_offset + (dst_pages - 1) * dst_stride + page_len,
+                         seed)
+
+
+def paged_default(seed=6):
+    """576,000 pages of 4 KiB (2250 MiB, the default workload's bytes) from a
+    pool of 720,000 pages to a pool of 640,000 pages, both tables permuted."""
+    return paged("paged_default", 576_000, 4 * KIB, 720_000, 640_000, seed=seed)
+
+
 # ---------------------------------------------------------------- payload bytes
 
 def splitmix64_np(x: np.ndarray) -> np.ndarray:
