@@ -38,7 +38,8 @@
  *   - stride is the uint64 wrapping difference addr(s+1) - addr(s), stored as
  *     its int64 bit pattern; a run of length 1 has stride 0.
  *   - runs are emitted lane-major, blocks ascending.
- *   - sort key (node, base, lane, first block), all ascending.
+ *   - sort key (node, base, lane, first block), all ascending (with empty
+ *     runs after the others of their node, see below).
  *   - "grown chunk still fits the stride": fits(c) <=> count == 1 or
  *     (stride > 0 and c <= stride); a run that fails it alone still forms a
  *     one-run group.
@@ -48,6 +49,14 @@
  *     i*G.stride)), the "dense local mirror" of step 4.
  *   - descriptors split into 32 MiB pieces, remainder last; order = group,
  *     block, piece.
+ *   - zero-size slots: lane l = 2*slot + kv; only a zero-size K slot (even
+ *     lane) is rejected, as the page lists.  A zero-size V lane (a K-only
+ *     cache) is accepted: its runs are validated like any other, but as they
+ *     move no byte they must not decide how byte-carrying runs group, so
+ *     they sort after every non-empty run of their NUMA node (key: node,
+ *     empty, base, lane, block).  There the same grouping rule gives them
+ *     groups of chunk 0 -- no slab bytes, no descriptor -- and their rebuilt
+ *     pointers are empty ranges at the end of the node's partition.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -58,7 +67,7 @@
 #define KVXO_S_ARRAYS     2u    /* parallel arrays not in sync */
 #define KVXO_S_COVERAGE   4u    /* a lane's run counts do not add up to B */
 #define KVXO_S_ZERO_COUNT 8u    /* a run with count 0 */
-#define KVXO_S_ZERO_LEN   16u   /* a template lane with segment length 0 */
+#define KVXO_S_ZERO_LEN   16u   /* a K lane (even lane) with segment length 0 */
 #define KVXO_S_SPAN       32u   /* a remote span overflows / leaves the pool */
 #define KVXO_S_STRIDE1    64u   /* a one-block run with nonzero stride */
 #define KVXO_S_BOUNDS     128u  /* a local pointer / copy outside its range */
@@ -153,6 +162,7 @@ static int cmp_run(const void *pa, const void *pb)
     const run_rec *a = &g_sort_recs[*(const uint64_t *)pa];
     const run_rec *b = &g_sort_recs[*(const uint64_t *)pb];
     if (a->node != b->node) return a->node < b->node ? -1 : 1;
+    if ((a->len == 0) != (b->len == 0)) return a->len == 0 ? 1 : -1;  /* empty runs last */
     if (a->base != b->base) return a->base < b->base ? -1 : 1;
     if (a->lane != b->lane) return a->lane < b->lane ? -1 : 1;
     if (a->block != b->block) return a->block < b->block ? -1 : 1;
@@ -204,7 +214,7 @@ uint32_t kvxo_plan(const uint32_t *runs_per_lane, uint32_t table_lanes,
     uint32_t st = 0;
     uint64_t total_len = 0;
     for (uint32_t l = 0; l < table_lanes; l++) {
-        if (seg_len[l] == 0)
+        if (seg_len[l] == 0 && l % 2 == 0)     /* a zero-size K slot */
             st |= KVXO_S_ZERO_LEN;
         if (runs_per_lane[l] == 0 && B > 0)
             st |= KVXO_S_COVERAGE;

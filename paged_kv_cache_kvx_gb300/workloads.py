@@ -72,24 +72,28 @@ class Workload:
         return int(self.blocks) * int(self.seg_len.astype(np.uint64).sum())
 
 
-def _build(name, blocks, slots, seg, region_slots, positions, npos, seed):
-    """Assemble a Workload from per-region slot ranges and block positions."""
+def _build(name, blocks, slots, seg, region_slots, positions, npos, seed, v_seg=None):
+    """Assemble a Workload from per-region slot ranges and block positions.
+    v_seg (default seg) is the V segment length; 0 gives a K-only cache whose
+    empty V segments sit where the next segment starts."""
+    v_seg = seg if v_seg is None else v_seg
     L = 2 * slots
     addr = np.zeros((blocks, L), dtype=np.uint64)
     numa = np.zeros(L, dtype=np.uint32)
     regions = []
     base = 0
     for r, (first, nslots) in enumerate(region_slots):
-        chunk = 2 * nslots * seg
+        chunk = nslots * (seg + v_seg)
         pos = np.asarray(positions[r], dtype=np.uint64)
         lanes = np.arange(2 * first, 2 * (first + nslots))
-        within = (lanes - 2 * first).astype(np.uint64) * np.uint64(seg)
+        j = (lanes - 2 * first) // 2
+        within = (j * (seg + v_seg) + (lanes % 2) * seg).astype(np.uint64)
         addr[:, lanes] = (np.uint64(base) + pos[:, None] * np.uint64(chunk)
                           + within[None, :])
         numa[lanes] = r
         regions.append((first, nslots, base, npos[r]))
         base += npos[r] * chunk
-    seg_len = np.full(L, seg, dtype=np.uint32)
+    seg_len = np.array([seg, v_seg] * slots, dtype=np.uint32)
     return Workload(name=name, blocks=blocks, slots=slots, seg=seg, addr=addr,
                     seg_len=seg_len, numa=numa, pool_bytes=base, seed=seed,
                     regions=regions, pos=[np.asarray(p, dtype=np.int64) for p in positions])
@@ -100,11 +104,11 @@ def _two_regions(slots):
     return [(0, half), (half, slots - half)]
 
 
-def bump(name="default", blocks=1000, slots=288, seg=4 * KIB, nregions=2, seed=2):
+def bump(name="default", blocks=1000, slots=288, seg=4 * KIB, nregions=2, seed=2, v_seg=None):
     """Fully bump-allocated holder: pos(b) = b in every region."""
     regs = _two_regions(slots) if nregions == 2 else [(0, slots)]
     pos = [np.arange(blocks)] * len(regs)
-    return _build(name, blocks, slots, seg, regs, pos, [blocks] * len(regs), seed)
+    return _build(name, blocks, slots, seg, regs, pos, [blocks] * len(regs), seed, v_seg)
 
 
 def tiny():
@@ -122,13 +126,13 @@ def wide64k():
     return bump("wide64k", blocks=200, slots=288, seg=64 * KIB, nregions=2, seed=6)
 
 
-def worst(blocks=1000, slots=288, seg=4 * KIB, npos=2048, seed=3):
+def worst(blocks=1000, slots=288, seg=4 * KIB, npos=2048, seed=3, v_seg=None):
     """Per-block allocation order permuted: pos(b) = first B of a seeded shuffle of
     [0, npos), the same permutation in both regions (pool = 2 * npos * chunk)."""
     rng = np.random.default_rng(seed)
     perm = rng.permutation(npos)[:blocks]
     regs = _two_regions(slots)
-    return _build("worst", blocks, slots, seg, regs, [perm, perm], [npos, npos], seed)
+    return _build("worst", blocks, slots, seg, regs, [perm, perm], [npos, npos], seed, v_seg)
 
 
 def mixed(blocks=4096, slots=64, seg=16 * KIB, gap_mean=56.0 / 3.0, run_mean=8.0, seed=4):
@@ -188,6 +192,19 @@ CONFIGS = {
     "many_small": many_small,
     "wide64k": wide64k,
 }
+
+
+def k_only(layout: str, null_v: bool = False, **kw) -> Workload:
+    """A K-only cache (every V segment of length 0, as in a cache that keeps a
+    single latent per token), laid out like bump() or worst() with the same
+    keyword arguments.  The holder either places each empty V segment where
+    the next segment starts (what a bump allocator gives) or reports address
+    0 for it (null_v)."""
+    wl = {"bump": bump, "worst": worst}[layout](v_seg=0, **kw)
+    wl.name = f"{wl.name}_konly" + ("_nullv" if null_v else "")
+    if null_v:
+        wl.addr[:, 1::2] = 0
+    return wl
 
 
 def small_variants():

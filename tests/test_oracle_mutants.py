@@ -58,6 +58,10 @@ MUTANTS = [
     ("unpack_transposed", "memcpy(dst_pool + d[k].remote, slab + d[k].local, d[k].len);",
      "memcpy(dst_pool + d[k].local, slab + d[k].remote, d[k].len);"),
     ("tiling_check_dropped", "if (d[k].local != expect || d[k].len == 0)", "if (d[k].len == 0)"),
+    ("zero_len_any_lane", "if (seg_len[l] == 0 && l % 2 == 0)", "if (seg_len[l] == 0)"),
+    ("zero_len_v_lanes", "if (seg_len[l] == 0 && l % 2 == 0)", "if (seg_len[l] == 0 && l % 2 == 1)"),
+    ("empty_runs_not_last", "    if ((a->len == 0) != (b->len == 0)) return a->len == 0 ? 1 : -1;  /* empty runs last */\n", ""),
+    ("empty_runs_first", "return a->len == 0 ? 1 : -1;  /* empty runs last */", "return a->len == 0 ? -1 : 1;"),
     ("verify_skips_instead_of_stopping", "        if (!ok)\n            break;", "        if (!ok)\n            continue;"),
     ("verify_checks_lane0_only", "for (uint32_t l = 0; l < L && ok; l++)", "for (uint32_t l = 0; l < 1 && ok; l++)"),
     ("verify_prefix_off_by_one", "taken = b + 1;", "taken = b;"),

@@ -289,3 +289,110 @@ def test_paged_empty():
     assert oracle.paged_writes(4, src, [], 4, 0, dst, [], 4, 0) == 0
     assert oracle.paged_writes(0, src, [3, 1], 4, 0, dst, [0, 1], 4, 0) == 0
     assert (dst == 7).all()
+
+
+# ------------------------------------------------------- zero-size V lanes
+
+def _compressed(wl):
+    """The same holder with the V lanes dropped: the bytes a K-only cache
+    really has."""
+    return (np.ascontiguousarray(wl.addr[:, ::2]), np.ascontiguousarray(wl.seg_len[::2]),
+            np.ascontiguousarray(wl.numa[::2]))
+
+
+def _plan_of(addr, seg_len, numa, pool):
+    t = oracle.encode_runs(addr)
+    return t, oracle.plan(t, addr.shape[0], seg_len, numa, pool)
+
+
+K_ONLY = [dict(layout="bump", name="tiny", blocks=8, slots=4, seg=4096, seed=1),
+          dict(layout="bump", name="bump_s", blocks=37, slots=24, seg=4096, seed=2),
+          dict(layout="worst", blocks=61, slots=18, npos=128, seed=3)]
+
+
+def _check_k_only_plan(wl, p, t, p2, t2):
+    """The plan of a K-only table against the plan of the same table without
+    its V lanes: identical reads and slab; the byte-carrying groups equal the
+    K-only groups field by field; every empty V run sits in a group of chunk
+    0 placed after its node's other groups (so at the end of the node's
+    partition); rebuilt K pointers are unchanged and V pointers are empty
+    ranges at the end of their node's partition."""
+    assert p.status == 0 and p2.status == 0
+    for k in ["remote", "local", "len"]:
+        assert (p.descs[k] == p2.descs[k]).all(), k
+    assert p.slab_bytes == p2.slab_bytes == wl.blocks * int(wl.seg_len.sum())
+    full = p.groups[p.groups["chunk"] > 0]
+    for k in ["base", "stride", "chunk", "local", "block", "count", "node", "dense"]:
+        assert (full[k] == p2.groups[k]).all(), k
+    # group order: node ascending, and inside a node the empty groups last
+    nodes = p.groups["node"]
+    assert (np.diff(nodes.astype(np.int64)) >= 0).all()
+    for n in np.unique(nodes):
+        sel = p.groups[nodes == n]
+        ch = sel["chunk"] == 0
+        assert not (ch[:-1] & ~ch[1:]).any()       # no byte-carrying group after an empty one
+        part_end = int((sel["local"] + sel["count"].astype(np.uint64) * sel["chunk"]).max())
+        assert (sel["local"][ch] == part_end).all()
+    # every V run is in an empty group, every K run in a byte-carrying one
+    L = wl.lanes
+    for l in range(L):
+        r0, r1 = int(p.lane_first[l]), int(p.lane_first[l + 1])
+        ch = p.groups["chunk"][p.run_group[r0:r1]]
+        assert ((ch == 0) == (l % 2 == 1)).all()
+    st, local = oracle.rebuild(t, p, wl.blocks, L, wl.seg_len)
+    assert st == 0
+    _, local2 = oracle.rebuild(t2, p2, wl.blocks, L // 2, wl.seg_len[::2].copy())
+    assert (local[:, ::2] == local2).all()
+    for l in range(1, L, 2):
+        g = p.groups[p.run_group[int(p.lane_first[l])]]
+        assert (local[:, l] == g["local"]).all()
+
+
+@pytest.mark.parametrize("null_v", [False, True])
+@pytest.mark.parametrize("kw", K_ONLY, ids=lambda k: k.get("name", k["layout"]))
+def test_k_only_plan_is_the_k_lanes_plan(kw, null_v):
+    """Empty V segments where the next segment starts (allocation order) or
+    at address 0: either way they move no byte and change no read."""
+    kw = dict(kw)
+    wl = W.k_only(kw.pop("layout"), null_v=null_v, **kw)
+    assert (wl.seg_len[1::2] == 0).all()
+    t, p = _plan_of(wl.addr, wl.seg_len, wl.numa, wl.pool_bytes)
+    a2, s2, n2 = _compressed(wl)
+    t2, p2 = _plan_of(a2, s2, n2, wl.pool_bytes)
+    _check_k_only_plan(wl, p, t, p2, t2)
+
+
+def test_k_only_empty_groups_closed_form():
+    """Bump-allocated K-only tiny table, V at the next segment: each V lane
+    is one run (stride = the block chunk); runs of V lanes are adjacent only
+    through zero lengths (V(j) + 0 != V(j+1)), so every V lane is its own
+    empty group: 2 + 4 groups, 2 reads."""
+    wl = W.k_only("bump", name="tiny", blocks=8, slots=4, seg=4096, seed=1)
+    t, p = _plan_of(wl.addr, wl.seg_len, wl.numa, wl.pool_bytes)
+    assert p.status == 0
+    assert p.groups.size == 6 and p.descs.size == 2
+    assert list(p.groups["chunk"]) == [8192, 0, 0, 8192, 0, 0]
+    assert list(p.groups["local"]) == [0, 65536, 65536, 65536, 131072, 131072]
+
+
+def test_zero_size_k_still_rejected():
+    wl = W.k_only("bump", name="tiny", blocks=8, slots=4, seg=4096, seed=1)
+    t = oracle.encode_runs(wl.addr)
+    sl = wl.seg_len.copy()
+    sl[4] = 0                                      # K of slot 2
+    assert oracle.plan(t, wl.blocks, sl, wl.numa, wl.pool_bytes).status == 16
+
+
+def test_k_only_pack_moves_only_k_bytes():
+    wl = W.k_only("worst", blocks=23, slots=6, npos=64, seed=9)
+    t, p = _plan_of(wl.addr, wl.seg_len, wl.numa, wl.pool_bytes)
+    pool = W.holder_pool_np(wl)
+    slab = np.zeros(p.slab_bytes, np.uint8)
+    assert oracle.pack(pool, p.descs, slab) == 0
+    dst = np.full(wl.pool_bytes, 0xA5, np.uint8)
+    assert oracle.unpack(slab, p.descs, dst) == 0
+    covered = np.zeros(wl.pool_bytes, bool)
+    for b in range(wl.blocks):
+        for l in range(0, wl.lanes, 2):
+            covered[int(wl.addr[b, l]):int(wl.addr[b, l]) + int(wl.seg_len[l])] = True
+    assert (dst[covered] == pool[covered]).all() and (dst[~covered] == 0xA5).all()
