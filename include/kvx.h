@@ -82,7 +82,7 @@ typedef enum kvx_status {
 #define KVX_S_ARRAYS     2u    /* per-lane run counts do not add up to the run arrays' length */
 #define KVX_S_COVERAGE   4u    /* a lane's run counts do not add up to the block count */
 #define KVX_S_ZERO_COUNT 8u    /* a run covers zero blocks */
-#define KVX_S_ZERO_LEN   16u   /* a template lane has segment length 0 */
+#define KVX_S_ZERO_LEN   16u   /* a K lane (even lane) has segment length 0 */
 #define KVX_S_SPAN       32u   /* a run's remote span wraps or leaves the holder pool */
 #define KVX_S_STRIDE1    64u   /* a one-block run with a nonzero stride */
 #define KVX_S_BOUNDS     128u  /* a pointer or copy outside its slab/pool/group range */
@@ -198,15 +198,19 @@ size_t kvx_plan_workspace_size(uint32_t L, uint64_t run_capacity, uint64_t pool_
  *
  * Step 1, validate: table_lanes == template_lanes (else KVX_S_LANES, nothing
  * else checked); per-lane run counts add up to *num_runs, which must be <=
- * run_capacity (KVX_S_ARRAYS); every template segment length > 0
- * (KVX_S_ZERO_LEN); every lane's counts add up to B (KVX_S_COVERAGE); every
+ * run_capacity (KVX_S_ARRAYS); every K lane (even lane, l = 2*slot + kv)
+ * has a segment length > 0 (KVX_S_ZERO_LEN; a V lane of length 0 is a
+ * K-only cache and is accepted); every lane's counts add up to B
+ * (KVX_S_COVERAGE); every
  * count > 0 (KVX_S_ZERO_COUNT); a one-block run has stride 0
  * (KVX_S_STRIDE1); base + i*stride for i in [0, count) plus the segment
  * length stays inside [0, pool_bytes) with exact arithmetic (KVX_S_SPAN).
  * All failing classes are reported together.  On any failure the counts are
  * 0 and nothing else is planned.
  * Step 2: decode each run (lane, first block, node = numa[lane], length =
- * seg_len[lane]) and sort by (node, base, lane, first block).
+ * seg_len[lane]) and sort by (node, empty, base, lane, first block), where
+ * empty = (length == 0): runs that move no byte come after the node's other
+ * runs, so they never split a coalescable stretch.
  * Step 3: walk the sorted runs; a run joins the open group when it has the
  * same node, first block, count and stride, its base equals group base +
  * chunk, and the grown chunk still fits the stride (count == 1, or stride > 0
@@ -214,7 +218,8 @@ size_t kvx_plan_workspace_size(uint32_t L, uint64_t run_capacity, uint64_t pool_
  * Step 4: carve the slab: groups back to back in order (so each NUMA node's
  * groups form one contiguous partition).  A dense group is one read of
  * count*chunk bytes; a non-dense group is one read of chunk bytes per block
- * into a dense local mirror.  Every read is split into 32 MiB pieces.
+ * into a dense local mirror.  Every read is split into 32 MiB pieces.  A
+ * group of empty runs has chunk 0: no slab bytes and no read.
  *
  * Inputs: the run table as kvx_encode_runs writes it (num_runs on the
  * device); B; the slot template seg_len[template_lanes], numa[template_lanes];
@@ -223,7 +228,8 @@ size_t kvx_plan_workspace_size(uint32_t L, uint64_t run_capacity, uint64_t pool_
  * lane_first[table_lanes + 1] (index of each lane's first run, exclusive
  * prefix of runs_per_lane); per run run_block (decoded first block),
  * run_group, run_off (run base - group base);
- * counts[3] = {groups, descriptors, slab bytes} (device).  Capacities below
+ * counts[3] = {groups, descriptors, slab bytes} (device).  run_capacity must
+ * be <= 2^31 (else KVX_EINVAL).  Capacities below
  * run_capacity groups or kvx_desc_capacity() descriptors may end in
  * KVX_S_CAPACITY on the device.
  */

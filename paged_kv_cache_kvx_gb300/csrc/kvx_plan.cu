@@ -44,13 +44,21 @@ struct PlanCtl {
     uint32_t st;
     unsigned long long or_base, and_base;
     uint32_t or_node, and_node;
+    uint32_t or_empty, and_empty;  // some / every run has a zero-size segment
 };
 
+// Sort record; r holds the run index in its low 31 bits and, in the top bit,
+// whether the run's segments are empty (zero-size V lane).
 struct SortItem {
     uint64_t base;
     uint32_t node;
     uint32_t r;
 };
+
+constexpr uint32_t kEmptyBit = 1u << 31;
+constexpr uint32_t kEmptyDigit = 12;  // radix digit of the empty flag
+
+__device__ __forceinline__ uint32_t item_run(const SortItem &it) { return it.r & ~kEmptyBit; }
 
 struct Rec {
     uint64_t base;
@@ -171,8 +179,13 @@ __device__ T reduce_prefix(const T *agg, uint64_t t, Op op, T identity, T *sh) {
     return tot;
 }
 
-__device__ __forceinline__ uint32_t digit_of(uint64_t base, uint32_t node, uint32_t dig) {
-    return dig < 8 ? (uint32_t)(base >> (8 * dig)) & 0xFFu : (node >> (8 * (dig - 8))) & 0xFFu;
+// Radix digits of the sort key (node, empty, base): 0-7 base bytes, 8-11 node
+// bytes, 12 the empty flag (runs of zero-size segments after the others of
+// their node).
+__device__ __forceinline__ uint32_t digit_of(uint64_t base, uint32_t node, uint32_t empty, uint32_t dig) {
+    if (dig < 8) return (uint32_t)(base >> (8 * dig)) & 0xFFu;
+    if (dig == kEmptyDigit) return empty;
+    return (node >> (8 * (dig - 8))) & 0xFFu;
 }
 
 // Largest l with lane_first[l] <= r (lane_first has L + 1 entries).
@@ -225,6 +238,8 @@ __device__ void phase_init(const PlanArgs &a, uint64_t R) {
         ctl->and_base = ~0ull;
         ctl->or_node = 0;
         ctl->and_node = ~0u;
+        ctl->or_empty = 0;
+        ctl->and_empty = 1;
         a.counts[0] = a.counts[1] = a.counts[2] = 0;
     }
     __syncthreads();
@@ -242,7 +257,7 @@ __device__ void phase_init(const PlanArgs &a, uint64_t R) {
             if (i < L) {
                 v = a.rpl[i];
                 const uint32_t len = a.seg_len[i];
-                if (len == 0) mybits |= KVX_S_ZERO_LEN;
+                if (len == 0 && (i & 1u) == 0) mybits |= KVX_S_ZERO_LEN;  // zero-size K slot
                 if (v == 0 && a.B > 0) mybits |= KVX_S_COVERAGE;
                 lensum += len;
             }
@@ -296,7 +311,7 @@ __device__ void phase_decode(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
     __syncthreads();
     uint32_t bits = 0;
     unsigned long long o = 0, an = ~0ull;
-    uint32_t on = 0, ann = ~0u;
+    uint32_t on = 0, ann = ~0u, oe = 0, ae = 1;
     for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
         Seg agg{0, 0, 0};
         const uint64_t r0 = (uint64_t)tile * kTile + (uint64_t)threadIdx.x * kIPT;
@@ -348,6 +363,8 @@ __device__ void phase_decode(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
             an &= base;
             on |= node;
             ann &= node;
+            oe |= len == 0;
+            ae &= len == 0;
         }
         Seg ex, tot;
         block_scan(agg, SegOp(), Seg{0, 0, 0}, sm.seg, &ex, &tot);
@@ -357,6 +374,8 @@ __device__ void phase_decode(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
     bits = __reduce_or_sync(0xFFFFFFFFu, bits);
     on = __reduce_or_sync(0xFFFFFFFFu, on);
     ann = __reduce_and_sync(0xFFFFFFFFu, ann);
+    oe = __reduce_or_sync(0xFFFFFFFFu, oe);
+    ae = __reduce_and_sync(0xFFFFFFFFu, ae);
     const uint32_t o_lo = __reduce_or_sync(0xFFFFFFFFu, (uint32_t)o);
     const uint32_t o_hi = __reduce_or_sync(0xFFFFFFFFu, (uint32_t)(o >> 32));
     const uint32_t a_lo = __reduce_and_sync(0xFFFFFFFFu, (uint32_t)an);
@@ -367,6 +386,8 @@ __device__ void phase_decode(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
         atomicAnd(&s_and, ((unsigned long long)a_hi << 32) | a_lo);
         atomicOr(&s_orn, on);
         atomicAnd(&s_andn, ann);
+        if (oe) atomicOr(&a.ctl->or_empty, 1u);
+        if (!ae) atomicAnd(&a.ctl->and_empty, 0u);
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -378,15 +399,18 @@ __device__ void phase_decode(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
     }
 }
 
-// Active radix digits (base bytes low to high, then node bytes): the bytes in
-// which not all keys agree.  Fewer than two runs need no sort.
+// Active radix digits (base bytes low to high, the empty flag, then node
+// bytes): the digits in which not all keys agree.  Fewer than two runs need
+// no sort.
 __device__ uint32_t active_digits(const PlanArgs &a, uint64_t R, uint32_t *act) {
     const unsigned long long db = __ldcg(&a.ctl->or_base) ^ __ldcg(&a.ctl->and_base);
     const uint32_t dn = __ldcg(&a.ctl->or_node) ^ __ldcg(&a.ctl->and_node);
+    const uint32_t de = __ldcg(&a.ctl->or_empty) ^ __ldcg(&a.ctl->and_empty);
     uint32_t n = 0;
     if (R > 1) {
         for (uint32_t d = 0; d < 8; d++)
             if ((db >> (8 * d)) & 0xFFu) act[n++] = d;
+        if (de) act[n++] = kEmptyDigit;
         for (uint32_t d = 0; d < 4; d++)
             if ((dn >> (8 * d)) & 0xFFu) act[n++] = 8 + d;
     }
@@ -407,7 +431,7 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
         const Seg carry = reduce_prefix(a.seg, tile, SegOp(), Seg{0, 0, 0}, sm.seg);
         const uint64_t r0 = (uint64_t)tile * kTile + (uint64_t)threadIdx.x * kIPT;
         Seg agg{0, 0, 0};
-        uint32_t cnts[kIPT], lanes[kIPT], nodes[kIPT];
+        uint32_t cnts[kIPT], lanes[kIPT], nodes[kIPT], empty[kIPT];
         uint64_t bases[kIPT];
         uint32_t heads = 0;
 #pragma unroll
@@ -426,6 +450,7 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
             const uint64_t r = r0 + j;
             if (r >= R) continue;
             nodes[j] = __ldg(a.numa + lanes[j]);
+            empty[j] = __ldg(a.seg_len + lanes[j]) == 0 ? 1u : 0u;
             const bool head = r == (lf_smem ? s_lf[lanes[j]] : __ldcg(a.lane_first + lanes[j]));
             if (head) heads |= 1u << j;
             agg = SegOp()(agg, Seg{cnts[j], head ? 1u : 0u, 0});
@@ -443,7 +468,7 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
             blk += cnts[j];
             const uint32_t next_first = lf_smem ? s_lf[l + 1] : __ldcg(a.lane_first + l + 1);
             if (r + 1 == (uint64_t)next_first && blk != a.B) bits |= KVX_S_COVERAGE;
-            a.items0[r] = SortItem{bases[j], nodes[j], (uint32_t)r};
+            a.items0[r] = SortItem{bases[j], nodes[j], (uint32_t)r | (empty[j] ? kEmptyBit : 0u)};
         }
         if (nact) {
             // histogram of the first active digit; one shared atomic per distinct
@@ -451,7 +476,7 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
 #pragma unroll
             for (int j = 0; j < kIPT; j++) {
                 const uint64_t r = r0 + j;
-                const uint32_t d = r < R ? digit_of(bases[j], nodes[j], dig0) : kDigits;
+                const uint32_t d = r < R ? digit_of(bases[j], nodes[j], empty[j], dig0) : kDigits;
                 const uint32_t peers = __match_any_sync(0xFFFFFFFFu, d);
                 if (d < kDigits && (threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1))
                     atomicAdd(&s_hist[d], __popc(peers));
@@ -540,7 +565,7 @@ __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint
                 const uint64_t idx = t0 + (uint64_t)j * 32 + lane;
                 if (idx < R) {
                     it[j] = ld_cg(in + idx);
-                    d[j] = digit_of(it[j].base, it[j].node, dig);
+                    d[j] = digit_of(it[j].base, it[j].node, it[j].r >> 31, dig);
                 } else {
                     d[j] = kDigits;  // past the end: matches only other past-the-end lanes
                 }
@@ -573,7 +598,7 @@ __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint
                     if (dst < R) {  // always: the offsets are a permutation of [0, R)
                         out[dst] = it[j];
                         if (has_next)
-                            key = (dst / kTile) * kDigits + digit_of(it[j].base, it[j].node, ndig);
+                            key = (dst / kTile) * kDigits + digit_of(it[j].base, it[j].node, it[j].r >> 31, ndig);
                     }
                 }
                 if (has_next) {  // one atomic per distinct bin in the warp
@@ -587,6 +612,7 @@ __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint
 }
 
 __device__ __forceinline__ Rec make_rec(const PlanArgs &a, SortItem it, uint64_t R) {
+    it.r = item_run(it);
     if (it.r >= R) it.r = 0;  // never taken: sorted items are a permutation of the runs
     Rec x;
     x.base = it.base;
@@ -618,6 +644,7 @@ __device__ void phase_adjacent(const PlanArgs &a, uint64_t R, uint32_t nt, uint3
             its[j].r = 0;
             if (p0 + j < R) {
                 its[j] = ld_cg(sorted + p0 + j);
+                its[j].r = item_run(its[j]);
                 if (its[j].r >= R) its[j].r = 0;  // never taken: a permutation of the runs
             }
         }
@@ -938,7 +965,7 @@ __global__ void __launch_bounds__(kST, 1) k_plan_small(const __grid_constant__ P
     __shared__ CAgg wc[kSW];
     __shared__ uint32_t s_bits;
     __shared__ unsigned long long s_or, s_and;
-    __shared__ uint32_t s_orn, s_andn;
+    __shared__ uint32_t s_orn, s_andn, s_ore, s_ande;
     const uint64_t R = *a.num_runs;
     if (!plan_is_small(a, R)) return;
     const uint32_t tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -949,6 +976,8 @@ __global__ void __launch_bounds__(kST, 1) k_plan_small(const __grid_constant__ P
         s_and = ~0ull;
         s_orn = 0;
         s_andn = ~0u;
+        s_ore = 0;
+        s_ande = 1;
         a.counts[0] = a.counts[1] = a.counts[2] = 0;
     }
     __syncthreads();
@@ -962,7 +991,7 @@ __global__ void __launch_bounds__(kST, 1) k_plan_small(const __grid_constant__ P
         if (i < L) {
             v = a.rpl[i];
             const uint32_t len = a.seg_len[i];
-            if (len == 0) bits |= KVX_S_ZERO_LEN;
+            if (len == 0 && (i & 1u) == 0) bits |= KVX_S_ZERO_LEN;  // zero-size K slot
             if (v == 0 && a.B > 0) bits |= KVX_S_COVERAGE;
             lensum += len;
         }
@@ -1004,7 +1033,7 @@ __global__ void __launch_bounds__(kST, 1) k_plan_small(const __grid_constant__ P
     const uint32_t r0 = 2 * tid;
     bits = 0;
     unsigned long long o = 0, an = ~0ull;
-    uint32_t on = 0, ann = ~0u;
+    uint32_t on = 0, ann = ~0u, oe = 0, ae = 1;
     Seg agg{0, 0, 0};
 #pragma unroll
     for (int j = 0; j < 2; j++) {
@@ -1040,6 +1069,8 @@ __global__ void __launch_bounds__(kST, 1) k_plan_small(const __grid_constant__ P
         an &= base;
         on |= node;
         ann &= node;
+        oe |= len == 0;
+        ae &= len == 0;
     }
     {
         Seg ex, tot;
@@ -1060,6 +1091,8 @@ __global__ void __launch_bounds__(kST, 1) k_plan_small(const __grid_constant__ P
     bits = __reduce_or_sync(0xFFFFFFFFu, bits);
     on = __reduce_or_sync(0xFFFFFFFFu, on);
     ann = __reduce_and_sync(0xFFFFFFFFu, ann);
+    oe = __reduce_or_sync(0xFFFFFFFFu, oe);
+    ae = __reduce_and_sync(0xFFFFFFFFu, ae);
     {
         const uint32_t o_lo = __reduce_or_sync(0xFFFFFFFFu, (uint32_t)o);
         const uint32_t o_hi = __reduce_or_sync(0xFFFFFFFFu, (uint32_t)(o >> 32));
@@ -1071,6 +1104,8 @@ __global__ void __launch_bounds__(kST, 1) k_plan_small(const __grid_constant__ P
             atomicAnd(&s_and, ((unsigned long long)a_hi << 32) | a_lo);
             atomicOr(&s_orn, on);
             atomicAnd(&s_andn, ann);
+            if (oe) atomicOr(&s_ore, 1u);
+            if (!ae) atomicAnd(&s_ande, 0u);
         }
     }
     __syncthreads();
@@ -1080,12 +1115,13 @@ __global__ void __launch_bounds__(kST, 1) k_plan_small(const __grid_constant__ P
     }
 
     // ---- step 2: stable LSD radix sort of run indices on (node, base)
-    uint32_t act[12], nact = 0;
+    uint32_t act[13], nact = 0;
     if (R > 1) {
         const unsigned long long db = s_or ^ s_and;
         const uint32_t dn = s_orn ^ s_andn;
         for (uint32_t d = 0; d < 8; d++)
             if ((db >> (8 * d)) & 0xFFu) act[nact++] = d;
+        if (s_ore ^ s_ande) act[nact++] = kEmptyDigit;
         for (uint32_t d = 0; d < 4; d++)
             if ((dn >> (8 * d)) & 0xFFu) act[nact++] = 8 + d;
     }
@@ -1105,7 +1141,7 @@ __global__ void __launch_bounds__(kST, 1) k_plan_small(const __grid_constant__ P
             item[j] = 0;
             if (p < R) {
                 item[j] = in[p];
-                d[j] = digit_of(S.base[item[j]], S.node[item[j]], dig);
+                d[j] = digit_of(S.base[item[j]], S.node[item[j]], S.len[item[j]] == 0 ? 1u : 0u, dig);
             }
         }
 #pragma unroll
@@ -1298,7 +1334,7 @@ __global__ void __launch_bounds__(kST, 1) k_plan_small(const __grid_constant__ P
 
 __global__ void __launch_bounds__(kT, 2) k_plan(const __grid_constant__ PlanArgs a) {
     __shared__ ScanSmem sm;
-    __shared__ uint32_t s_act[12];
+    __shared__ uint32_t s_act[13];
     __shared__ uint32_t s_nact;
     __shared__ uint32_t s_lf[kLaneSmem];
     const uint64_t R_in = *a.num_runs;
@@ -1447,7 +1483,8 @@ extern "C" kvx_status kvx_plan_groups(const uint32_t *runs_per_lane, uint32_t ta
     if (run_capacity && (!run_base || !run_stride || !run_count || !run_block || !run_group ||
                          !run_off))
         return KVX_EINVAL;
-    if (run_capacity >= (1ull << 32) || table_lanes == 0xFFFFFFFFu) return KVX_EINVAL;
+    // run indices travel in 31 bits of the sort records
+    if (run_capacity > (1ull << 31) || table_lanes == 0xFFFFFFFFu) return KVX_EINVAL;
     if ((group_capacity && !groups) || (desc_capacity && !descs)) return KVX_EINVAL;
     size_t need = 0;
     Ws w = carve(ws, run_capacity, &need);

@@ -348,3 +348,58 @@ def test_verify_encode_full_size_default():
     size = np.tile(wl.seg_len, (B, 1))
     size[700, 301] = 2048
     assert check_verify(wl.addr, size, wl.seg_len) == 700
+
+
+# ------------------------------------------------------- zero-size V lanes
+
+from gpu_helpers import check_all  # noqa: E402
+
+K_ONLY_GPU = [
+    dict(layout="bump", name="tiny", blocks=8, slots=4, seg=4096, seed=1),
+    dict(layout="bump", name="bump_s", blocks=37, slots=24, seg=4096, seed=2),
+    dict(layout="worst", blocks=61, slots=18, npos=128, seed=3),        # single-block planner
+    dict(layout="worst", blocks=301, slots=40, npos=512, seed=4),       # cooperative planner
+]
+
+
+@pytest.mark.parametrize("null_v", [False, True])
+@pytest.mark.parametrize("kw", K_ONLY_GPU, ids=lambda k: f'{k["layout"]}_{k["blocks"]}')
+def test_k_only_bit_exact(kw, null_v):
+    kw = dict(kw)
+    wl = W.k_only(kw.pop("layout"), null_v=null_v, **kw)
+    tr, t, p, local = check_all(wl.addr, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
+    assert (p.groups["chunk"] == 0).any()
+
+
+@pytest.mark.parametrize("kw", K_ONLY_GPU[1:], ids=lambda k: f'{k["layout"]}_{k["blocks"]}')
+def test_k_only_seal_bit_exact(kw):
+    kw = dict(kw)
+    wl = W.k_only(kw.pop("layout"), **kw)
+    B, L = wl.addr.shape
+    dst_addr, size = receiver_layout(B, wl.seg_len, np.random.default_rng(B))
+    assert check_seal(wl.addr, B, wl.seg_len, wl.numa, wl.pool_bytes, dst_addr, size) == 0
+
+
+@pytest.mark.parametrize("kw", [K_ONLY_GPU[0], K_ONLY_GPU[3]], ids=["small", "cooperative"])
+def test_zero_size_k_rejected_on_gpu(kw):
+    kw = dict(kw)
+    wl = W.k_only(kw.pop("layout"), **kw)
+    sl = wl.seg_len.copy()
+    sl[2] = 0
+    t = oracle.encode_runs(wl.addr)
+    assert oracle.plan(t, wl.blocks, sl, wl.numa, wl.pool_bytes).status == oracle.S_ZERO_LEN
+    tr = kvx.Transfer(wl.blocks, sl, wl.numa, wl.pool_bytes)
+    tr.set_addr(wl.addr)
+    tr.encode()
+    tr.plan()
+    torch.cuda.synchronize()
+    assert tr.read_status() == oracle.S_ZERO_LEN
+    assert tr.read_counts() == (0, 0, 0)
+
+
+@pytest.mark.parametrize("layout", ["bump", "worst"])
+def test_k_only_full_size(layout):
+    """The default and worst shapes as K-only caches (288 slots, V lanes of
+    size 0): every run-table, plan and rebuild array bit-exact."""
+    wl = W.k_only(layout)
+    check_all(wl.addr, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes, data=False)
