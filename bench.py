@@ -41,6 +41,7 @@ WORKLOAD = ("default: 1000 blocks x 288 slots x 2 segments (K,V) x 4 KiB uint8 =
             "segments, 2250 MiB, bump-allocated holder, slots 0-143 / 144-287 in two NUMA regions")
 COPY_SRC = os.path.join(ROOT, "paged_kv_cache_kvx_gb300", "csrc", "kvx_copy.cu")
 PROFILE = os.path.join(ROOT, "profiles", "copy_default.md")
+SEGCOPY_SRC = os.path.join(ROOT, "paged_kv_cache_kvx_gb300", "csrc", "kvx_segcopy.cu")
 
 
 def dist_env():
@@ -75,21 +76,21 @@ def load_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def copy_kernel_hash():
-    with open(COPY_SRC, "rb") as f:
+def copy_kernel_hash(src=COPY_SRC):
+    with open(src, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per copy launch from the committed ncu summary, only while
-    the copy kernel's source is the one that was profiled."""
+def profiled_traffic(profile=PROFILE, src=COPY_SRC):
+    """DRAM bytes per launch from a committed ncu summary, only while the
+    kernel's source is the one that was profiled."""
     try:
-        text = open(PROFILE).read()
+        text = open(profile).read()
     except OSError:
         return None
     m = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
     t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m or not t or m.group(1) != copy_kernel_hash():
+    if not m or not t or m.group(1) != copy_kernel_hash(src):
         return None
     return float(t.group(1))
 
@@ -248,7 +249,7 @@ def pool_identity(wl, pool, dst):
     segments tile each used position, so this covers every segment byte)."""
     import torch
     for (first, nslots, base, npos), pos in zip(wl.regions, wl.pos):
-        chunk = 2 * nslots * wl.seg
+        chunk = int(wl.seg_len[2 * first:2 * (first + nslots)].astype(np.int64).sum())
         used = np.zeros(npos, dtype=bool)
         used[pos] = True
         u = torch.from_numpy(used).to(pool.device)
@@ -270,7 +271,10 @@ def run_kvx(args):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     build.build()
-    if args.workload != "default":
+    if args.workload == "konly":
+        wl = W.k_only("bump", name="default")
+        args.no_aux = True
+    elif args.workload != "default":
         wl = W.CONFIGS[args.workload]()
         args.no_aux = True  # the e2e / CPU legs are defined on the default workload
     elif args.blocks == 1000:
@@ -388,7 +392,10 @@ def run_kvx(args):
         "gpu_launches": int(launches),
         "clocks": clocks,
     }
-    if args.workload != "default":
+    if args.workload == "konly":
+        line["config"]["workload"] = ("konly: the default shape as a K-only cache (1000 blocks x 288 "
+                                      "slots, K 4 KiB, V 0 B), 1125 MiB per copy")
+    elif args.workload != "default":
         line["config"]["workload"] = "%s: %d blocks x %d slots x 2 x %d B, %d segments (a parity configuration, not the headline)" % (
             args.workload, wl.blocks, wl.slots, wl.seg, wl.segments)
         line["config"]["bytes_moved_per_step"] = 4 * N
@@ -540,6 +547,212 @@ def measure_e2e(tr, wl, pool, slab, dst, stream, args, dev):
             "copy_streams_per_direction": nchunk, "verified": ok}
 
 
+# ------------------------------------------------- rows beyond the main path
+
+def _events_loop(fn, K, stream):
+    """K calls of fn on stream between two events; returns ms."""
+    import torch
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(K):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b)
+
+
+def _timed_cpu(fn, target_s):
+    fn()
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < target_s:
+        fn()
+        n += 1
+    return (time.perf_counter() - t0) / max(n, 1), n
+
+
+def run_next(args):
+    """--workload paged | seal | verify: the calls that widen the path, each
+    on a full-size input, checked against the oracle / the generator first,
+    then K launches timed with CUDA events on one stream."""
+    import torch
+    import oracle
+    from paged_kv_cache_kvx_gb300 import kvx, workloads as W, build
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    oracle.build()
+    stream = torch.cuda.Stream(device=dev)
+    K = args.steps
+    peak, peak_kind = load_peak()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sampler = ClockSampler(0)
+    line = {"metric": METRIC, "n_gpus": 1, "steps": K, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+            "data": "synthetic", "e2e": None}
+
+    if args.workload == "paged":
+        wl = W.paged_default()
+        src = torch.empty(wl.src_bytes, dtype=torch.uint8, device=dev)
+        W.fill_pool_torch(src, wl.seed)
+        dst = torch.full((wl.dst_bytes,), W.CANARY, dtype=torch.uint8, device=dev)
+        si = torch.from_numpy(wl.src_idx.view(np.int32)).to(dev)
+        di = torch.from_numpy(wl.dst_idx.view(np.int32)).to(dev)
+
+        def call():
+            kvx.kvx_paged_writes(wl.page_len, src, wl.src_bytes, si, wl.src_stride, wl.src_offset,
+                                 dst, wl.dst_bytes, di, wl.dst_stride, wl.dst_offset, wl.num_pages,
+                                 status, stream)
+        call()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        rng = np.random.default_rng(1)
+        for i in rng.integers(0, wl.num_pages, 256):  # sampled pages against the generator
+            d = wl.dst_offset + int(wl.dst_idx[i]) * wl.dst_stride
+            s_ = wl.src_offset + int(wl.src_idx[i]) * wl.src_stride
+            assert np.array_equal(dst[d:d + wl.page_len].cpu().numpy(),
+                                  W.pool_bytes_np(wl.seed, s_, wl.page_len)), i
+        N = wl.bytes_moved
+        unit_bytes = 2 * N
+        cfg = ("paged: 576,000 pages of 4 KiB (2250 MiB) from a 720,000-page pool to a 640,000-page "
+               "pool through seeded permuted page tables (kvx_paged_writes)")
+        kernel = "kvx_paged_writes"
+
+        def cpu_leg():
+            n = 20000  # 80 MiB of 4 KiB pages between two 20,000-page pools, permuted tables
+            small = W.paged("paged_sample", n, wl.page_len, n, n, seed=wl.seed)
+            s_np = W.pool_bytes_np(wl.seed, 0, small.src_bytes)
+            d_np = np.zeros(small.dst_bytes, np.uint8)
+            per, reps = _timed_cpu(lambda: oracle.paged_writes(
+                small.page_len, s_np, small.src_idx, small.src_stride, 0, d_np, small.dst_idx,
+                small.dst_stride, 0), args.cpu_seconds)
+            return (2 * n * wl.page_len / per / 1e9,
+                    "oracle paged_writes, %d pages of 4 KiB between two %d-page pools, %d passes"
+                    % (n, n, reps))
+
+        def status_ok():
+            return int(status.item()) == 0
+    elif args.workload == "seal":
+        wl = W.default()
+        tr = kvx.Transfer(wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes, device=dev)
+        tr.set_addr(wl.addr)
+        pool = torch.empty(wl.pool_bytes, dtype=torch.uint8, device=dev)
+        W.fill_pool_torch(pool, wl.seed)
+        slab = torch.empty(tr.slab_bytes, dtype=torch.uint8, device=dev)
+        tr.encode(stream=stream)
+        tr.plan(stream=stream)
+        tr.pack(pool, slab, stream=stream)
+        B, L, seg = wl.blocks, wl.lanes, wl.seg
+        b = torch.arange(B, dtype=torch.int64, device=dev)[:, None]
+        l = torch.arange(L, dtype=torch.int64, device=dev)[None, :]
+        dst_addr = ((l * B + b) * seg).reshape(-1).contiguous()   # receiver: lane-major
+        dst = torch.full((B * L * seg,), W.CANARY, dtype=torch.uint8, device=dev)
+
+        def call():
+            tr.seal(slab, dst_addr, dst, stream=stream)
+        call()
+        torch.cuda.synchronize()
+        assert tr.read_status() == 0
+        rng = np.random.default_rng(2)
+        for bb, ll in zip(rng.integers(0, B, 256), rng.integers(0, L, 256)):
+            o = (int(ll) * B + int(bb)) * seg
+            assert np.array_equal(dst[o:o + seg].cpu().numpy(),
+                                  W.pool_bytes_np(wl.seed, int(wl.addr[bb, ll]), seg)), (bb, ll)
+        N = wl.payload_bytes
+        unit_bytes = 2 * N
+        cfg = ("seal: the default workload's slab (2250 MiB) installed into a lane-major receiver "
+               "layout with local offsets computed on the fly (kvx_seal_blocks)")
+        kernel = "kvx_seal_blocks"
+
+        def cpu_leg():
+            small = W.bump("seal_sample", blocks=40, slots=288, seg=4096, seed=2)
+            t = oracle.encode_runs(small.addr)
+            p = oracle.plan(t, small.blocks, small.seg_len, small.numa, small.pool_bytes)
+            hp = W.holder_pool_np(small)
+            sl = np.zeros(p.slab_bytes, np.uint8)
+            oracle.pack(hp, p.descs, sl)
+            da = ((np.arange(small.lanes)[None, :] * small.blocks + np.arange(small.blocks)[:, None])
+                  * small.seg).astype(np.uint64)
+            d_np = np.zeros(small.payload_bytes, np.uint8)
+            per, reps = _timed_cpu(lambda: oracle.seal_blocks(
+                t, p, small.blocks, small.lanes, small.seg_len, sl, da, d_np), args.cpu_seconds)
+            return 2 * small.payload_bytes / per / 1e9, "oracle seal_blocks on the first 40 of 1000 blocks, %d passes" % reps
+
+        def status_ok():
+            return tr.read_status() == 0
+    else:  # verify
+        wl = W.default()
+        tr = kvx.Transfer(wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes, device=dev)
+        tr.set_addr(wl.addr)
+        size_np = np.tile(wl.seg_len, (wl.blocks, 1))
+        size = torch.from_numpy(size_np.view(np.int32).reshape(-1).copy()).to(dev)
+        prefix = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def call():
+            tr.verify_encode(size, prefix, stream=stream)
+        # parity: every block passes here; one mismatch at block 700 ends the prefix there
+        bad = size_np.copy()
+        bad[700, 301] = 1
+        dbad = torch.from_numpy(bad.view(np.int32).reshape(-1).copy()).to(dev)
+        tr.verify_encode(dbad, prefix, stream=stream)
+        torch.cuda.synchronize()
+        pre_o, t_o = oracle.verify_encode(wl.addr, bad, wl.seg_len)
+        assert int(prefix.item()) == pre_o == 700
+        rpl, base, stride, count = tr.read_table()
+        assert np.array_equal(count, t_o.run_count) and np.array_equal(base, t_o.run_base)
+        call()
+        torch.cuda.synchronize()
+        assert int(prefix.item()) == wl.blocks and tr.read_status() == 0
+        N = wl.segments
+        unit_bytes = None
+        cfg = ("verify: the default table (576,000 segments) checked block by block against the slot "
+               "template and run-encoded in one cooperative launch (kvx_verify_encode)")
+        kernel = "kvx_verify_encode"
+
+        def cpu_leg():
+            per, reps = _timed_cpu(lambda: oracle.verify_encode(wl.addr, size_np, wl.seg_len),
+                                   args.cpu_seconds)
+            return wl.segments / per / 1e6, "oracle verify_encode on the whole default table, %d passes" % reps
+
+        def status_ok():
+            return tr.read_status() == 0 and int(prefix.item()) == wl.blocks
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    sampler.start()
+    l0 = kvx.kvx_launch_count()
+    with torch.cuda.stream(stream):
+        ms = _events_loop(call, K, stream)
+    launches = kvx.kvx_launch_count() - l0
+    clocks = sampler.stop()
+    assert status_ok()
+    per_ms = ms / K
+    if unit_bytes is not None:
+        value = unit_bytes * K / (ms / 1e3) / 1e9
+        line.update({"value": value, "unit": "GB/s",
+                     "roofline": {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s",
+                                  "frac": value / peak, "traffic": profiled_traffic(
+                                      os.path.join(ROOT, "profiles", "%s_default.md" % args.workload),
+                                      SEGCOPY_SRC), "kernel": kernel,
+                                  "peak_source": "%s hbm_gbs" % peak_kind}})
+    else:
+        value = N * K / (ms / 1e3) / 1e6
+        line.update({"value": value, "unit": "Msegments/s", "roofline": None})
+    line.update({"ms_per_step": per_ms, "gpu_launches": int(launches), "clocks": clocks,
+                 "launch_mode": "stream",
+                 "config": {"workload": cfg, "l2": "inputs larger than L2, no flush"
+                            if unit_bytes else "4.6 MB table (fits L2): latency-bound"}})
+    cb, desc = cpu_leg()
+    line["cpu_baseline"] = {"value": cb, "unit": line["unit"], "cores": 1, "kind": "oracle",
+                            "sample": desc}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def measure_memcpy(pool, slab, N, stream):
     import torch
     src = pool[:N]
@@ -569,8 +782,11 @@ def main(argv=None):
     ap.add_argument("--blocks", type=int, default=1000,
                     help="blocks of the default shape (1000; fewer only for profiler captures)")
     ap.add_argument("--workload", default="default",
-                    choices=["default", "tiny", "worst", "mixed", "many_small", "wide64k"],
-                    help="the default workload is the benchmark; the others are parity configurations")
+                    choices=["default", "tiny", "worst", "mixed", "many_small", "wide64k", "konly",
+                             "paged", "seal", "verify"],
+                    help="the default workload is the benchmark; the others are parity "
+                         "configurations (konly: the default shape as a K-only cache) and the "
+                         "calls beyond the main path (paged, seal, verify)")
     ap.add_argument("--no-aux", action="store_true",
                     help="skip the e2e, memcpy and CPU-baseline legs (profiler captures)")
     args = ap.parse_args(argv)
@@ -578,6 +794,8 @@ def main(argv=None):
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload in ("paged", "seal", "verify"):
+        return run_next(args)
     return run_kvx(args)
 
 

@@ -843,7 +843,7 @@ __device__ void phase_emit(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
                 const uint64_t total = (uint64_t)g.count * g.chunk;
                 for (uint64_t o = 0; o < total; o += M, d++)
                     a.descs[d] = kvx_desc{g.base + o, g.local + o, total - o < M ? total - o : M, gid, 0};
-            } else {
+            } else if (g.chunk > 0) {  // a group of empty runs has no read
                 for (uint64_t i = 0; i < g.count; i++) {
                     const uint64_t rb = g.base + i * (uint64_t)g.stride;
                     const uint64_t lb = g.local + i * g.chunk;
@@ -1314,7 +1314,7 @@ __global__ void __launch_bounds__(kST, 1) k_plan_small(const __grid_constant__ P
             const uint64_t total = (uint64_t)g.count * g.chunk;
             for (uint64_t off = 0; off < total; off += M, dd++)
                 a.descs[dd] = kvx_desc{g.base + off, g.local + off, total - off < M ? total - off : M, gids[j], 0};
-        } else {
+        } else if (g.chunk > 0) {  // a group of empty runs has no read
             for (uint64_t i = 0; i < g.count; i++) {
                 const uint64_t rb = g.base + i * (uint64_t)g.stride;
                 const uint64_t lb = g.local + i * g.chunk;
