@@ -136,6 +136,8 @@ struct PlanArgs {
     int64_t *segmax;
     GAgg *gagg;
     CAgg *cagg;
+    GAgg *gthr;  // per tile and thread: groups before the thread's first run
+    CAgg *cthr;  // per tile and thread: carve prefix inside the tile
 };
 
 union ScanSmem {
@@ -179,13 +181,56 @@ __device__ T reduce_prefix(const T *agg, uint64_t t, Op op, T identity, T *sh) {
     return tot;
 }
 
-// Radix digits of the sort key (node, empty, base): 0-7 base bytes, 8-11 node
-// bytes, 12 the empty flag (runs of zero-size segments after the others of
-// their node).
+// Radix digits of the sort key (node, empty, base), empty = the run's segments
+// have length 0 (such runs come after the others of their node).
+//
+// Packed form (the usual one): only the bit ranges in which the keys differ
+// matter, so the key is re-packed as node bits | empty bit | base bits, each
+// field cut to its differing range (every key agrees outside it, so the order
+// is unchanged), and sorted 8 bits at a time.  A digit descriptor then holds
+// kPacked, the digit index (bits 0-2) and the layout: base shift (3-8) and
+// width (9-15), empty width (16), node shift (17-21) and width (22-27).
+// Byte form (keys wider than 64 bits once packed): 0-7 base bytes, 8-11 node
+// bytes, kEmptyDigit the empty flag.
+constexpr uint32_t kPacked = 1u << 31;
+
+__device__ __forceinline__ uint64_t low_mask(uint32_t w) { return w >= 64 ? ~0ull : (1ull << w) - 1; }
+
 __device__ __forceinline__ uint32_t digit_of(uint64_t base, uint32_t node, uint32_t empty, uint32_t dig) {
+    if (dig & kPacked) {
+        const uint32_t k = dig & 7u, lo_b = (dig >> 3) & 63u, wb = (dig >> 9) & 127u;
+        const uint32_t we = (dig >> 16) & 1u, lo_n = (dig >> 17) & 31u, wn = (dig >> 22) & 63u;
+        uint64_t key = wb ? (base >> lo_b) & low_mask(wb) : 0;
+        if (we) key |= (uint64_t)empty << wb;  // wb < 64 whenever we = 1
+        if (wn) key |= (uint64_t)((node >> lo_n) & low_mask(wn)) << (wb + we);
+        return (uint32_t)(key >> (8 * k)) & 0xFFu;
+    }
     if (dig < 8) return (uint32_t)(base >> (8 * dig)) & 0xFFu;
     if (dig == kEmptyDigit) return empty;
     return (node >> (8 * (dig - 8))) & 0xFFu;
+}
+
+// The radix passes for keys whose bits differ as in db (base), de (empty), dn
+// (node): least significant digit first.  Returns the number of passes.
+__device__ __forceinline__ uint32_t plan_digits(uint64_t db, uint32_t de, uint32_t dn, uint32_t *act) {
+    const uint32_t lo_b = db ? __ffsll((long long)db) - 1 : 0;
+    const uint32_t wb = db ? 64 - __clzll((long long)db) - lo_b : 0;
+    const uint32_t we = de ? 1 : 0;
+    const uint32_t lo_n = dn ? __ffs((int)dn) - 1 : 0;
+    const uint32_t wn = dn ? 32 - __clz((int)dn) - lo_n : 0;
+    const uint32_t W = wb + we + wn;
+    uint32_t n = 0;
+    if (W <= 64) {
+        const uint32_t layout = kPacked | lo_b << 3 | wb << 9 | we << 16 | lo_n << 17 | wn << 22;
+        for (uint32_t k = 0; k * 8 < W; k++) act[n++] = layout | k;
+    } else {
+        for (uint32_t d = 0; d < 8; d++)
+            if ((db >> (8 * d)) & 0xFFu) act[n++] = d;
+        if (de) act[n++] = kEmptyDigit;
+        for (uint32_t d = 0; d < 4; d++)
+            if ((dn >> (8 * d)) & 0xFFu) act[n++] = 8 + d;
+    }
+    return n;
 }
 
 // Largest l with lane_first[l] <= r (lane_first has L + 1 entries).
@@ -399,22 +444,13 @@ __device__ void phase_decode(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
     }
 }
 
-// Active radix digits (base bytes low to high, the empty flag, then node
-// bytes): the digits in which not all keys agree.  Fewer than two runs need
-// no sort.
+// The radix passes over the bits in which not all keys agree.  Fewer than two
+// runs need no sort.
 __device__ uint32_t active_digits(const PlanArgs &a, uint64_t R, uint32_t *act) {
     const unsigned long long db = __ldcg(&a.ctl->or_base) ^ __ldcg(&a.ctl->and_base);
     const uint32_t dn = __ldcg(&a.ctl->or_node) ^ __ldcg(&a.ctl->and_node);
     const uint32_t de = __ldcg(&a.ctl->or_empty) ^ __ldcg(&a.ctl->and_empty);
-    uint32_t n = 0;
-    if (R > 1) {
-        for (uint32_t d = 0; d < 8; d++)
-            if ((db >> (8 * d)) & 0xFFu) act[n++] = d;
-        if (de) act[n++] = kEmptyDigit;
-        for (uint32_t d = 0; d < 4; d++)
-            if ((dn >> (8 * d)) & 0xFFu) act[n++] = 8 + d;
-    }
-    return n;
+    return R > 1 ? plan_digits(db, de, dn, act) : 0;
 }
 
 // Step 2: first block of each run, coverage, sort items, first histogram.
@@ -507,6 +543,7 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
 // scatter, and the next digit's histogram per output tile (atomics into Hn,
 // cleared one pass earlier).  Hz is cleared here for the pass after next.
 constexpr uint32_t kOwnChunk = 8;  // own tiles whose offsets are held at once
+constexpr int kSweep = 32;         // histogram rows loaded at once in the offset sweep
 
 __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P,
                                 const SortItem *in, SortItem *out, const uint32_t *H,
@@ -532,13 +569,13 @@ __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint
         uint64_t run = 0;
         uint32_t next_slot = 0;
         uint32_t next_tile = blockIdx.x + c0 * P;
-        for (uint32_t t = 0; t < nt; t += 8) {
-            uint32_t v[8];
+        for (uint32_t t = 0; t < nt; t += kSweep) {  // kSweep rows in flight per thread
+            uint32_t v[kSweep];
 #pragma unroll
-            for (int u = 0; u < 8; u++)
+            for (int u = 0; u < kSweep; u++)
                 v[u] = t + u < nt ? __ldcg(H + (uint64_t)(t + u) * kDigits + d_me) : 0;
 #pragma unroll
-            for (int u = 0; u < 8; u++) {
+            for (int u = 0; u < kSweep; u++) {
                 if (t + u == next_tile && next_slot < kOwnChunk && c0 + next_slot < own) {
                     s_off[next_slot][d_me] = (uint32_t)run;
                     next_slot++;
@@ -693,31 +730,49 @@ __device__ void phase_cut(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P
     for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
         const int64_t carry = reduce_prefix(a.segmax, tile, MaxOp(), (int64_t)-1, sm.i64);
         const uint64_t p0 = (uint64_t)tile * kTile + (uint64_t)threadIdx.x * kIPT;
-        int64_t mx = -1;
+        // every load of this thread's runs first
+        uint32_t cm = 0;  // bit j: position p0 + j is compatible with its predecessor
+        uint64_t xb[kIPT];
+        int64_t xs[kIPT];
+        uint32_t xc[kIPT], xl[kIPT];
+#pragma unroll
         for (int j = 0; j < kIPT; j++) {
             const uint64_t p = p0 + j;
-            if (p < R && !__ldcg(a.compat + p)) mx = (int64_t)p;
+            if (p < R) {
+                const Rec *q = a.rec + p;
+                if (__ldcg(a.compat + p)) cm |= 1u << j;
+                xb[j] = __ldcg(&q->base);
+                xs[j] = __ldcg(&q->stride);
+                xc[j] = __ldcg(&q->count);
+                xl[j] = __ldcg(&q->len);
+            }
         }
+        int64_t mx = -1;
+#pragma unroll
+        for (int j = 0; j < kIPT; j++)
+            if (p0 + j < R && !(cm >> j & 1u)) mx = (int64_t)(p0 + j);
         int64_t ex, tot;
         block_scan(mx, MaxOp(), (int64_t)-1, sm.i64, &ex, &tot);
-        int64_t s = carry > ex ? carry : ex;  // stretch start before this thread's first run
+        const int64_t s0 = carry > ex ? carry : ex;  // stretch start before this thread's first run
+        uint64_t s_base = 0;                          // base of the current stretch's first run
+        if (p0 < R && (cm & 1u)) s_base = __ldcg(&a.rec[s0 > 0 ? s0 : 0].base);
+#pragma unroll
         for (int j = 0; j < kIPT; j++) {
             const uint64_t p = p0 + j;
             if (p >= R) break;
-            const bool c = __ldcg(a.compat + p) != 0;
-            if (!c) s = (int64_t)p;
-            const Rec x = ld_cg(a.rec + p);
-            if (x.count == 1) {
+            const bool c = cm >> j & 1u;
+            if (!c) s_base = xb[j];
+            if (xc[j] == 1) {
                 a.gflag[p] = c ? 0 : 1;
                 continue;
             }
-            if (x.stride <= 0) {
+            if (xs[j] <= 0) {
                 a.gflag[p] = 1;  // a non-positive stride never fits: one run per group
                 continue;
             }
-            const uint64_t stride = (uint64_t)x.stride;
-            const uint64_t O = x.base - ld_cg(a.rec + (s > 0 ? s : 0)).base;  // offset in the stretch
-            const uint64_t E = O + x.len;
+            const uint64_t stride = (uint64_t)xs[j];
+            const uint64_t O = xb[j] - s_base;  // offset in the stretch
+            const uint64_t E = O + xl[j];
             if (E <= stride) {
                 a.gflag[p] = c ? 0 : 1;
             } else if (O <= stride) {
@@ -725,7 +780,7 @@ __device__ void phase_cut(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P
                 // rest of the stretch in order (only tables whose block chunks
                 // exceed their stride get here).
                 a.gflag[p] = 1;
-                uint64_t cur = x.base;
+                uint64_t cur = xb[j];
                 for (uint64_t q = p + 1; q < R && __ldcg(a.compat + q); q++) {
                     const Rec y = ld_cg(a.rec + q);
                     if (y.base + y.len - cur > stride) {
@@ -759,46 +814,90 @@ __device__ void phase_count(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t
 }
 
 // Group records, run_group / run_off; per tile the carve bytes and pieces.
+// Every load a thread needs is issued up front (flags, the fields of its
+// runs, and the fields of the runs that start groups), so a thread pays one
+// round trip per dependency level rather than one per run.  The thread's
+// group count and carve prefix inside the tile are kept for the emit phase.
 __device__ void phase_groups(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, ScanSmem &sm) {
     for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
         const GAgg carry = reduce_prefix(a.gagg, tile, GOp(), GAgg{0, -1}, sm.g);
         const uint64_t p0 = (uint64_t)tile * kTile + (uint64_t)threadIdx.x * kIPT;
-        GAgg g{0, -1};
+        uint32_t fl = 0;  // bit j: position p0 + j starts a group (bit kIPT: the next one, or R)
+#pragma unroll
+        for (int j = 0; j <= kIPT; j++) {
+            const uint64_t p = p0 + j;
+            const uint32_t v = p < R ? (__ldcg(a.gflag + p) ? 1u : 0u) : (p == R ? 1u : 0u);
+            fl |= v << j;
+        }
+        uint64_t xb[kIPT];
+        uint32_t xr[kIPT], xl[kIPT];
+        int64_t gs[kIPT];
+        uint32_t gb[kIPT], gc[kIPT], gn[kIPT];
+#pragma unroll
         for (int j = 0; j < kIPT; j++) {
             const uint64_t p = p0 + j;
-            if (p < R && __ldcg(a.gflag + p)) {
-                g.n++;
-                g.last = (int64_t)p;
+            if (p < R) {
+                const Rec *q = a.rec + p;
+                xb[j] = __ldcg(&q->base);
+                xl[j] = __ldcg(&q->len);
+                xr[j] = __ldcg(&q->r);
+                if (fl >> j & 1u) {
+                    gs[j] = __ldcg(&q->stride);
+                    gb[j] = __ldcg(&q->block);
+                    gc[j] = __ldcg(&q->count);
+                    gn[j] = __ldcg(&q->node);
+                }
             }
         }
+        GAgg g{0, -1};
+#pragma unroll
+        for (int j = 0; j < kIPT; j++)
+            if (p0 + j < R && (fl >> j & 1u)) {
+                g.n++;
+                g.last = (int64_t)(p0 + j);
+            }
         GAgg ex, tot;
         block_scan(g, GOp(), GAgg{0, -1}, sm.g, &ex, &tot);
         GAgg run = GOp()(carry, ex);
+        if (p0 < R) a.gthr[(uint64_t)tile * kT + threadIdx.x] = run;
+        // the group open at this thread's first run (position 0 always starts one)
+        uint64_t g_base = 0, g_block = 0, g_count = 0, g_node = 0;
+        int64_t g_stride = 0;
+        if (p0 < R && !(fl & 1u)) {
+            const Rec *q = a.rec + (run.last >= 0 ? run.last : 0);
+            g_base = __ldcg(&q->base);
+            g_stride = __ldcg(&q->stride);
+            g_block = __ldcg(&q->block);
+            g_count = __ldcg(&q->count);
+            g_node = __ldcg(&q->node);
+        }
         CAgg c{0, 0};
+#pragma unroll
         for (int j = 0; j < kIPT; j++) {
             const uint64_t p = p0 + j;
             if (p >= R) break;
-            if (__ldcg(a.gflag + p)) {
+            if (fl >> j & 1u) {
                 run.n++;
-                run.last = (int64_t)p;
+                g_base = xb[j];
+                g_stride = gs[j];
+                g_block = gb[j];
+                g_count = gc[j];
+                g_node = gn[j];
             }
             const uint64_t gid = run.n - 1;
-            const Rec x = ld_cg(a.rec + p);
-            const Rec g0 = ld_cg(a.rec + (run.last >= 0 ? run.last : 0));  // position 0 starts a group
-            const uint64_t off = x.base - g0.base;
-            a.run_group[x.r] = (uint32_t)gid;
-            a.run_off[x.r] = off;
-            const bool end = p + 1 == R || __ldcg(a.gflag + p + 1);
-            if (end) {
+            const uint64_t off = xb[j] - g_base;
+            a.run_group[xr[j]] = (uint32_t)gid;
+            a.run_off[xr[j]] = off;
+            if (fl >> (j + 1) & 1u) {  // the group ends here
                 kvx_group G;
-                G.base = g0.base;
-                G.stride = g0.stride;
-                G.chunk = off + x.len;
+                G.base = g_base;
+                G.stride = g_stride;
+                G.chunk = off + xl[j];
                 G.local = 0;
-                G.block = g0.block;
-                G.count = g0.count;
-                G.node = g0.node;
-                G.dense = group_dense(g0.count, g0.stride, G.chunk) ? 1u : 0u;
+                G.block = (uint32_t)g_block;
+                G.count = (uint32_t)g_count;
+                G.node = (uint32_t)g_node;
+                G.dense = group_dense(G.count, G.stride, G.chunk) ? 1u : 0u;
                 a.groups[gid] = G;
                 c.bytes += (uint64_t)G.count * G.chunk;
                 c.descs += group_pieces(G);
@@ -806,38 +905,46 @@ __device__ void phase_groups(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
         }
         CAgg cex, ctot;
         block_scan(c, COp(), CAgg{0, 0}, sm.c, &cex, &ctot);
+        if (p0 < R) a.cthr[(uint64_t)tile * kT + threadIdx.x] = cex;
         if (threadIdx.x == 0) a.cagg[tile] = ctot;
     }
 }
 
-// Step 4: carve and descriptors.
+// Step 4: carve and descriptors.  A thread takes its group count and carve
+// prefix from the groups phase, so each group end costs one load of its
+// record (all of them issued at once).
 __device__ void phase_emit(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, ScanSmem &sm) {
     for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
         const CAgg carry = reduce_prefix(a.cagg, tile, COp(), CAgg{0, 0}, sm.c);
         const uint64_t p0 = (uint64_t)tile * kTile + (uint64_t)threadIdx.x * kIPT;
-        CAgg c{0, 0};
-        uint32_t ends = 0;
-        for (int j = 0; j < kIPT; j++) {
+        if (p0 >= R) continue;
+        uint32_t fl = 0;
+#pragma unroll
+        for (int j = 0; j <= kIPT; j++) {
             const uint64_t p = p0 + j;
-            if (p >= R) break;
-            if (p + 1 == R || __ldcg(a.gflag + p + 1)) {
-                ends |= 1u << j;
-                const kvx_group g = ld_cg(a.groups + __ldcg(a.run_group + ld_cg(a.rec + p).r));
-                c.bytes += (uint64_t)g.count * g.chunk;
-                c.descs += group_pieces(g);
-            }
+            const uint32_t v = p < R ? (__ldcg(a.gflag + p) ? 1u : 0u) : (p == R ? 1u : 0u);
+            fl |= v << j;
         }
-        CAgg ex, tot;
-        block_scan(c, COp(), CAgg{0, 0}, sm.c, &ex, &tot);
-        CAgg cur = COp()(carry, ex);
+        const GAgg run0 = ld_cg(a.gthr + (uint64_t)tile * kT + threadIdx.x);
+        const CAgg cex = ld_cg(a.cthr + (uint64_t)tile * kT + threadIdx.x);
+        uint32_t gids[kIPT];
+        kvx_group G[kIPT];
+        uint64_t n = run0.n;
+#pragma unroll
         for (int j = 0; j < kIPT; j++) {
-            if (!(ends >> j & 1u)) continue;
-            const uint64_t p = p0 + j;
-            const uint32_t gid = __ldcg(a.run_group + ld_cg(a.rec + p).r);
-            kvx_group g = ld_cg(a.groups + gid);
+            if (p0 + j < R && (fl >> j & 1u)) n++;
+            gids[j] = (uint32_t)(n - 1);
+            if (p0 + j < R && (fl >> (j + 1) & 1u)) G[j] = ld_cg(a.groups + gids[j]);
+        }
+        CAgg cur = COp()(carry, cex);
+        const uint64_t M = KVX_MAX_READ_BYTES;
+#pragma unroll
+        for (int j = 0; j < kIPT; j++) {
+            if (p0 + j >= R || !(fl >> (j + 1) & 1u)) continue;
+            kvx_group g = G[j];
+            const uint32_t gid = gids[j];
             g.local = cur.bytes;
             a.groups[gid].local = cur.bytes;
-            const uint64_t M = KVX_MAX_READ_BYTES;
             uint64_t d = cur.descs;
             if (g.dense) {
                 const uint64_t total = (uint64_t)g.count * g.chunk;
@@ -1116,15 +1223,7 @@ __global__ void __launch_bounds__(kST, 1) k_plan_small(const __grid_constant__ P
 
     // ---- step 2: stable LSD radix sort of run indices on (node, base)
     uint32_t act[13], nact = 0;
-    if (R > 1) {
-        const unsigned long long db = s_or ^ s_and;
-        const uint32_t dn = s_orn ^ s_andn;
-        for (uint32_t d = 0; d < 8; d++)
-            if ((db >> (8 * d)) & 0xFFu) act[nact++] = d;
-        if (s_ore ^ s_ande) act[nact++] = kEmptyDigit;
-        for (uint32_t d = 0; d < 4; d++)
-            if ((dn >> (8 * d)) & 0xFFu) act[nact++] = 8 + d;
-    }
+    if (R > 1) nact = plan_digits(s_or ^ s_and, s_ore ^ s_ande, s_orn ^ s_andn, act);
     for (uint32_t r = tid; r < R; r += kST) S.idx[0][r] = (uint16_t)r;
     const uint32_t lt_mask = (1u << lane) - 1u;
     for (uint32_t k = 0; k < nact; k++) {
@@ -1412,6 +1511,8 @@ struct Ws {
     int64_t *segmax;
     GAgg *gagg;
     CAgg *cagg;
+    GAgg *gthr;
+    CAgg *cthr;
 };
 
 Ws carve(void *base, uint64_t run_cap, size_t *bytes) {
@@ -1430,6 +1531,8 @@ Ws carve(void *base, uint64_t run_cap, size_t *bytes) {
     w.segmax = c.take<int64_t>(ntc);
     w.gagg = c.take<GAgg>(ntc);
     w.cagg = c.take<CAgg>(ntc);
+    w.gthr = c.take<GAgg>(ntc * kT);
+    w.cthr = c.take<CAgg>(ntc * kT);
     *bytes = c.off;
     return w;
 }
@@ -1525,6 +1628,8 @@ extern "C" kvx_status kvx_plan_groups(const uint32_t *runs_per_lane, uint32_t ta
     a.segmax = w.segmax;
     a.gagg = w.gagg;
     a.cagg = w.cagg;
+    a.gthr = w.gthr;
+    a.cthr = w.cthr;
     static bool small_ready[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
