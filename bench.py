@@ -602,10 +602,12 @@ def run_next(args):
         si = torch.from_numpy(wl.src_idx.view(np.int32)).to(dev)
         di = torch.from_numpy(wl.dst_idx.view(np.int32)).to(dev)
 
+        seg_ws = torch.zeros(kvx.kvx_segcopy_workspace_size(), dtype=torch.uint8, device=dev)
+
         def call():
             kvx.kvx_paged_writes(wl.page_len, src, wl.src_bytes, si, wl.src_stride, wl.src_offset,
                                  dst, wl.dst_bytes, di, wl.dst_stride, wl.dst_offset, wl.num_pages,
-                                 status, stream)
+                                 status, seg_ws, stream)
         call()
         torch.cuda.synchronize()
         assert int(status.item()) == 0

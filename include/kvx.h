@@ -310,6 +310,9 @@ kvx_status kvx_unpack(const uint8_t *slab, uint64_t slab_bytes,
 
 /* -------------------------------------------- seal from template metadata */
 
+/* Scratch for kvx_seal_blocks / kvx_paged_writes on their bulk-copy path. */
+size_t kvx_segcopy_workspace_size(void);
+
 /*
  * Seal the fetched blocks into the receiver's cache (pegaflow PR #350: the
  * follow-up named after the stage breakdown, "seal from template metadata",
@@ -325,7 +328,15 @@ kvx_status kvx_unpack(const uint8_t *slab, uint64_t slab_bytes,
  * Inputs: the plan outputs as for kvx_rebuild; the slab (read, slab_bytes);
  * dst_addr [B][L] uint64 byte offsets into dst (block-major); dst, dst_bytes.
  * Destination ranges must not overlap each other (else the overlap holds
- * undefined bytes) and must not overlap the slab.  No workspace; one launch.
+ * undefined bytes) and must not overlap the slab.
+ *
+ * ws, ws_bytes: optional scratch of kvx_segcopy_workspace_size() bytes.
+ * With it the copy runs through the SM's bulk-copy engine (shared-memory
+ * rings fed by cp.async.bulk, batches claimed from a counter in ws, which
+ * the call zeroes); with ws == NULL through registers (16-byte vectors),
+ * allocation-free.  Both give the same bytes.  On GB300 the bulk path is the
+ * faster one for segments of 2 KiB and more, the register path for shorter
+ * ones.  One launch (plus a memset of ws).
  */
 kvx_status kvx_seal_blocks(const uint32_t *lane_first, const uint32_t *run_block,
                            const uint32_t *run_group, const uint64_t *run_off,
@@ -334,7 +345,8 @@ kvx_status kvx_seal_blocks(const uint32_t *lane_first, const uint32_t *run_block
                            uint32_t B, uint32_t L, const uint32_t *seg_len,
                            const uint8_t *slab, uint64_t slab_bytes,
                            const uint64_t *dst_addr, uint8_t *dst,
-                           uint64_t dst_bytes, uint32_t *status, void *stream);
+                           uint64_t dst_bytes, uint32_t *status, void *ws,
+                           size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------ paged writes */
 
@@ -352,7 +364,10 @@ kvx_status kvx_seal_blocks(const uint32_t *lane_first, const uint32_t *run_block
  *
  *   src_indices, dst_indices  [num_pages] uint32 (device).
  *   src, dst                  device buffers of src_bytes / dst_bytes.
- * No workspace; one launch.  num_pages == 0 enqueues nothing.
+ *   ws, ws_bytes              optional, as for kvx_seal_blocks: with it, pages
+ *                             of 2 KiB or more take the bulk-copy path; without
+ *                             it, or for shorter pages, the register path.
+ * One launch.  num_pages == 0 enqueues nothing.
  */
 kvx_status kvx_paged_writes(uint64_t page_len,
                             const uint8_t *src, uint64_t src_bytes,
@@ -361,7 +376,8 @@ kvx_status kvx_paged_writes(uint64_t page_len,
                             uint8_t *dst, uint64_t dst_bytes,
                             const uint32_t *dst_indices, uint64_t dst_stride,
                             uint64_t dst_offset,
-                            uint64_t num_pages, uint32_t *status, void *stream);
+                            uint64_t num_pages, uint32_t *status,
+                            void *ws, size_t ws_bytes, void *stream);
 
 /*
  * kvx_pack without a caller workspace, for callers that cannot allocate

@@ -55,10 +55,11 @@ _SIGS = {
     "kvx_pack_noalloc": (ctypes.c_int, [_P, _U64, _P, _P, _U64, _P, _U64, _P, _P]),
     "kvx_verify_encode": (ctypes.c_int, [_P, _P, _P, _U32, _U32, _P, _P, _P, _P, _P, _U64, _P, _P,
                                          _P, _SZ, _P]),
+    "kvx_segcopy_workspace_size": (_SZ, []),
     "kvx_seal_blocks": (ctypes.c_int, [_P, _P, _P, _P, _U64, _P, _U64, _P, _U32, _U32, _P, _P, _U64,
-                                       _P, _P, _U64, _P, _P]),
+                                       _P, _P, _U64, _P, _P, _SZ, _P]),
     "kvx_paged_writes": (ctypes.c_int, [_U64, _P, _U64, _P, _U64, _U64, _P, _U64, _P, _U64, _U64,
-                                        _U64, _P, _P]),
+                                        _U64, _P, _P, _SZ, _P]),
     "kvx_selftest_timeouts": (ctypes.c_int, [_P, _P]),
     "kvx_launch_count": (_U64, []),
     "kvx_version": (_U32, []),
@@ -192,20 +193,29 @@ def kvx_verify_encode(addr, seg_size, seg_len, B, L, prefix_blocks, runs_per_lan
            "kvx_verify_encode")
 
 
+def kvx_segcopy_workspace_size() -> int:
+    return int(lib().kvx_segcopy_workspace_size())
+
+
 def kvx_seal_blocks(lane_first, run_block, run_group, run_off, run_capacity, groups,
                     group_capacity, counts, B, L, seg_len, slab, slab_bytes, dst_addr, dst,
-                    dst_bytes, status, stream=None):
+                    dst_bytes, status, ws=None, stream=None):
+    """ws (a uint8 device tensor of kvx_segcopy_workspace_size() bytes) selects the
+    bulk-copy path; None the register path."""
     _check(lib().kvx_seal_blocks(_ptr(lane_first), _ptr(run_block), _ptr(run_group), _ptr(run_off),
                                  run_capacity, _ptr(groups), group_capacity, _ptr(counts), B, L,
                                  _ptr(seg_len), _ptr(slab), slab_bytes, _ptr(dst_addr), _ptr(dst),
-                                 dst_bytes, _ptr(status), _stream(stream)), "kvx_seal_blocks")
+                                 dst_bytes, _ptr(status), _ptr(ws), 0 if ws is None else ws.numel(),
+                                 _stream(stream)), "kvx_seal_blocks")
 
 
 def kvx_paged_writes(page_len, src, src_bytes, src_indices, src_stride, src_offset, dst, dst_bytes,
-                     dst_indices, dst_stride, dst_offset, num_pages, status, stream=None):
+                     dst_indices, dst_stride, dst_offset, num_pages, status, ws=None, stream=None):
+    """ws as for kvx_seal_blocks."""
     _check(lib().kvx_paged_writes(page_len, _ptr(src), src_bytes, _ptr(src_indices), src_stride,
                                   src_offset, _ptr(dst), dst_bytes, _ptr(dst_indices), dst_stride,
-                                  dst_offset, num_pages, _ptr(status), _stream(stream)),
+                                  dst_offset, num_pages, _ptr(status), _ptr(ws),
+                                  0 if ws is None else ws.numel(), _stream(stream)),
            "kvx_paged_writes")
 
 
@@ -242,6 +252,7 @@ class Transfer:
         numa = np.asarray(numa, dtype=np.uint32)
         self.B = int(B)
         self.L = int(seg_len.size)
+        self.seg_len_host = seg_len.copy()
         self.pool_bytes = int(pool_bytes)
         self.device = torch.device(device)
         L, dev = self.L, self.device
@@ -273,6 +284,7 @@ class Transfer:
         self.plan_ws = torch.empty(kvx_plan_workspace_size(L, self.run_cap, self.pool_bytes),
                                    dtype=u8, device=dev)
         self.copy_ws = torch.empty(kvx_copy_workspace_size(self.slab_bytes), dtype=u8, device=dev)
+        self.seg_ws = torch.empty(kvx_segcopy_workspace_size(), dtype=u8, device=dev)
 
     # -- the five calls ------------------------------------------------
     def encode(self, addr=None, stream=None):
@@ -313,12 +325,18 @@ class Transfer:
         kvx_unpack(slab, slab.numel(), self.descs, self.counts[1:], self.desc_cap, dst_pool,
                    dst_pool.numel(), self.status, self.copy_ws, stream)
 
-    def seal(self, slab, dst_addr, dst, stream=None):
+    def seal(self, slab, dst_addr, dst, stream=None, bulk=None):
         """Install every segment from the slab at dst[dst_addr[b][l]] (seal
-        from template metadata; no local table is written)."""
+        from template metadata; no local table is written).  bulk selects the
+        bulk-copy path (True) or the register path (False); by default the
+        bulk path when every non-empty segment is at least 2 KiB."""
+        if bulk is None:
+            sl = self.seg_len_host[self.seg_len_host > 0]
+            bulk = bool(sl.size) and int(sl.min()) >= 2048
         kvx_seal_blocks(self.lane_first, self.run_block, self.run_group, self.run_off, self.run_cap,
                         self.groups, self.group_cap, self.counts, self.B, self.L, self.seg_len,
-                        slab, slab.numel(), dst_addr, dst, dst.numel(), self.status, stream)
+                        slab, slab.numel(), dst_addr, dst, dst.numel(), self.status,
+                        self.seg_ws if bulk else None, stream)
 
     def step(self, pool, slab, dst_pool, stream=None, side=None):
         """One pass of the whole path: encode, plan, rebuild, pack, unpack.

@@ -28,24 +28,32 @@ def _u32_dev(a):
 
 # --------------------------------------------------------------- paged writes
 
-def gpu_paged(page_len, src, s_idx, s_stride, s_off, dst, d_idx, d_stride, d_off):
+def _seg_ws():
+    return torch.zeros(kvx.kvx_segcopy_workspace_size(), dtype=torch.uint8, device="cuda")
+
+
+def gpu_paged(page_len, src, s_idx, s_stride, s_off, dst, d_idx, d_stride, d_off, bulk=True):
     """Run kvx_paged_writes on copies of the host buffers; returns (status, dst)."""
     dsrc = _dev(src if src.size else np.zeros(1, np.uint8))
     ddst = _dev(dst if dst.size else np.zeros(1, np.uint8))
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     n = len(s_idx)
     kvx.kvx_paged_writes(page_len, dsrc, src.size, _u32_dev(s_idx), s_stride, s_off, ddst,
-                         dst.size, _u32_dev(d_idx), d_stride, d_off, n, status)
+                         dst.size, _u32_dev(d_idx), d_stride, d_off, n, status,
+                         _seg_ws() if bulk else None)
     torch.cuda.synchronize()
     return int(status.cpu().numpy().view(np.uint32)[0]), ddst.cpu().numpy()[: dst.size]
 
 
 def check_paged(page_len, src, s_idx, s_stride, s_off, dst, d_idx, d_stride, d_off):
+    """Both copy paths (bulk-copy ring and registers) against the oracle."""
     want = dst.copy()
     st_o = oracle.paged_writes(page_len, src, s_idx, s_stride, s_off, want, d_idx, d_stride, d_off)
-    st_g, got = gpu_paged(page_len, src, s_idx, s_stride, s_off, dst, d_idx, d_stride, d_off)
-    assert st_g == st_o
-    assert np.array_equal(got, want)
+    for bulk in (True, False):
+        st_g, got = gpu_paged(page_len, src, s_idx, s_stride, s_off, dst, d_idx, d_stride, d_off,
+                              bulk)
+        assert st_g == st_o, bulk
+        assert np.array_equal(got, want), bulk
     return st_o
 
 
@@ -54,13 +62,14 @@ def _golden():
         return json.load(f)["cases"]
 
 
+@pytest.mark.parametrize("bulk", [True, False])
 @pytest.mark.parametrize("case", _golden(), ids=lambda c: c["name"])
-def test_paged_hand_fixtures_on_gpu(case):
+def test_paged_hand_fixtures_on_gpu(case, bulk):
     src = np.arange(case["src_bytes"], dtype=np.uint64).astype(np.uint8)
     dst = np.zeros(case["dst_bytes"], np.uint8)
     st, got = gpu_paged(case["page_len"], src, case["src_idx"], case["src_stride"],
                         case["src_offset"], dst, case["dst_idx"], case["dst_stride"],
-                        case["dst_offset"])
+                        case["dst_offset"], bulk)
     assert st == case["status"]
     assert got.tolist() == case["dst"]
 
@@ -70,7 +79,8 @@ def test_paged_hand_fixtures_on_gpu(case):
 # addresses (byte path)
 PAGED_SHAPES = [
     (16, 0, 0), (48, 16, 32), (512, 0, 4096), (4096, 0, 0), (4096, 64, 128),
-    (65536, 0, 0), (65552, 16, 0), (131072, 0, 65536), (4100, 0, 0), (4096, 3, 0),
+    (1024, 0, 0), (2048, 16, 0), (65536, 0, 0), (65552, 16, 0), (131072, 0, 65536),
+    (4100, 0, 0), (4096, 3, 0),
     (4096, 0, 5), (1, 7, 9), (33, 1, 2),
 ]
 
@@ -117,7 +127,8 @@ def test_paged_empty():
     assert check_paged(0, src, [1, 2], 16, 0, dst, [0, 1], 16, 0) == 0
 
 
-def test_paged_full_size():
+@pytest.mark.parametrize("bulk", [True, False])
+def test_paged_full_size(bulk):
     """The benchmark's paged workload (576,000 pages of 4 KiB, 2250 MiB moved
     between two page pools by permuted page tables): every destination page
     checked against the generator's bytes of its source page on the device,
@@ -129,7 +140,7 @@ def test_paged_full_size():
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     kvx.kvx_paged_writes(wl.page_len, src, wl.src_bytes, _u32_dev(wl.src_idx), wl.src_stride,
                          wl.src_offset, dst, wl.dst_bytes, _u32_dev(wl.dst_idx), wl.dst_stride,
-                         wl.dst_offset, wl.num_pages, status)
+                         wl.dst_offset, wl.num_pages, status, _seg_ws() if bulk else None)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     P = wl.page_len
@@ -184,15 +195,16 @@ def check_seal(addr, B, seg_len, numa, pool_bytes, dst_addr, dst_bytes, groups=N
     st_o = oracle.seal_blocks(t, p, B, L, seg_len, slab, dst_addr, want[:dst_bytes],
                               groups=groups, slab_bytes=sb)
     dslab = _dev(slab)
-    ddst = torch.full((max(1, dst_bytes),), 0xA5, dtype=torch.uint8, device="cuda")
     daddr = _dev(np.ascontiguousarray(dst_addr, np.uint64).view(np.int64).reshape(-1))
-    tr.status.zero_()
-    kvx.kvx_seal_blocks(tr.lane_first, tr.run_block, tr.run_group, tr.run_off, tr.run_cap,
-                        tr.groups, tr.group_cap, tr.counts, B, L, tr.seg_len, dslab, sb, daddr,
-                        ddst, dst_bytes, tr.status)
-    torch.cuda.synchronize()
-    assert tr.read_status() == st_o
-    assert np.array_equal(ddst.cpu().numpy(), want)
+    for bulk in (True, False):
+        ddst = torch.full((max(1, dst_bytes),), 0xA5, dtype=torch.uint8, device="cuda")
+        tr.status.zero_()
+        kvx.kvx_seal_blocks(tr.lane_first, tr.run_block, tr.run_group, tr.run_off, tr.run_cap,
+                            tr.groups, tr.group_cap, tr.counts, B, L, tr.seg_len, dslab, sb, daddr,
+                            ddst, dst_bytes, tr.status, _seg_ws() if bulk else None)
+        torch.cuda.synchronize()
+        assert tr.read_status() == st_o, bulk
+        assert np.array_equal(ddst.cpu().numpy(), want), bulk
     return st_o
 
 
@@ -215,6 +227,20 @@ def test_seal_random_holders_bit_exact():
         addr, seg_len, numa, pool = random_holder(rng, B, int(rng.integers(1, 9)), int(rng.integers(1, 4)))
         dst_addr, size = receiver_layout(B, seg_len, rng, lane_major=bool(rng.integers(0, 2)))
         assert check_seal(addr, B, seg_len, numa, pool, dst_addr, size) == 0
+
+
+def test_seal_long_segments_in_rounds():
+    """64 KiB and 20 KiB segments: the bulk path moves them in 16 KiB rounds."""
+    B, slots = 9, 3
+    L = 2 * slots
+    seg_len = np.array([65536, 20480] * slots, np.uint32)
+    per_block = int(seg_len.sum())
+    addr = np.zeros((B, L), np.uint64)
+    for b in range(B):
+        addr[b] = b * per_block + np.concatenate([[0], np.cumsum(seg_len)[:-1]])
+    numa = np.zeros(L, np.uint32)
+    dst_addr, size = receiver_layout(B, seg_len, np.random.default_rng(5))
+    assert check_seal(addr, B, seg_len, numa, B * per_block, dst_addr, size) == 0
 
 
 def test_seal_per_lane_lengths():
@@ -256,7 +282,8 @@ def test_seal_corrupt_groups():
                       groups=groups) == oracle.S_BOUNDS
 
 
-def test_seal_full_size_default():
+@pytest.mark.parametrize("bulk", [True, False])
+def test_seal_full_size_default(bulk):
     """The default workload end to end on the device: pack, then seal into a
     lane-major receiver layout; every segment compared on the device with
     the holder bytes it came from."""
@@ -273,7 +300,7 @@ def test_seal_full_size_default():
     l = torch.arange(L, dtype=torch.int64, device="cuda")[None, :]
     dst_addr = ((l * B + b) * seg).reshape(-1).contiguous()
     dst = torch.empty(B * L * seg, dtype=torch.uint8, device="cuda")
-    tr.seal(slab, dst_addr, dst)
+    tr.seal(slab, dst_addr, dst, bulk=bulk)
     torch.cuda.synchronize()
     assert tr.read_status() == 0
     src_addr = torch.from_numpy(wl.addr.view(np.int64)).cuda()
