@@ -274,6 +274,10 @@ kvx_status kvx_rebuild(const uint32_t *lane_first, const uint32_t *run_block,
 
 /* ------------------------------------------------------------ pack/unpack */
 
+/* Scratch for kvx_pack / kvx_unpack: the slab's 64 KiB tile lists plus a
+ * list of descriptor pieces (about 24 B per 2 KiB of slab).  A workspace of
+ * at least the tile lists' size but below this size is accepted too: tiles
+ * shared by several descriptors then all take the register path. */
 size_t kvx_copy_workspace_size(uint64_t slab_bytes);
 
 /*

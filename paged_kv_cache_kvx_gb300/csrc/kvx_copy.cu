@@ -5,7 +5,7 @@
 //
 // HBM-bound copy, no contraction.  The slab side is always contiguous (the
 // descriptors tile it), so the work is cut into fixed 64 KiB slab tiles.  A
-// prep kernel checks the descriptors and sorts every tile into one of two
+// prep kernel checks the descriptors and sorts every tile into one of three
 // lists:
 //   - TMA jobs: tiles inside one 16-byte aligned descriptor (every tile of a
 //     dense 32 MiB read, most tiles of a 1 MiB per-block read).  One lane per
@@ -17,16 +17,20 @@
 //     are done rather than when the slowest ring is.  Sweeps on GB300 (16-96
 //     KiB tiles, 2-12 stages, 38-304 rings, static or claimed work, claims of
 //     1-8 jobs) put one ring per SM, 3 x 64 KiB, claims of 2 first.
-//   - vector tiles: tiles that hold several descriptors (4 KiB / 512 B
-//     segment reads) or unaligned ones.  256 threads per tile; the tile's
+//   - pieces: tiles shared by several 16-byte aligned descriptors of 2 to
+//     16 KiB (the 4 KiB per-segment reads of a scattered holder), one piece
+//     per descriptor, moved by the four 16 KiB-stage bulk-copy rings per SM
+//     of kvx_ring.cuh.
+//   - vector tiles: the other shared tiles (512 B segment reads, 32 KiB
+//     block reads) and unaligned ones.  256 threads per tile; the tile's
 //     descriptors are staged in shared memory and each 16-byte vector finds
 //     its descriptor by binary search (byte copies when anything is
 //     unaligned).
-// Both copy kernels walk their list round-robin over a persistent grid, so
+// The tile kernels walk their list round-robin over a persistent grid, so
 // the grid streams one window of the slab at a time.
 #include <atomic>
 
-#include "kvx_common.cuh"
+#include "kvx_ring.cuh"
 
 namespace kvx {
 namespace {
@@ -44,7 +48,23 @@ struct CopyCtl {
     uint32_t n_tma;           // TMA jobs
     uint32_t n_vec;           // vector tiles
     uint32_t next_job;        // next unclaimed TMA job
+    uint32_t n_piece;         // descriptor pieces of shared tiles for the ring path
+    ring::SegCtl seg;         // claim counter of the ring path
 };
+
+// A tile shared by several descriptors goes to the ring path of kvx_ring.cuh
+// (four warps per SM, 3 x 16 KiB stages each), one piece per descriptor, when
+// every descriptor there is aligned and at least this long (below it the
+// register path is the faster one) ...
+constexpr uint64_t kPieceMinDesc = 2048;
+constexpr uint32_t kPiecesPerTile = (uint32_t)(kTileBytes / kPieceMinDesc) + 1;  // 33
+// ... and when one of them is shorter than this: tiles of longer descriptors
+// run faster on the register path (measured on GB300: 32 KiB descriptors
+// 6572 GB/s there, 6307 through the rings; 4 KiB descriptors ~6000 there,
+// 6427 through the rings).  A whole tile of one descriptor always takes the
+// 64 KiB-stage ring of k_copy_tma (a ring of 16 KiB stages reached only ~6090
+// on the default workload, against ~6870).
+constexpr uint64_t kPieceMaxDesc = 16 * 1024;
 
 struct TmaJob {
     uint64_t lo;      // slab offset of the tile
@@ -58,9 +78,12 @@ struct Ws {
     uint32_t *tile_desc;  // [ntiles]
     TmaJob *jobs;         // [ntiles]
     uint32_t *vec_tiles;  // [ntiles]
+    TmaJob *pieces;       // [kPiecesPerTile * ntiles], when the workspace holds them
 };
 
-Ws carve(void *base, uint64_t slab_bytes, size_t *bytes) {
+// The workspace: the tile lists, then (optional) the piece list.  base_bytes
+// gets the size without the piece list.
+Ws carve(void *base, uint64_t slab_bytes, size_t *bytes, size_t *base_bytes = nullptr) {
     const uint64_t nt = ceil_div(slab_bytes, kTileBytes);
     Carver c(base);
     Ws w;
@@ -68,6 +91,8 @@ Ws carve(void *base, uint64_t slab_bytes, size_t *bytes) {
     w.tile_desc = c.take<uint32_t>(nt);
     w.jobs = c.take<TmaJob>(nt);
     w.vec_tiles = c.take<uint32_t>(nt);
+    if (base_bytes) *base_bytes = c.off;
+    w.pieces = c.take<TmaJob>((size_t)kPiecesPerTile * nt);
     *bytes = c.off;
     return w;
 }
@@ -83,7 +108,8 @@ __global__ void __launch_bounds__(kThreads)
 k_copy_prep(const kvx_desc *__restrict__ descs, const uint64_t *__restrict__ num_descs,
             uint64_t desc_cap, uint64_t pool_bytes, uint64_t slab_bytes, bool bases_aligned,
             uint32_t *__restrict__ tile_desc, TmaJob *__restrict__ jobs,
-            uint32_t *__restrict__ vec_tiles, CopyCtl *ctl, uint32_t *status) {
+            uint32_t *__restrict__ vec_tiles, TmaJob *__restrict__ pieces, CopyCtl *ctl,
+            uint32_t *status) {
     const uint64_t n = *num_descs < desc_cap ? *num_descs : desc_cap;
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
     const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -118,11 +144,13 @@ k_copy_prep(const kvx_desc *__restrict__ descs, const uint64_t *__restrict__ num
     for (uint64_t t0 = tid - lane; t0 < ntiles; t0 += stride) {  // warp-uniform loop
         const uint64_t t = t0 + lane;
         bool is_tma = false, is_vec = false;
+        uint32_t npieces = 0;  // this tile's pieces for the ring path (0: not on it)
+        uint64_t lo = 0, hi = 0, a = 0;
         TmaJob job{};
         if (t < ntiles) {
-            const uint64_t lo = t * kTileBytes;
-            const uint64_t hi = lo + kTileBytes < used ? lo + kTileBytes : used;
-            uint64_t a = 0, z = n;  // last k with descs[k].local <= lo, in [a, z)
+            lo = t * kTileBytes;
+            hi = lo + kTileBytes < used ? lo + kTileBytes : used;
+            uint64_t z = n;  // last k with descs[k].local <= lo, in [a, z)
             while (z - a > 1) {
                 const uint64_t m = (a + z) >> 1;
                 if (descs[m].local <= lo) a = m; else z = m;
@@ -139,6 +167,30 @@ k_copy_prep(const kvx_desc *__restrict__ descs, const uint64_t *__restrict__ num
                 job = TmaJob{lo, delta, (uint32_t)(hi - lo), 0};
             } else {
                 is_vec = true;
+                if (pieces && bases_aligned) {
+                    // a shared tile: one piece per descriptor, if each is aligned
+                    // and long enough for the bulk engine
+                    bool fit = true, short_desc = false;
+                    uint32_t np = 0;
+                    for (uint64_t k = a; k < n; k++) {
+                        const kvx_desc e = descs[k];
+                        if (e.local >= hi) break;
+                        const uint64_t plo = e.local > lo ? e.local : lo;
+                        const uint64_t phi = e.len < hi - e.local ? e.local + e.len : hi;
+                        if (plo >= phi) continue;
+                        if (e.len < kPieceMinDesc || ((plo | phi | (e.remote - e.local)) & 15)) {
+                            fit = false;
+                            break;
+                        }
+                        short_desc |= e.len < kPieceMaxDesc;
+                        if (in_range(e.remote, e.len, pool_bytes) && in_range(e.local, e.len, slab_bytes))
+                            np++;  // a descriptor outside the pool or slab is skipped
+                    }
+                    if (fit && short_desc && np <= kPiecesPerTile) {
+                        is_vec = false;
+                        npieces = np;
+                    }
+                }
             }
         }
         const uint32_t mt = __ballot_sync(0xFFFFFFFFu, is_tma);
@@ -153,6 +205,27 @@ k_copy_prep(const kvx_desc *__restrict__ descs, const uint64_t *__restrict__ num
         const uint32_t below = (1u << lane) - 1u;
         if (is_tma) jobs[bt + __popc(mt & below)] = job;
         if (is_vec) vec_tiles[bv + __popc(mv & below)] = (uint32_t)t;
+        if (pieces) {  // reserve this warp's pieces, then write them
+            const uint32_t incl = warp_incl_sum(npieces);
+            const uint32_t wtot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+            uint32_t bp = 0;
+            if (lane == 0 && wtot) bp = atomicAdd(&ctl->n_piece, wtot);
+            bp = __shfl_sync(0xFFFFFFFFu, bp, 0) + incl - npieces;
+            if (npieces) {
+                for (uint64_t k = a; k < n; k++) {
+                    const kvx_desc e = descs[k];
+                    if (e.local >= hi) break;
+                    const uint64_t plo = e.local > lo ? e.local : lo;
+                    const uint64_t phi = e.len < hi - e.local ? e.local + e.len : hi;
+                    if (plo >= phi) continue;
+                    if (!(in_range(e.remote, e.len, pool_bytes) && in_range(e.local, e.len, slab_bytes)))
+                        continue;
+                    if (bp < (uint64_t)kPiecesPerTile * ntiles)  // always: at most kPiecesPerTile per tile
+                        pieces[bp] = TmaJob{plo, e.remote - e.local, (uint32_t)(phi - plo), 0};
+                    bp++;
+                }
+            }
+        }
     }
 }
 
@@ -367,15 +440,35 @@ cudaError_t set_tma_smem() {
     return e;
 }
 
+// The ring path's segments: the pieces of shared tiles listed by the prep.
+template <bool PACK>
+struct PieceGen {
+    const uint8_t *pool_r;
+    uint8_t *pool_w;
+    const uint8_t *slab_r;
+    uint8_t *slab_w;
+    const TmaJob *pieces;
+    const CopyCtl *ctl;
+    uint32_t *st;
+    __device__ uint64_t units() const { return ctl->bad ? 0 : ctl->n_piece; }
+    __device__ ring::Seg get(uint64_t u, uint32_t &) const {
+        const TmaJob j = pieces[u];
+        return PACK ? ring::Seg{pool_r + j.lo + j.delta, slab_w + j.lo, j.len, true}
+                    : ring::Seg{slab_r + j.lo, pool_w + j.lo + j.delta, j.len, true};
+    }
+    __device__ uint32_t *status() const { return st; }
+};
+
 kvx_status launch(bool pack, const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r,
                   uint8_t *slab_w, uint64_t pool_bytes, uint64_t slab_bytes, const kvx_desc *descs,
                   const uint64_t *num_descs, uint64_t desc_cap, uint32_t *status, void *ws,
                   size_t ws_bytes, void *stream) {
     if (!descs || !num_descs || !status || !ws) return KVX_EINVAL;
     if ((pool_bytes && !(pool_r || pool_w)) || (slab_bytes && !(slab_r || slab_w))) return KVX_EINVAL;
-    size_t need = 0;
-    Ws w = carve(ws, slab_bytes, &need);
-    if (ws_bytes < need) return KVX_EINVAL;
+    size_t need = 0, need_base = 0;
+    Ws w = carve(ws, slab_bytes, &need, &need_base);
+    if (ws_bytes < need_base) return KVX_EINVAL;
+    if (ws_bytes < need) w.pieces = nullptr;  // shared tiles stay on the register path
     if ((pack ? set_tma_smem<true>() : set_tma_smem<false>()) != cudaSuccess) return KVX_ECUDA;
     cudaStream_t s = as_stream(stream);
     if (cudaMemsetAsync(w.ctl, 0, sizeof(CopyCtl), s) != cudaSuccess) return KVX_ECUDA;
@@ -384,7 +477,8 @@ kvx_status launch(bool pack, const uint8_t *pool_r, uint8_t *pool_w, const uint8
     const bool aligned = ((pa | sa) & 15) == 0;
     const int sms = sm_count();
     k_copy_prep<<<sms * 2, kThreads, 0, s>>>(descs, num_descs, desc_cap, pool_bytes, slab_bytes,
-                                              aligned, w.tile_desc, w.jobs, w.vec_tiles, w.ctl, status);
+                                              aligned, w.tile_desc, w.jobs, w.vec_tiles, w.pieces,
+                                              w.ctl, status);
     KVX_LAUNCHED();
     const size_t smem = (size_t)kStages * kTileBytes;
     if (pack)
@@ -392,6 +486,11 @@ kvx_status launch(bool pack, const uint8_t *pool_r, uint8_t *pool_w, const uint8
     else
         k_copy_tma<false><<<sms * kTmaCtasPerSm, 32, smem, s>>>(pool_r, pool_w, slab_r, slab_w, w.jobs, w.ctl, status);
     KVX_LAUNCHED();
+    if (w.pieces) {
+        const kvx_status r = pack ? ring::launch_ring(PieceGen<true>{pool_r, pool_w, slab_r, slab_w, w.pieces, w.ctl, status}, &w.ctl->seg, s)
+                                  : ring::launch_ring(PieceGen<false>{pool_r, pool_w, slab_r, slab_w, w.pieces, w.ctl, status}, &w.ctl->seg, s);
+        if (r != KVX_OK) return r;
+    }
     const uint32_t grid = (uint32_t)(sms * kCtasPerSm);
     if (pack)
         k_copy_vec<true><<<grid, kThreads, 0, s>>>(pool_r, pool_w, slab_r, slab_w, pool_bytes,
@@ -471,7 +570,11 @@ extern "C" kvx_status kvx_pack_noalloc(const uint8_t *pool, uint64_t pool_bytes,
                                        const kvx_desc *descs, const uint64_t *num_descs,
                                        uint64_t desc_capacity, uint8_t *slab, uint64_t slab_bytes,
                                        uint32_t *status, void *stream) {
-    if (kvx_copy_workspace_size(slab_bytes) > kNoallocScratchBytes) return KVX_ECAPACITY;
+    // the scratch holds the tile lists (not the piece list: shared tiles take
+    // the register path here)
+    size_t full = 0, base = 0;
+    carve(nullptr, slab_bytes, &full, &base);
+    if (base > kNoallocScratchBytes) return KVX_ECAPACITY;
     void *scratch = pack_scratch_address();
     if (!scratch) return KVX_ECUDA;
     return launch(true, pool, nullptr, nullptr, slab, pool_bytes, slab_bytes, descs, num_descs,

@@ -260,6 +260,75 @@ def test_pack_descriptor_checks_match_oracle():
         assert np.array_equal(slab.cpu().numpy(), want), mutate
 
 
+def _desc_list(rng, lengths, bad=()):
+    """Descriptors tiling [0, sum(lengths)) of the slab in order, read from
+    disjoint pool ranges placed in a shuffled order with small gaps (16-byte
+    aligned unless the length is not a multiple of 16); indices in bad point
+    past the end of the pool.  Returns (descs, slab bytes, pool bytes)."""
+    n = len(lengths)
+    d = np.zeros(n, dtype=oracle.DESC_DTYPE)
+    remote = np.zeros(n, dtype=np.int64)
+    cur = 0
+    for k in rng.permutation(n):
+        ln = int(lengths[k])
+        cur += int(rng.integers(0, 4)) * 16 + (int(rng.integers(1, 16)) if ln % 16 else 0)
+        remote[k] = cur
+        cur += ln
+    pool_bytes = cur + 4096
+    local = 0
+    for k in range(n):
+        ln = int(lengths[k])
+        r = pool_bytes - ln // 2 if k in bad else int(remote[k])
+        d[k] = (r, local, ln, 0, 0)
+        local += ln
+    return d, local, pool_bytes
+
+
+@pytest.mark.parametrize("mix", ["ring_4k", "ring_2k_6k", "register_32k", "short_mixed",
+                                 "unaligned", "with_bad"])
+def test_copy_paths_descriptor_mix(mix):
+    """Tiles of one descriptor (bulk ring), tiles shared by aligned 2-16 KiB
+    descriptors (per-descriptor pieces on the 16 KiB-stage rings), and the
+    rest (register path): pack and unpack bit-exact against the oracle,
+    skipped out-of-range descriptors included."""
+    rng = np.random.default_rng(sum(map(ord, mix)))
+    if mix == "ring_4k":
+        lens = [4096] * 700 + [1 << 20] * 3 + [4096] * 33
+    elif mix == "ring_2k_6k":
+        lens = list(rng.choice([2048, 6144, 10240], size=900))
+    elif mix == "register_32k":
+        lens = [32768] * 200
+    elif mix == "short_mixed":
+        lens = list(rng.choice([1024, 4096, 512, 8192], size=900))
+    elif mix == "unaligned":
+        lens = list(rng.choice([4096, 4100, 2056], size=700))
+    else:
+        lens = [4096] * 600
+    bad = {5, 77, 301} if mix == "with_bad" else set()
+    d, slab_bytes, pool_bytes = _desc_list(rng, [int(x) for x in lens], bad)
+    host_pool = rng.integers(0, 256, pool_bytes, dtype=np.uint8)
+    want_slab = np.zeros(slab_bytes, np.uint8)
+    st_p = oracle.pack(host_pool, d, want_slab)
+    want_pool = np.full(pool_bytes, 0xA5, np.uint8)
+    st_u = oracle.unpack(want_slab, d, want_pool)
+    dd = torch.from_numpy(d.view(np.uint8).copy()).cuda()
+    nd = torch.tensor([len(d), 0, 0], dtype=torch.int64, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(kvx.kvx_copy_workspace_size(slab_bytes), dtype=torch.uint8, device="cuda")
+    pool = torch.from_numpy(host_pool).cuda()
+    slab = torch.zeros(slab_bytes, dtype=torch.uint8, device="cuda")
+    kvx.kvx_pack(pool, pool_bytes, dd, nd, len(d), slab, slab_bytes, status, ws)
+    torch.cuda.synchronize()
+    assert int(status.item()) == st_p
+    assert np.array_equal(slab.cpu().numpy(), want_slab)
+    dst = torch.full((pool_bytes,), 0xA5, dtype=torch.uint8, device="cuda")
+    status.zero_()
+    kvx.kvx_unpack(slab, slab_bytes, dd, nd, len(d), dst, pool_bytes, status, ws)
+    torch.cuda.synchronize()
+    assert int(status.item()) == st_u
+    assert np.array_equal(dst.cpu().numpy(), want_pool)
+
+
 # ------------------------------------------------------------ full sizes
 
 FULL = ["tiny", "default", "worst", "mixed", "many_small", "wide64k"]
