@@ -1221,9 +1221,24 @@ __global__ void __launch_bounds__(kST, 1) k_plan_small(const __grid_constant__ P
         return;
     }
 
-    // ---- step 2: stable LSD radix sort of run indices on (node, base)
+    // ---- step 2: stable LSD radix sort of run indices on (node, empty, base);
+    // a table already in key order (a bump-allocated holder whose lanes are
+    // numbered by address) needs no pass
+    bool in_order = true;
+#pragma unroll
+    for (int j = 0; j < 2; j++) {
+        const uint32_t y = r0 + j;
+        if (y == 0 || y >= R) continue;
+        const uint32_t x = y - 1;
+        const bool ex = S.len[x] == 0, ey = S.len[y] == 0;
+        const bool le = S.node[x] != S.node[y] ? S.node[x] < S.node[y]
+                        : ex != ey              ? !ex
+                                                : S.base[x] <= S.base[y];
+        in_order = in_order && le;
+    }
+    const bool sorted_already = __syncthreads_and(in_order) != 0;
     uint32_t act[13], nact = 0;
-    if (R > 1) nact = plan_digits(s_or ^ s_and, s_ore ^ s_ande, s_orn ^ s_andn, act);
+    if (R > 1 && !sorted_already) nact = plan_digits(s_or ^ s_and, s_ore ^ s_ande, s_orn ^ s_andn, act);
     for (uint32_t r = tid; r < R; r += kST) S.idx[0][r] = (uint16_t)r;
     const uint32_t lt_mask = (1u << lane) - 1u;
     for (uint32_t k = 0; k < nact; k++) {
