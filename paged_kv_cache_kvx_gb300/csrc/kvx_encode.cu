@@ -11,12 +11,12 @@
 // (entry state, runs before, last start before), and an emit pass writes
 // each run at its lane-major index.
 //
-// One cooperative kernel, four phases separated by bounded grid barriers:
+// One cooperative kernel, three phases separated by bounded grid barriers:
 //   1. per tile (32 lanes x 8K blocks): the tile's effect on each lane;
 //   2. one warp per lane: a warp-shuffle scan of its tiles' effects gives
-//      every tile's entry prefix and the lane's run count;
-//   3. one warp per 32-lane tile: the tile's run total;
-//   4. per tile: lane offsets (totals of earlier lane tiles plus a warp
+//      every tile's entry prefix and the lane's run count, which is also
+//      added atomically to its 32-lane tile's total;
+//   3. per tile: lane offsets (totals of earlier lane tiles plus a warp
 //      scan), then every thread re-walks its slice from its entry prefix
 //      and writes its runs.
 // Thread layout: a CTA is 8 warps; lane t of warp w handles table lane
@@ -170,8 +170,8 @@ Ws carve(void *base, uint32_t B, uint32_t L, size_t *bytes) {
     Carver c(base);
     Ws w;
     w.ctl = c.take<EncodeCtl>(1);
-    w.tiles = c.take<TileRec>((size_t)g.ntr * L);
     w.tile_runs = c.take<uint64_t>(g.ntl);
+    w.tiles = c.take<TileRec>((size_t)g.ntr * L);
     *bytes = c.off;
     return w;
 }
@@ -314,26 +314,18 @@ __global__ void __launch_bounds__(kThreads) k_encode(const __grid_constant__ Enc
             if (r < g.ntr) *slot = TileRec{mine.state, mine.runs, mine.prev, 0u};
             carry = prefix_then(carry, shfl_xfer(incl, 31));
         }
-        if (t == 0) a.runs_per_lane[l] = carry.runs;
+        if (t == 0) {
+            a.runs_per_lane[l] = carry.runs;
+            atomicAdd(reinterpret_cast<unsigned long long *>(a.tile_runs + l / 32),
+                      (unsigned long long)carry.runs);  // zeroed with the ctl
+        }
     }
     if (!grid_barrier(&a.ctl->gs, G)) {
         if (threadIdx.x == 0) atomicOr(a.status, KVX_S_TIMEOUT);
         return;
     }
 
-    // ---- phase 3: runs of each 32-lane tile, one warp per lane tile
-    for (uint32_t tl = blockIdx.x * kRows + w; tl < g.ntl; tl += G * kRows) {
-        const uint32_t l = tl * 32 + t;
-        uint64_t v = l < L ? __ldcg(a.runs_per_lane + l) : 0;
-        for (int d = 16; d > 0; d >>= 1) v += __shfl_down_sync(0xFFFFFFFFu, v, d);
-        if (t == 0) a.tile_runs[tl] = v;
-    }
-    if (!grid_barrier(&a.ctl->gs, G)) {
-        if (threadIdx.x == 0) atomicOr(a.status, KVX_S_TIMEOUT);
-        return;
-    }
-
-    // ---- phase 4: lane offsets, then every slice writes its runs
+    // ---- phase 3: lane offsets, then every slice writes its runs
     if (blockIdx.x == 0) {  // total runs
         const uint64_t tot = block_sum_tiles(a.tile_runs, g.ntl, s_red);
         if (threadIdx.x == 0) *a.num_runs = tot;
@@ -454,7 +446,9 @@ kvx_status launch_encode(const uint64_t *addr, const uint32_t *seg_size, const u
     if (ws_bytes < need) return KVX_EINVAL;
     const Geometry g = geometry(B, L);
     cudaStream_t s = as_stream(stream);
-    if (cudaMemsetAsync(w.ctl, 0, sizeof(EncodeCtl), s) != cudaSuccess) return KVX_ECUDA;
+    // the control block and the lane-tile totals (carved right after it) start at zero
+    const size_t zero_bytes = reinterpret_cast<char *>(w.tile_runs + g.ntl) - reinterpret_cast<char *>(w.ctl);
+    if (cudaMemsetAsync(w.ctl, 0, zero_bytes, s) != cudaSuccess) return KVX_ECUDA;
     EncodeArgs a;
     a.addr = addr;
     a.seg_size = seg_size;
