@@ -13,9 +13,10 @@
 //
 // One cooperative kernel, three phases separated by bounded grid barriers:
 //   1. per tile (32 lanes x 8K blocks): the tile's effect on each lane;
-//   2. one warp per lane: a warp-shuffle scan of its tiles' effects gives
-//      every tile's entry prefix and the lane's run count, which is also
-//      added atomically to its 32-lane tile's total;
+//   2. one warp per lane (one block per lane for tall tables): a
+//      warp-shuffle scan of its tiles' effects gives every tile's entry
+//      prefix and the lane's run count, which is also added atomically to
+//      its 32-lane tile's total;
 //   3. per tile: lane offsets (totals of earlier lane tiles plus a warp
 //      scan), then every thread re-walks its slice from its entry prefix
 //      and writes its runs.
@@ -231,6 +232,65 @@ struct EncodeArgs {
     uint32_t *status;
 };
 
+// Row tiles per lane above which the lane scan takes a whole block per lane.
+constexpr uint32_t kTallRows = 64;
+
+// Scans the effects of row tiles [r_lo, r_hi) of lane l in chunks of 32 (one
+// per lane of the warp), from entry prefix carry: every tile's record is
+// replaced by its entry prefix.  Returns the prefix after r_hi.
+__device__ Prefix scan_tile_range(TileRec *tiles, uint32_t L, uint32_t l, uint32_t r_lo, uint32_t r_hi,
+                                  Prefix carry, uint32_t t) {
+    for (uint32_t c0 = r_lo; c0 < r_hi; c0 += 32) {
+        const uint32_t r = c0 + t;
+        TileRec *slot = tiles + (uint64_t)r * L + l;
+        Xfer x = xfer_identity();
+        if (r < r_hi) {
+            const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(slot));
+            x = unpack_xfer(TileRec{v.x, v.y, v.z, v.w});
+        }
+        Xfer incl = x;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const Xfer o = shfl_up_xfer(incl, d);
+            if ((int)t >= d) incl = xfer_then(o, incl);
+        }
+        Xfer excl = shfl_up_xfer(incl, 1);
+        if (t == 0) excl = xfer_identity();
+        const Prefix mine = prefix_then(carry, excl);
+        if (r < r_hi) *slot = TileRec{mine.state, mine.runs, mine.prev, 0u};
+        carry = prefix_then(carry, shfl_xfer(incl, 31));
+    }
+    return carry;
+}
+
+// The combined effect of row tiles [r_lo, r_hi) of lane l (nothing stored).
+__device__ Xfer range_xfer(const TileRec *tiles, uint32_t L, uint32_t l, uint32_t r_lo, uint32_t r_hi,
+                           uint32_t t) {
+    Xfer agg = xfer_identity();
+    for (uint32_t c0 = r_lo; c0 < r_hi; c0 += 32) {
+        const uint32_t r = c0 + t;
+        Xfer x = xfer_identity();
+        if (r < r_hi) {
+            const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(tiles + (uint64_t)r * L + l));
+            x = unpack_xfer(TileRec{v.x, v.y, v.z, v.w});
+        }
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const Xfer o = shfl_up_xfer(x, d);
+            if ((int)t >= d) x = xfer_then(o, x);
+        }
+        agg = xfer_then(agg, shfl_xfer(x, 31));
+    }
+    return agg;
+}
+
+// A lane's run count, and its share of its 32-lane tile's total (zeroed with
+// the control block).
+__device__ __forceinline__ void lane_done(const EncodeArgs &a, uint32_t l, uint32_t runs) {
+    a.runs_per_lane[l] = runs;
+    atomicAdd(reinterpret_cast<unsigned long long *>(a.tile_runs + l / 32), (unsigned long long)runs);
+}
+
 __global__ void __launch_bounds__(kThreads) k_encode(const __grid_constant__ EncodeArgs a) {
     __shared__ Xfer sx[kRows][32];
     __shared__ Prefix sp[kRows][32];
@@ -291,33 +351,28 @@ __global__ void __launch_bounds__(kThreads) k_encode(const __grid_constant__ Enc
         return;
     }
 
-    // ---- phase 2: one warp per lane, warp-shuffle scan over its tiles
-    for (uint32_t l = blockIdx.x * kRows + w; l < L; l += G * kRows) {
-        Prefix carry{0u, 0u, kNone};
-        for (uint32_t c0 = 0; c0 < g.ntr; c0 += 32) {
-            const uint32_t r = c0 + t;
-            TileRec* slot = a.tiles + (uint64_t)r * L + l;
-            Xfer x = xfer_identity();
-            if (r < g.ntr) {
-                const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(slot));
-                x = unpack_xfer(TileRec{v.x, v.y, v.z, v.w});
-            }
-            Xfer incl = x;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const Xfer o = shfl_up_xfer(incl, d);
-                if ((int)t >= d) incl = xfer_then(o, incl);
-            }
-            Xfer excl = shfl_up_xfer(incl, 1);
-            if (t == 0) excl = xfer_identity();
-            const Prefix mine = prefix_then(carry, excl);
-            if (r < g.ntr) *slot = TileRec{mine.state, mine.runs, mine.prev, 0u};
-            carry = prefix_then(carry, shfl_xfer(incl, 31));
+    // ---- phase 2: per lane, a warp-shuffle scan over its tiles' effects.  One
+    // warp per lane; for tall tables (many row tiles, few lanes) one block
+    // per lane, its warps scanning contiguous ranges of the lane's tiles and
+    // chaining through their ranges' totals.
+    if (g.ntr <= kTallRows) {
+        for (uint32_t l = blockIdx.x * kRows + w; l < L; l += G * kRows) {
+            const Prefix carry = scan_tile_range(a.tiles, L, l, 0, g.ntr, Prefix{0u, 0u, kNone}, t);
+            if (t == 0) lane_done(a, l, carry.runs);
         }
-        if (t == 0) {
-            a.runs_per_lane[l] = carry.runs;
-            atomicAdd(reinterpret_cast<unsigned long long *>(a.tile_runs + l / 32),
-                      (unsigned long long)carry.runs);  // zeroed with the ctl
+    } else {
+        const uint32_t per = (g.ntr + kRows - 1) / kRows;
+        const uint32_t r_lo = w * per < g.ntr ? w * per : g.ntr;
+        const uint32_t r_hi = r_lo + per < g.ntr ? r_lo + per : g.ntr;
+        for (uint32_t l = blockIdx.x; l < L; l += G) {
+            const Xfer agg = range_xfer(a.tiles, L, l, r_lo, r_hi, t);
+            if (t == 0) sx[w][0] = agg;
+            __syncthreads();
+            Prefix carry{0u, 0u, kNone};
+            for (uint32_t i = 0; i < w; i++) carry = prefix_then(carry, sx[i][0]);
+            const Prefix end = scan_tile_range(a.tiles, L, l, r_lo, r_hi, carry, t);
+            if (w == kRows - 1 && t == 0) lane_done(a, l, end.runs);
+            __syncthreads();  // sx is rewritten for the next lane
         }
     }
     if (!grid_barrier(&a.ctl->gs, G)) {

@@ -56,6 +56,32 @@ def test_random_lanes_many_tiles_all_radix_digits():
         assert np.array_equal(tr.read_local(), local)
 
 
+@pytest.mark.parametrize("B,L,kind", [(20011, 6, "random"), (30013, 9, "random"), (40960, 4, "bump"),
+                                      (9001, 2, "bump")])
+def test_tall_tables_block_per_lane_scan(B, L, kind):
+    """Tables with far more row tiles than lanes: the encoder's lane scan runs
+    one block per lane, its warps chaining over ranges of the lane's tiles
+    (pair runs, and long runs broken by relocated blocks)."""
+    rng = np.random.default_rng(B + L)
+    if kind == "random":
+        addr, seg_len, numa, pool = random_lanes(rng, B, L)
+    else:
+        seg = 64
+        pos = np.arange(B, dtype=np.int64)
+        rel = np.sort(rng.choice(B, size=B // 40, replace=False))
+        pos[rel] = B + np.arange(rel.size)
+        addr = (pos[:, None] * (L * seg) + np.arange(L)[None, :] * seg).astype(np.uint64)
+        seg_len, numa = np.full(L, seg, np.uint32), np.zeros(L, np.uint32)
+        pool = int(addr.max()) + seg
+    t = oracle.encode_runs(addr)
+    tr = kvx.Transfer(B, seg_len, numa, pool)
+    tr.set_addr(addr)
+    tr.encode()
+    torch.cuda.synchronize()
+    assert tr.read_status() == 0
+    assert_table_equal(tr, t)
+
+
 @pytest.mark.parametrize("B,L", [(0, 4), (1, 2), (1, 7 * 2), (2, 2), (3, 50), (65, 34), (513, 2)])
 def test_edge_shapes(B, L):
     rng = np.random.default_rng(B * 1000 + L)
