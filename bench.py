@@ -274,6 +274,9 @@ def run_kvx(args):
     if args.workload == "konly":
         wl = W.k_only("bump", name="default")
         args.no_aux = True
+    elif args.workload == "worst" and args.blocks != 1000:
+        wl = W.worst(blocks=args.blocks, npos=2 * args.blocks + 48)  # reduced for profiler captures
+        args.no_aux = True
     elif args.workload != "default":
         wl = W.CONFIGS[args.workload]()
         args.no_aux = True  # the e2e / CPU legs are defined on the default workload
@@ -782,7 +785,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work for the oracle baseline leg of the kvx arm")
     ap.add_argument("--blocks", type=int, default=1000,
-                    help="blocks of the default shape (1000; fewer only for profiler captures)")
+                    help="blocks of the default (or worst) shape (1000; fewer only for profiler "
+                         "captures)")
     ap.add_argument("--workload", default="default",
                     choices=["default", "tiny", "worst", "mixed", "many_small", "wide64k", "konly",
                              "paged", "seal", "verify"],
