@@ -41,7 +41,8 @@ WORKLOAD = ("default: 1000 blocks x 288 slots x 2 segments (K,V) x 4 KiB uint8 =
             "segments, 2250 MiB, bump-allocated holder, slots 0-143 / 144-287 in two NUMA regions")
 COPY_SRC = os.path.join(ROOT, "paged_kv_cache_kvx_gb300", "csrc", "kvx_copy.cu")
 PROFILE = os.path.join(ROOT, "profiles", "copy_default.md")
-SEGCOPY_SRC = os.path.join(ROOT, "paged_kv_cache_kvx_gb300", "csrc", "kvx_segcopy.cu")
+SEGCOPY_SRC = [os.path.join(ROOT, "paged_kv_cache_kvx_gb300", "csrc", f)
+               for f in ("kvx_segcopy.cu", "kvx_ring.cuh")]
 
 
 def dist_env():
@@ -77,8 +78,13 @@ def load_peak():
 
 
 def copy_kernel_hash(src=COPY_SRC):
-    with open(src, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """First 16 hex digits of the SHA-256 of a source file (or of several,
+    concatenated in order)."""
+    h = hashlib.sha256()
+    for path in ([src] if isinstance(src, str) else src):
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic(profile=PROFILE, src=COPY_SRC):
