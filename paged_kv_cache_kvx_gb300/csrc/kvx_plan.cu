@@ -147,25 +147,50 @@ union ScanSmem {
     CAgg c[kT];
 };
 
-// Hillis-Steele block scan through shared memory.  Returns the inclusive
-// value; *excl gets the exclusive one, *total the block total.
+// Shuffle of any 4-byte-multiple value, one 32-bit word at a time.
+template <class T>
+__device__ __forceinline__ T shfl_up_words(const T &v, int d) {
+    static_assert(sizeof(T) % 4 == 0, "4-byte multiple");
+    T o;
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(&v);
+    uint32_t *dst = reinterpret_cast<uint32_t *>(&o);
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(T) / 4); i++) dst[i] = __shfl_up_sync(0xFFFFFFFFu, src[i], d);
+    return o;
+}
+
+// Block scan (blockDim a multiple of 32, at most 1024): warp-shuffle scans,
+// then one warp scans the warp totals through shared memory -- three block
+// barriers.  Returns the inclusive value; *excl gets the exclusive one,
+// *total the block total.  sh holds at least 32 elements.
 template <class T, class Op>
 __device__ T block_scan(T v, Op op, T identity, T *sh, T *excl, T *total) {
-    const int tid = threadIdx.x;
-    __syncthreads();
-    sh[tid] = v;
-    __syncthreads();
-    for (int d = 1; d < (int)blockDim.x; d <<= 1) {
-        T o = tid >= d ? sh[tid - d] : identity;
-        __syncthreads();
-        if (tid >= d) v = op(o, v);
-        sh[tid] = v;
-        __syncthreads();
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int nw = (int)(blockDim.x >> 5);
+    T x = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const T o = shfl_up_words(x, d);
+        if (lane >= d) x = op(o, x);
     }
-    *excl = tid > 0 ? sh[tid - 1] : identity;
-    *total = sh[blockDim.x - 1];
+    __syncthreads();  // sh may still be read from a previous scan
+    if (lane == 31) sh[w] = x;
     __syncthreads();
-    return v;
+    if (w == 0) {
+        T t = lane < nw ? sh[lane] : identity;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const T o = shfl_up_words(t, d);
+            if (lane >= d) t = op(o, t);
+        }
+        sh[lane] = t;
+    }
+    __syncthreads();
+    const T before = w > 0 ? sh[w - 1] : identity;
+    const T in_warp = shfl_up_words(x, 1);
+    *excl = lane > 0 ? op(before, in_warp) : before;
+    *total = sh[nw - 1];
+    return op(before, x);
 }
 
 // Ordered reduction of agg[0, t) by the whole block (the carry into tile t).
