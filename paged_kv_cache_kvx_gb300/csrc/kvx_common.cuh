@@ -75,14 +75,18 @@ __device__ __forceinline__ bool last_block(uint32_t *ticket) {
 }
 
 // Grid barrier for cooperative launches (every participating block is
-// resident).  Sense by generation: the last block to arrive resets the count
-// and bumps the generation; the others poll it.  The wait is bounded: after
-// about a second a block gives up, raises the shared abort flag and returns
-// false, and so do the blocks still waiting.
-// With a single participating block it is a plain __syncthreads().
+// resident).  One monotonic arrival counter, zeroed before the launch: the
+// arrivals of the k-th barrier are exactly k*nblocks .. (k+1)*nblocks - 1 (no
+// block passes a barrier before all have reached it), so a block's own
+// arrival number tells it the count that releases it, and the last arrival
+// releases everyone with no second atomic.  Waiters spin on the counter, hot
+// at first and then with short sleeps.  The wait is bounded: after about a
+// second a block gives up, raises the shared abort flag and returns false,
+// and so do the blocks still waiting.  With a single participating block it
+// is a plain __syncthreads().
 struct GridSync {
     uint32_t count;
-    uint32_t gen;
+    uint32_t gen;  // unused
     uint32_t abort;
     uint32_t pad;
 };
@@ -98,6 +102,12 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ bool grid_barrier(GridSync *gs, uint32_t nblocks) {
     __shared__ int s_ok;
     if (nblocks <= 1) {
@@ -107,24 +117,22 @@ __device__ __forceinline__ bool grid_barrier(GridSync *gs, uint32_t nblocks) {
     __syncthreads();
     if (threadIdx.x == 0) {
         int ok = 1;
-        volatile uint32_t *vgen = &gs->gen;
-        volatile uint32_t *vabort = &gs->abort;
-        const uint32_t g = *vgen;
         __threadfence();
-        const uint32_t arrived = atomicAdd(&gs->count, 1u) + 1u;
-        if (arrived == nblocks) {
-            atomicExch(&gs->count, 0u);
-            __threadfence();
-            atomicAdd(&gs->gen, 1u);
-        } else {
-            const uint64_t t0 = global_ns();
-            for (uint32_t polls = 0; *vgen == g; polls++) {
-                if (*vabort || polls >= kBarrierPolls || global_ns() - t0 > kWaitNs) {
-                    atomicExch(&gs->abort, 1u);
-                    ok = 0;
-                    break;
+        const uint32_t arrived = atomicAdd(&gs->count, 1u);
+        const uint32_t target = (arrived / nblocks + 1) * nblocks;
+        if (arrived + 1 != target) {
+            const volatile uint32_t *vabort = &gs->abort;
+            uint64_t t0 = 0;
+            for (uint32_t polls = 0; ld_acquire_gpu(&gs->count) < target; polls++) {
+                if (polls >= 256) {
+                    if (polls == 256) t0 = global_ns();
+                    if (*vabort || polls >= kBarrierPolls || global_ns() - t0 > kWaitNs) {
+                        atomicExch(&gs->abort, 1u);
+                        ok = 0;
+                        break;
+                    }
+                    __nanosleep(32);
                 }
-                if (polls > 32) __nanosleep(100);
             }
         }
         __threadfence();
