@@ -291,7 +291,9 @@ __device__ __forceinline__ void lane_done(const EncodeArgs &a, uint32_t l, uint3
     atomicAdd(reinterpret_cast<unsigned long long *>(a.tile_runs + l / 32), (unsigned long long)runs);
 }
 
-__global__ void __launch_bounds__(kThreads) k_encode(const __grid_constant__ EncodeArgs a) {
+// Six blocks per SM (40 registers): a grid of 912 resident blocks covers the
+// 782 tiles of a 100,000 x 64 table, one tile per block.
+__global__ void __launch_bounds__(kThreads, 6) k_encode(const __grid_constant__ EncodeArgs a) {
     __shared__ Xfer sx[kRows][32];
     __shared__ Prefix sp[kRows][32];
     __shared__ uint64_t s_lb[32];
@@ -332,12 +334,15 @@ __global__ void __launch_bounds__(kThreads) k_encode(const __grid_constant__ Enc
     }
 
     // ---- phase 1: each tile's effect on each of its lanes
+    const bool one_tile = ntiles <= G;  // every block has at most one tile in phases 1 and 3
+    Xfer my_sx = xfer_identity();
     for (uint32_t tile = blockIdx.x; tile < ntiles; tile += G) {
         const uint32_t tl = tile % g.ntl, tr = tile / g.ntl;
         const uint32_t l = tl * 32 + t;
         const uint64_t b0 = (uint64_t)tr * kRows * g.K + (uint64_t)w * g.K;
         const uint64_t b1 = b0 + g.K < Bv ? b0 + g.K : Bv;
-        sx[w][t] = (l < L && b0 < Bv) ? slice_xfer(a.addr, L, l, b0, b1) : xfer_identity();
+        my_sx = (l < L && b0 < Bv) ? slice_xfer(a.addr, L, l, b0, b1) : xfer_identity();
+        sx[w][t] = my_sx;
         __syncthreads();
         if (w == 0 && l < L) {
             Xfer acc = sx[0][t];
@@ -404,7 +409,8 @@ __global__ void __launch_bounds__(kThreads) k_encode(const __grid_constant__ Enc
         const uint64_t b0 = (uint64_t)tr * kRows * g.K + (uint64_t)w * g.K;
         const uint64_t b1 = b0 + g.K < Bv ? b0 + g.K : Bv;
         const bool active = l < L && b0 < Bv;
-        sx[w][t] = active ? slice_xfer(a.addr, L, l, b0, b1) : xfer_identity();
+        // a block with one tile kept its slice's effect from phase 1
+        sx[w][t] = !active ? xfer_identity() : one_tile ? my_sx : slice_xfer(a.addr, L, l, b0, b1);
         __syncthreads();
         if (w == 0 && l < L) {
             const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(a.tiles + (uint64_t)tr * L + l));
