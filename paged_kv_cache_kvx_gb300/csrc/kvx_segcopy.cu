@@ -10,17 +10,17 @@
 //       offset comes from the group carve and run_off, so no per-segment
 //       local table is ever written.
 //
-// HBM-bound copies.  One warp takes 32 segments at a time (pages longer than
-// 4 KiB count as several 4 KiB segments, so that the batches of a copy stay
-// small and many against the grid's warps whatever the page size): lane i computes
-// segment i's addresses and checks (coalesced metadata loads, the lanes'
-// lookups in parallel), then the whole warp moves the 32 segments.  Aligned
-// segments of up to 64 KiB form one index space of 16-byte vectors, walked
-// four vectors per lane per step (loads first, then stores), so short and
-// long segments alike keep several loads in flight per lane and every
-// access of a warp instruction stays inside one or two segments (coalesced).
-// Longer aligned segments go one at a time in 4-vector steps; unaligned ones
-// byte by byte.  Streaming cache hints: neither side is read again.
+// HBM-bound copies, one warp per batch of 32 segments (pages longer than 4 KiB
+// count as several 4 KiB segments, so that batches stay small and many
+// whatever the page size): lane i computes segment i's addresses and checks
+// (coalesced metadata loads, the lanes' lookups in parallel), then the batch
+// is moved by one of the two engines of kvx_ring.cuh:
+//   - with a caller workspace, the SM's bulk-copy engine (k_seg_tma: four
+//     warps per SM, each with a ring of 3 x 16 KiB shared-memory stages, the
+//     batches claimed from a counter in the workspace);
+//   - without one, or for pages under 2 KiB, registers (k_paged_writes /
+//     k_seal_blocks below: 16-byte streaming vectors, several loads in flight
+//     per lane), which measured faster for short segments.
 #include "kvx_ring.cuh"
 
 namespace kvx {
