@@ -67,6 +67,24 @@ def step_value(payload_bytes: int, steps: int, world: int, total_ms: float) -> f
     return 4.0 * payload_bytes * steps * world / (total_ms / 1e3) / 1e9
 
 
+def host_info():
+    """The host the CPU baseline ran on: logical cores and CPU model."""
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware") and ":" in line:
+                    model = line.split(":", 1)[1].strip()
+                    break
+                if key == "cpu part" and not model:
+                    model = "cpu part " + line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return {"nproc": os.cpu_count(), "cpu": model or platform.processor() or platform.machine()}
+
+
 def load_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -216,6 +234,7 @@ def run_reference(args):
             "vs_baseline": None, "dtype": "u8", "data": "synthetic",
             "config": {"workload": WORKLOAD, "sample_blocks": blocks},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "host": host_info(),
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -413,6 +432,7 @@ def run_kvx(args):
     if rank == 0 and world == 1 and not args.no_aux:
         cb, desc, n, per = oracle_baseline(target_s=args.cpu_seconds)
         line["cpu_baseline"] = {"value": cb, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "host": host_info(),
                                 "sample": desc}
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -759,6 +779,7 @@ def run_next(args):
                             if unit_bytes else "4.6 MB table (fits L2): latency-bound"}})
     cb, desc = cpu_leg()
     line["cpu_baseline"] = {"value": cb, "unit": line["unit"], "cores": 1, "kind": "oracle",
+                            "host": host_info(),
                             "sample": desc}
     print(json.dumps(line), flush=True)
     return 0
