@@ -58,3 +58,60 @@ def test_binding_has_no_cpu_fallback():
     finally:
         kvx.lib_path = orig
         kvx._lib = saved
+
+
+# Host-side argument checks return before any CUDA call, so they run here
+# without a GPU.  Pointers are dummy non-null addresses that are never
+# dereferenced; KVX_EINVAL = 1, KVX_ECAPACITY = 3.
+EINVAL, ECAPACITY = 1, 3
+P = 0x1000  # a non-null dummy device pointer
+
+
+def _lib():
+    from paged_kv_cache_kvx_gb300 import kvx
+    return kvx.lib()
+
+
+def test_encode_rejects_small_capacity_and_workspace():
+    L = _lib()
+    B, Ln = 1000, 576
+    cap = int(L.kvx_run_capacity(B, Ln))
+    ws = int(L.kvx_encode_workspace_size(B, Ln))
+    assert L.kvx_encode_runs(P, B, Ln, P, P, P, P, cap - 1, P, P, P, ws, None) == ECAPACITY
+    assert L.kvx_encode_runs(P, B, Ln, P, P, P, P, cap, P, P, P, ws - 1, None) == EINVAL
+    assert L.kvx_encode_runs(P, B, Ln, P, P, P, P, cap, P, None, P, ws, None) == EINVAL  # no status
+    assert L.kvx_verify_encode(P, None, P, B, Ln, P, P, P, P, P, cap, P, P, P, ws, None) == EINVAL
+
+
+def test_plan_rejects_oversized_run_capacity():
+    L = _lib()
+    args = [P, 4, P, P, P, P, (1 << 31) + 1, 10, P, P, 4, 1 << 20, P, 1, P, 1, P, P, P, P, P, P, P,
+            1 << 40, None]
+    assert L.kvx_plan_groups(*args) == EINVAL
+
+
+def test_copies_reject_small_workspaces():
+    L = _lib()
+    slab = 1 << 30
+    ws = int(L.kvx_copy_workspace_size(slab))
+    # below even the tile lists
+    assert L.kvx_pack(P, 1 << 31, P, P, 10, P, slab, P, P, 64, None) == EINVAL
+    assert L.kvx_unpack(P, slab, P, P, 10, P, 1 << 31, P, P, 64, None) == EINVAL
+    # the segment copies: a workspace, if given, must hold the claim counter
+    seg_ws = int(L.kvx_segcopy_workspace_size())
+    assert seg_ws >= 4
+    assert L.kvx_paged_writes(4096, P, 1 << 20, P, 4096, 0, P, 1 << 20, P, 4096, 0, 10, P, P,
+                              seg_ws - 1, None) == EINVAL
+    assert L.kvx_paged_writes(4096, P, 1 << 20, P, 4096, 0, P, 1 << 20, P, 4096, 0, 10, None, P,
+                              seg_ws, None) == EINVAL  # no status word
+    # nothing to copy: returns at once, no launch
+    assert L.kvx_paged_writes(4096, P, 1 << 20, P, 4096, 0, P, 1 << 20, P, 4096, 0, 0, P, None, 0,
+                              None) == 0
+    assert L.kvx_seal_blocks(P, P, P, P, 10, P, 10, P, 4, 4, P, P, 1 << 20, P, P, 1 << 20, P, P,
+                             seg_ws - 1, None) == EINVAL
+    assert ws > 0
+
+
+def test_noalloc_pack_rejects_slabs_beyond_its_scratch():
+    L = _lib()
+    assert L.kvx_pack_noalloc(P, 1 << 40, P, P, 10, P, 1 << 34, P, None) == ECAPACITY
