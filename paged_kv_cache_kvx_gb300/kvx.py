@@ -391,3 +391,41 @@ class Transfer:
 
     def read_local(self) -> np.ndarray:
         return _u64_np(self.local)[: self.B * self.L].reshape(self.B, self.L).copy()
+
+
+def overlapped_steps(transfers, pool, slab, dst_pool, n, main, ctl, side):
+    """n passes of the whole path over a stream of transfers, taking the
+    Transfer objects in turn (at least two, each with its own metadata and
+    the same table): the control path of a pass (encode, plan) runs on the
+    ctl stream while the previous pass copies on main, rebuild runs on side
+    next to pack, and a Transfer's next encode waits until its previous
+    pass's copies are done (they read its plan).  Every pass does all five
+    calls; only independent passes overlap."""
+    k = len(transfers)
+    assert k >= 2
+    copied = [None] * k
+    start = torch.cuda.Event()  # ctl and side fork from main (also what a graph capture needs)
+    start.record(main)
+    ctl.wait_event(start)
+    side.wait_event(start)
+    for i in range(n):
+        tr = transfers[i % k]
+        if copied[i % k] is not None:
+            ctl.wait_event(copied[i % k])
+        tr.encode(stream=ctl)
+        tr.plan(stream=ctl)
+        planned = torch.cuda.Event()
+        planned.record(ctl)
+        side.wait_event(planned)
+        tr.rebuild(stream=side)
+        rebuilt = torch.cuda.Event()
+        rebuilt.record(side)
+        main.wait_event(planned)
+        tr.pack(pool, slab, stream=main)
+        tr.unpack(slab, dst_pool, stream=main)
+        main.wait_event(rebuilt)
+        done = torch.cuda.Event()
+        done.record(main)
+        copied[i % k] = done
+    # the last pass's plan and rebuild were joined into main above, so every
+    # operation on ctl and side is ordered before main's end

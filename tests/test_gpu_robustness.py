@@ -80,3 +80,54 @@ def test_identity_plans_copy_every_byte(name):
     assert np.array_equal(plan["groups"]["local"], plan["groups"]["base"])
     assert tr.slab_bytes == wl.pool_bytes
     assert torch.equal(slab, pool)
+
+
+def test_overlapped_transfers_bit_exact():
+    """Independent passes over two metadata sets, each pass's encode and plan
+    overlapping the previous pass's copies (stream launches, then the same
+    passes captured once as a graph and replayed): every output equals the
+    oracle's."""
+    import oracle
+    from paged_kv_cache_kvx_gb300 import kvx, workloads as W
+    wl = {v.name: v for v in W.small_variants()}["worst"]
+    trs = [kvx.Transfer(wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes) for _ in range(2)]
+    for tr in trs:
+        tr.set_addr(wl.addr)
+    host_pool = W.holder_pool_np(wl)
+    pool = torch.from_numpy(host_pool).cuda()
+    slab = torch.zeros(trs[0].slab_bytes, dtype=torch.uint8, device="cuda")
+    dst = torch.full((wl.pool_bytes,), W.CANARY, dtype=torch.uint8, device="cuda")
+    main, ctl, side = (torch.cuda.Stream() for _ in range(3))
+    t = oracle.encode_runs(wl.addr)
+    p = oracle.plan(t, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
+    st, local = oracle.rebuild(t, p, wl.blocks, wl.lanes, wl.seg_len)
+    want_slab = np.zeros(p.slab_bytes, np.uint8)
+    assert oracle.pack(host_pool, p.descs, want_slab) == 0
+    want_dst = np.full(wl.pool_bytes, W.CANARY, np.uint8)
+    assert oracle.unpack(want_slab, p.descs, want_dst) == 0
+
+    def check():
+        for tr in trs:
+            assert tr.read_status() == 0
+            g = tr.read_plan()
+            assert g["descs"].tobytes() == p.descs.tobytes()
+            assert np.array_equal(tr.read_local(), local)
+        assert np.array_equal(slab.cpu().numpy(), want_slab)
+        assert np.array_equal(dst.cpu().numpy(), want_dst)
+
+    kvx.overlapped_steps(trs, pool, slab, dst, 5, main, ctl, side)
+    torch.cuda.synchronize()
+    check()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=main):
+        kvx.overlapped_steps(trs, pool, slab, dst, 4, main, ctl, side)
+    slab.zero_()
+    dst.fill_(W.CANARY)
+    for tr in trs:
+        tr.status.zero_()
+        tr.local.fill_(0)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    check()
