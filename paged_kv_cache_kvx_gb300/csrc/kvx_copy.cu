@@ -245,12 +245,10 @@ struct Grab {
 };
 
 template <bool PACK>
-__global__ void __launch_bounds__(32, kTmaCtasPerSm)
-k_copy_tma(const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r, uint8_t *slab_w,
-           const TmaJob *__restrict__ jobs, CopyCtl *ctl, uint32_t *status) {
-    extern __shared__ __align__(128) uint8_t ring[];
-    __shared__ __align__(8) uint64_t bars[kStages];
-    const uint32_t lane = threadIdx.x;
+__device__ void tile_ring(const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r, uint8_t *slab_w,
+                          const TmaJob *__restrict__ jobs, CopyCtl *ctl, uint32_t *status, uint8_t *ring,
+                          uint64_t *bars) {
+    const uint32_t lane = threadIdx.x & 31;
     if (ctl->bad) return;
     const uint32_t n = ctl->n_tma;
     if (n == 0) return;
@@ -321,6 +319,50 @@ k_copy_tma(const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r, uint8_
         bulk_wait_all();
     }
     __syncwarp();
+}
+
+// The ring path's segments: the pieces of shared tiles listed by the prep.
+template <bool PACK>
+struct PieceGen {
+    const uint8_t *pool_r;
+    uint8_t *pool_w;
+    const uint8_t *slab_r;
+    uint8_t *slab_w;
+    const TmaJob *pieces;
+    const CopyCtl *ctl;
+    uint32_t *st;
+    __device__ uint64_t units() const { return ctl->bad ? 0 : ctl->n_piece; }
+    __device__ ring::Seg get(uint64_t u, uint32_t &) const {
+        const TmaJob j = pieces[u];
+        return PACK ? ring::Seg{pool_r + j.lo + j.delta, slab_w + j.lo, j.len, true}
+                    : ring::Seg{slab_r + j.lo, pool_w + j.lo + j.delta, j.len, true};
+    }
+    __device__ uint32_t *status() const { return st; }
+};
+
+// The bulk-copy kernel, one CTA per SM: warp 0 streams the whole-tile jobs
+// through a ring of 3 x 64 KiB stages; then the same shared memory becomes
+// four rings of 3 x 16 KiB, one per remaining warp, for the pieces of shared
+// tiles.  One launch for both lists: an SM that runs out of tiles moves on
+// to pieces, and a copy without pieces pays nothing for them.
+constexpr int kBulkWarps = 1 + ring::kRingWarps;
+static_assert(kStages * kTileBytes == ring::kRingWarps * ring::kRing * ring::kStageBytes,
+              "the piece rings reuse the tile ring's shared memory");
+
+template <bool PACK>
+__global__ void __launch_bounds__(32 * kBulkWarps, kTmaCtasPerSm)
+k_copy_tma(const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r, uint8_t *slab_w,
+           const TmaJob *__restrict__ jobs, const TmaJob *pieces, CopyCtl *ctl, uint32_t *status) {
+    extern __shared__ __align__(128) uint8_t ring[];
+    __shared__ __align__(8) uint64_t bars[kStages];
+    __shared__ ring::RingSmem rs[ring::kRingWarps];
+    const uint32_t wid = threadIdx.x >> 5;
+    if (wid == 0) tile_ring<PACK>(pool_r, pool_w, slab_r, slab_w, jobs, ctl, status, ring, bars);
+    __syncthreads();  // the tile ring's copies are complete: its stages are free
+    if (!pieces || wid == 0) return;
+    const PieceGen<PACK> g{pool_r, pool_w, slab_r, slab_w, pieces, ctl, status};
+    ring::ring_warp(g, &ctl->seg, ring + (uint64_t)(wid - 1) * ring::kRing * ring::kStageBytes, rs[wid - 1],
+                    threadIdx.x & 31);
 }
 
 // ---------------------------------------------------------- vector path
@@ -440,25 +482,6 @@ cudaError_t set_tma_smem() {
     return e;
 }
 
-// The ring path's segments: the pieces of shared tiles listed by the prep.
-template <bool PACK>
-struct PieceGen {
-    const uint8_t *pool_r;
-    uint8_t *pool_w;
-    const uint8_t *slab_r;
-    uint8_t *slab_w;
-    const TmaJob *pieces;
-    const CopyCtl *ctl;
-    uint32_t *st;
-    __device__ uint64_t units() const { return ctl->bad ? 0 : ctl->n_piece; }
-    __device__ ring::Seg get(uint64_t u, uint32_t &) const {
-        const TmaJob j = pieces[u];
-        return PACK ? ring::Seg{pool_r + j.lo + j.delta, slab_w + j.lo, j.len, true}
-                    : ring::Seg{slab_r + j.lo, pool_w + j.lo + j.delta, j.len, true};
-    }
-    __device__ uint32_t *status() const { return st; }
-};
-
 kvx_status launch(bool pack, const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r,
                   uint8_t *slab_w, uint64_t pool_bytes, uint64_t slab_bytes, const kvx_desc *descs,
                   const uint64_t *num_descs, uint64_t desc_cap, uint32_t *status, void *ws,
@@ -482,15 +505,12 @@ kvx_status launch(bool pack, const uint8_t *pool_r, uint8_t *pool_w, const uint8
     KVX_LAUNCHED();
     const size_t smem = (size_t)kStages * kTileBytes;
     if (pack)
-        k_copy_tma<true><<<sms * kTmaCtasPerSm, 32, smem, s>>>(pool_r, pool_w, slab_r, slab_w, w.jobs, w.ctl, status);
+        k_copy_tma<true><<<sms * kTmaCtasPerSm, 32 * kBulkWarps, smem, s>>>(pool_r, pool_w, slab_r, slab_w,
+                                                                            w.jobs, w.pieces, w.ctl, status);
     else
-        k_copy_tma<false><<<sms * kTmaCtasPerSm, 32, smem, s>>>(pool_r, pool_w, slab_r, slab_w, w.jobs, w.ctl, status);
+        k_copy_tma<false><<<sms * kTmaCtasPerSm, 32 * kBulkWarps, smem, s>>>(pool_r, pool_w, slab_r, slab_w,
+                                                                             w.jobs, w.pieces, w.ctl, status);
     KVX_LAUNCHED();
-    if (w.pieces) {
-        const kvx_status r = pack ? ring::launch_ring(PieceGen<true>{pool_r, pool_w, slab_r, slab_w, w.pieces, w.ctl, status}, &w.ctl->seg, s)
-                                  : ring::launch_ring(PieceGen<false>{pool_r, pool_w, slab_r, slab_w, w.pieces, w.ctl, status}, &w.ctl->seg, s);
-        if (r != KVX_OK) return r;
-    }
     const uint32_t grid = (uint32_t)(sms * kCtasPerSm);
     if (pack)
         k_copy_vec<true><<<grid, kThreads, 0, s>>>(pool_r, pool_w, slab_r, slab_w, pool_bytes,

@@ -149,18 +149,23 @@ struct SegCtl {
     uint32_t next;  // next unclaimed batch
 };
 
+// A ring's bookkeeping in shared memory: one mbarrier per stage, and per
+// stage the store each lane owes (destination, offset in the stage, length).
+struct RingSmem {
+    uint64_t bars[kRing];
+    uint8_t *s_dst[kRing][32];
+    uint32_t s_off[kRing][32], s_len[kRing][32];
+};
+
+// One warp drives one ring: ring points at its kRing * kStageBytes bytes of
+// shared memory.  Batches of 32 segments are claimed from ctl until g has
+// none left.
 template <class Gen>
-__global__ void __launch_bounds__(32 * kRingWarps, 1) k_seg_tma(const __grid_constant__ Gen g, SegCtl *ctl) {
-    extern __shared__ __align__(128) uint8_t ring_all[];
-    __shared__ __align__(8) uint64_t bars_all[kRingWarps][kRing];
-    __shared__ uint8_t *s_dst_all[kRingWarps][kRing][32];
-    __shared__ uint32_t s_off_all[kRingWarps][kRing][32], s_len_all[kRingWarps][kRing][32];
-    const uint32_t lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    uint8_t *ring = ring_all + (uint64_t)wid * kRing * kStageBytes;
-    uint64_t *bars = bars_all[wid];
-    auto &s_dst = s_dst_all[wid];
-    auto &s_off = s_off_all[wid];
-    auto &s_len = s_len_all[wid];
+__device__ void ring_warp(const Gen &g, SegCtl *ctl, uint8_t *ring, RingSmem &rs, uint32_t lane) {
+    uint64_t *bars = rs.bars;
+    auto &s_dst = rs.s_dst;
+    auto &s_off = rs.s_off;
+    auto &s_len = rs.s_len;
     const uint64_t units = g.units();
     const uint64_t nb = ceil_div(units, 32);
     if (lane == 0) {
@@ -254,6 +259,14 @@ __global__ void __launch_bounds__(32 * kRingWarps, 1) k_seg_tma(const __grid_con
     }
     bulk_wait_all();
     warp_raise(g.status(), bad, lane);
+}
+
+template <class Gen>
+__global__ void __launch_bounds__(32 * kRingWarps, 1) k_seg_tma(const __grid_constant__ Gen g, SegCtl *ctl) {
+    extern __shared__ __align__(128) uint8_t ring_all[];
+    __shared__ RingSmem rs[kRingWarps];
+    const uint32_t wid = threadIdx.x >> 5;
+    ring_warp(g, ctl, ring_all + (uint64_t)wid * kRing * kStageBytes, rs[wid], threadIdx.x & 31);
 }
 
 template <class Gen>
