@@ -101,6 +101,41 @@ __device__ __forceinline__ bool in_range(uint64_t off, uint64_t len, uint64_t si
     return off <= size && len <= size - off;
 }
 
+// The fields of a descriptor the tile lists need, in two loads.
+struct DescView {
+    uint64_t remote, local, len;
+};
+__device__ __forceinline__ DescView load_desc(const kvx_desc *d) {
+    const ulonglong2 rl = __ldg(reinterpret_cast<const ulonglong2 *>(d));  // remote, local
+    return DescView{rl.x, rl.y, __ldg(&d->len)};
+}
+
+// The descriptors from a on that start below hi, at most kWalkMax of them,
+// in batches whose loads are issued together: f(e) for each; f returns false
+// to stop.  Returns false when the walk hit kWalkMax with descriptors left
+// (more than kPiecesPerTile pieces: some descriptor there is too short for
+// the ring path anyway).
+constexpr int kWalkBatch = 4;
+constexpr uint64_t kWalkMax = kPiecesPerTile + 1;
+
+template <class F>
+__device__ __forceinline__ bool walk_tile_descs(const kvx_desc *__restrict__ descs, uint64_t n, uint64_t a,
+                                                uint64_t hi, F &&f) {
+    const uint64_t end = n - a < kWalkMax ? n : a + kWalkMax;
+    for (uint64_t k0 = a; k0 < end; k0 += kWalkBatch) {
+        DescView e[kWalkBatch];
+#pragma unroll
+        for (int j = 0; j < kWalkBatch; j++)
+            if (k0 + j < end) e[j] = load_desc(descs + k0 + j);
+#pragma unroll
+        for (int j = 0; j < kWalkBatch; j++) {
+            if (k0 + j >= end || e[j].local >= hi) return true;
+            if (!f(e[j])) return true;
+        }
+    }
+    return end == n;
+}
+
 // Descriptor checks (one thread per descriptor: tiling, bounds), then one
 // thread per tile: the descriptor holding the tile's first byte (binary
 // search) and the tile's list.
@@ -140,14 +175,19 @@ k_copy_prep(const kvx_desc *__restrict__ descs, const uint64_t *__restrict__ num
     const kvx_desc last = descs[n - 1];
     const uint64_t used = last.local + last.len < slab_bytes ? last.local + last.len : slab_bytes;
     const uint64_t ntiles = ceil_div(used, kTileBytes);
+    // Every block takes a contiguous share of the tiles, so the walks over
+    // shared tiles (one cache line per descriptor and lane) spread over all SMs.
     const uint32_t lane = threadIdx.x & 31;
-    for (uint64_t t0 = tid - lane; t0 < ntiles; t0 += stride) {  // warp-uniform loop
+    const uint64_t per = ceil_div(ntiles, (uint64_t)gridDim.x);
+    const uint64_t tb = (uint64_t)blockIdx.x * per;
+    const uint64_t te = tb + per < ntiles ? tb + per : ntiles;
+    for (uint64_t t0 = tb + (threadIdx.x - lane); t0 < te; t0 += blockDim.x) {  // warp-uniform loop
         const uint64_t t = t0 + lane;
         bool is_tma = false, is_vec = false;
         uint32_t npieces = 0;  // this tile's pieces for the ring path (0: not on it)
         uint64_t lo = 0, hi = 0, a = 0;
         TmaJob job{};
-        if (t < ntiles) {
+        if (t < te) {
             lo = t * kTileBytes;
             hi = lo + kTileBytes < used ? lo + kTileBytes : used;
             uint64_t z = n;  // last k with descs[k].local <= lo, in [a, z)
@@ -172,21 +212,20 @@ k_copy_prep(const kvx_desc *__restrict__ descs, const uint64_t *__restrict__ num
                     // and long enough for the bulk engine
                     bool fit = true, short_desc = false;
                     uint32_t np = 0;
-                    for (uint64_t k = a; k < n; k++) {
-                        const kvx_desc e = descs[k];
-                        if (e.local >= hi) break;
+                    const bool whole = walk_tile_descs(descs, n, a, hi, [&](const DescView &e) {
                         const uint64_t plo = e.local > lo ? e.local : lo;
                         const uint64_t phi = e.len < hi - e.local ? e.local + e.len : hi;
-                        if (plo >= phi) continue;
+                        if (plo >= phi) return true;
                         if (e.len < kPieceMinDesc || ((plo | phi | (e.remote - e.local)) & 15)) {
                             fit = false;
-                            break;
+                            return false;
                         }
                         short_desc |= e.len < kPieceMaxDesc;
                         if (in_range(e.remote, e.len, pool_bytes) && in_range(e.local, e.len, slab_bytes))
                             np++;  // a descriptor outside the pool or slab is skipped
-                    }
-                    if (fit && short_desc && np <= kPiecesPerTile) {
+                        return true;
+                    });
+                    if (whole && fit && short_desc && np <= kPiecesPerTile) {
                         is_vec = false;
                         npieces = np;
                     }
@@ -212,18 +251,18 @@ k_copy_prep(const kvx_desc *__restrict__ descs, const uint64_t *__restrict__ num
             if (lane == 0 && wtot) bp = atomicAdd(&ctl->n_piece, wtot);
             bp = __shfl_sync(0xFFFFFFFFu, bp, 0) + incl - npieces;
             if (npieces) {
-                for (uint64_t k = a; k < n; k++) {
-                    const kvx_desc e = descs[k];
-                    if (e.local >= hi) break;
+                const uint64_t cap = (uint64_t)kPiecesPerTile * ntiles;
+                walk_tile_descs(descs, n, a, hi, [&](const DescView &e) {
                     const uint64_t plo = e.local > lo ? e.local : lo;
                     const uint64_t phi = e.len < hi - e.local ? e.local + e.len : hi;
-                    if (plo >= phi) continue;
+                    if (plo >= phi) return true;
                     if (!(in_range(e.remote, e.len, pool_bytes) && in_range(e.local, e.len, slab_bytes)))
-                        continue;
-                    if (bp < (uint64_t)kPiecesPerTile * ntiles)  // always: at most kPiecesPerTile per tile
+                        return true;
+                    if (bp < cap)  // always: at most kPiecesPerTile per tile
                         pieces[bp] = TmaJob{plo, e.remote - e.local, (uint32_t)(phi - plo), 0};
                     bp++;
-                }
+                    return true;
+                });
             }
         }
     }
