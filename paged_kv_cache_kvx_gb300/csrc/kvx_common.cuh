@@ -55,25 +55,6 @@ __device__ __forceinline__ void raise(uint32_t *st, uint32_t bits) {
     if (bits) atomicOr(st, bits);
 }
 
-// Last-block ticket: every block of the grid calls this after its global
-// writes; it returns true in exactly one block, the last to arrive, which
-// then sees every other block's writes.  Nothing waits: blocks that are not
-// last simply go on (and exit).  The counter is left at zero.
-__device__ __forceinline__ bool last_block(uint32_t *ticket) {
-    __shared__ bool s_last;
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const uint32_t total = gridDim.x * gridDim.y * gridDim.z;
-        const uint32_t t = atomicAdd(ticket, 1u);
-        s_last = (t == total - 1);
-        if (s_last) atomicExch(ticket, 0u);
-    }
-    __syncthreads();
-    if (s_last) __threadfence();
-    return s_last;
-}
-
 // Grid barrier for cooperative launches (every participating block is
 // resident).  One monotonic arrival counter, zeroed before the launch: the
 // arrivals of the k-th barrier are exactly k*nblocks .. (k+1)*nblocks - 1 (no
@@ -86,9 +67,7 @@ __device__ __forceinline__ bool last_block(uint32_t *ticket) {
 // is a plain __syncthreads().
 struct GridSync {
     uint32_t count;
-    uint32_t gen;  // unused
     uint32_t abort;
-    uint32_t pad;
 };
 
 // Waits are bounded in time (%globaltimer nanoseconds) with a poll-count
