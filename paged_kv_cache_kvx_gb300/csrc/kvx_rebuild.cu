@@ -7,9 +7,11 @@
 //                          = G.local + i * G.stride + run_off[r]
 //   non-dense group: local = G.local + i * G.chunk + run_off[r]
 // (the page's formula, and its dense local mirror of each remote block).
-// The checks: the group index is valid, b is inside the group's block range,
-// [local, local + len) lies inside block i's slice [G.local + i*chunk,
-// G.local + (i+1)*chunk) of the carve, and the carve ends inside the slab.
+// The checks: the group index is valid, the run starts at the group's first
+// block, b is inside the group's block range, [local, local + len) lies
+// inside block i's slice [G.local + i*chunk, G.local + (i+1)*chunk) of the
+// carve, and the carve ends inside the slab.  The call is not given the runs'
+// strides: a dense group's stride stands for them.
 //
 // Thread layout as in the encoder: a CTA is 8 warps; lane t of warp w handles
 // lane l0 + t over K consecutive blocks, so each warp store is one coalesced
@@ -126,15 +128,16 @@ k_rebuild(const uint32_t *__restrict__ lane_first, const uint32_t *__restrict__ 
         g_count = G.count;
         off = run_off[r];
         rb = run_block[r];
-        // the carve of the group ends inside the slab
+        // the carve of the group ends inside the slab, and the run starts at
+        // the group's first block (every run of a group does)
         if ((__int128)g_local + (__int128)G.count * (__int128)g_chunk > (__int128)slab_bytes) return;
+        if (rb != g_block) return;
         if (G.dense && G.count > 1 && (__int128)g_stride != (__int128)g_chunk) {
             general = true;
             return;
         }
         if (!(off <= g_chunk && len <= g_chunk - off)) return;  // the segment overruns its slice
-        vs = g_block > rb ? g_block : rb;
-        if (vs < b) vs = b;
+        vs = g_block > b ? g_block : b;
         ve = g_block + g_count;
         if (vs < ve) v = g_local + (vs - g_block) * g_chunk + off;
     };
@@ -157,7 +160,7 @@ k_rebuild(const uint32_t *__restrict__ lane_first, const uint32_t *__restrict__ 
         if (b >= vs && b < ve) {
             out = v;
             v += g_chunk;
-        } else if (general && b >= g_block && b - g_block < g_count && rb <= b) {
+        } else if (general && b >= g_block && b - g_block < g_count) {
             // dense: remote(b) - group_remote advances by the stride
             const uint64_t i = b - g_block;
             const __int128 loc = (__int128)g_local + (__int128)i * g_stride + (__int128)off;

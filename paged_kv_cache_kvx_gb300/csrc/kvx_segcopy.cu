@@ -120,10 +120,12 @@ __device__ __forceinline__ Seg seal_seg(const SealArgs &a, uint64_t s, uint64_t 
             if (a.run_block[m] <= b) x = m; else z = m;
         }
         const uint32_t gi = a.run_group[x];
-        if (gi < ngroups && a.run_block[x] <= b) {
+        const uint32_t rb = a.run_block[x];
+        if (gi < ngroups && rb <= b) {
             const kvx_group G = a.groups[gi];
             const __int128 g_local = (__int128)G.local, g_chunk = (__int128)G.chunk;
-            if (b >= G.block && b - G.block < G.count &&
+            // the run starts at the group's first block (every run of a group does)
+            if (rb == G.block && b >= G.block && b - G.block < G.count &&
                 g_local + (__int128)G.count * g_chunk <= (__int128)a.slab_bytes) {
                 const __int128 i = (__int128)(b - G.block);
                 const __int128 step = G.dense ? (__int128)G.stride : g_chunk;

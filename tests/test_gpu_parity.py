@@ -263,6 +263,44 @@ def test_rebuild_bounds_match_oracle():
     assert np.array_equal(tr.read_local(), want)
 
 
+@pytest.mark.parametrize("mutate", ["block", "count", "dense", "off", "chunk_small", "local"])
+def test_rebuild_corrupt_groups_match_oracle(mutate):
+    """Group records that break one check each, on groups of many blocks: the
+    first block moved (its runs no longer start there), the block count cut,
+    a non-dense group marked dense (its stride then differs from its chunk
+    and every block is checked on its own), the chunk one byte short of its
+    last run's end, a chunk shorter than the segments, a carve past the slab.
+    Every pointer and the status word match the oracle's rebuild of the same
+    records, which works from the runs' own addresses."""
+    wl = {v.name: v for v in W.small_variants()}["many_small" if mutate == "dense" else "default_s"]
+    B, L = wl.addr.shape
+    t, p, st, local = oracle_all(wl.addr, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
+    tr = gpu_plan(wl.addr, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
+    g = p.groups.copy()
+    k = int(np.flatnonzero(g["count"] > 1)[0])
+    if mutate == "block":
+        g["block"][k] += 1
+    elif mutate == "count":
+        g["count"][k] -= 1
+    elif mutate == "dense":
+        nd = np.flatnonzero((g["dense"] == 0) & (g["count"] > 1))
+        g["dense"][int(nd[0])] = 1
+    elif mutate == "off":
+        g["chunk"][k] -= 1
+    elif mutate == "chunk_small":
+        g["chunk"][k] = max(1, int(g["chunk"][k]) // 3)
+    else:
+        g["local"][k] += np.uint64(p.slab_bytes)
+    tr.groups[: g.nbytes].copy_(torch.from_numpy(g.view(np.uint8)))
+    tr.status.zero_()
+    tr.rebuild()
+    torch.cuda.synchronize()
+    stw, want = oracle.rebuild(t, p, B, L, wl.seg_len, groups=g)
+    assert stw == oracle.S_BOUNDS
+    assert tr.read_status() == stw
+    assert np.array_equal(tr.read_local(), want)
+
+
 def test_pack_descriptor_checks_match_oracle():
     wl = W.tiny()
     t, p, st, local = oracle_all(wl.addr, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)

@@ -282,6 +282,19 @@ def test_seal_corrupt_groups():
                       groups=groups) == oracle.S_BOUNDS
 
 
+def test_seal_group_block_moved():
+    """A group whose first block no longer matches its runs' first block: every
+    segment of its runs is rejected, as in the oracle's seal."""
+    wl = {v.name: v for v in W.small_variants()}["default_s"]
+    B, L = wl.addr.shape
+    p = oracle.plan(oracle.encode_runs(wl.addr), B, wl.seg_len, wl.numa, wl.pool_bytes)
+    groups = p.groups.copy()
+    groups["block"][0] += np.uint32(1)
+    dst_addr, size = receiver_layout(B, wl.seg_len)
+    assert check_seal(wl.addr, B, wl.seg_len, wl.numa, wl.pool_bytes, dst_addr, size,
+                      groups=groups) == oracle.S_BOUNDS
+
+
 @pytest.mark.parametrize("bulk", [True, False])
 def test_seal_full_size_default(bulk):
     """The default workload end to end on the device: pack, then seal into a
