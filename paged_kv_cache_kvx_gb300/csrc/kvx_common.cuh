@@ -122,14 +122,22 @@ __device__ __forceinline__ bool grid_barrier(GridSync *gs, uint32_t nblocks) {
 }
 
 // Loads that bypass L1: data other blocks wrote earlier in the same kernel.
+// Types aligned to 16 bytes move in 16-byte pieces, others in 8-byte ones.
 template <class T>
 __device__ __forceinline__ T ld_cg(const T *p) {
     static_assert(sizeof(T) % 8 == 0, "8-byte multiple");
     T v;
-    const unsigned long long *src = reinterpret_cast<const unsigned long long *>(p);
-    unsigned long long *dst = reinterpret_cast<unsigned long long *>(&v);
+    if constexpr (alignof(T) >= 16 && sizeof(T) % 16 == 0) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(p);
+        uint4 *dst = reinterpret_cast<uint4 *>(&v);
 #pragma unroll
-    for (int i = 0; i < (int)(sizeof(T) / 8); i++) dst[i] = __ldcg(src + i);
+        for (int i = 0; i < (int)(sizeof(T) / 16); i++) dst[i] = __ldcg(src + i);
+    } else {
+        const unsigned long long *src = reinterpret_cast<const unsigned long long *>(p);
+        unsigned long long *dst = reinterpret_cast<unsigned long long *>(&v);
+#pragma unroll
+        for (int i = 0; i < (int)(sizeof(T) / 8); i++) dst[i] = __ldcg(src + i);
+    }
     return v;
 }
 

@@ -49,7 +49,7 @@ struct PlanCtl {
 
 // Sort record; r holds the run index in its low 31 bits and, in the top bit,
 // whether the run's segments are empty (zero-size V lane).
-struct SortItem {
+struct __align__(16) SortItem {
     uint64_t base;
     uint32_t node;
     uint32_t r;
@@ -60,14 +60,14 @@ constexpr uint32_t kEmptyDigit = 12;  // radix digit of the empty flag
 
 __device__ __forceinline__ uint32_t item_run(const SortItem &it) { return it.r & ~kEmptyBit; }
 
-struct Rec {
+struct __align__(16) Rec {
     uint64_t base;
     int64_t stride;
     uint32_t len, block, count, node, r, pad;
 };
 
 // Segmented sum: value since the last segment head, and whether a head was seen.
-struct Seg {
+struct __align__(16) Seg {
     uint64_t sum;
     uint32_t head;
     uint32_t pad;
@@ -81,7 +81,7 @@ struct MaxOp {
     __device__ int64_t operator()(int64_t a, int64_t b) const { return a > b ? a : b; }
 };
 // Group numbering: starts so far and position of the last start.
-struct GAgg {
+struct __align__(16) GAgg {
     uint64_t n;
     int64_t last;
 };
@@ -91,7 +91,7 @@ struct GOp {
     }
 };
 // Carve: slab bytes and descriptor count so far.
-struct CAgg {
+struct __align__(16) CAgg {
     uint64_t bytes;
     uint64_t descs;
 };
