@@ -38,6 +38,8 @@ namespace {
 constexpr int kThreads = 256;
 constexpr uint64_t kTileBytes = 64 * 1024;
 constexpr int kVecPerThread = (int)(kTileBytes / (kThreads * 16));  // 16
+constexpr int kBucketShift = 6;                                       // 64-byte buckets of a vector tile
+constexpr int kBuckets = (int)(kTileBytes >> kBucketShift);          // 1024
 constexpr int kCtasPerSm = 3;
 constexpr int kStages = 3;                  // TMA ring depth per CTA
 constexpr int kTmaCtasPerSm = 1;
@@ -423,6 +425,7 @@ k_copy_vec(const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r, uint8_
     __shared__ uint64_t s_lo[kThreads + 1];
     __shared__ uint64_t s_delta[kThreads];
     __shared__ uint8_t s_ok[kThreads];
+    __shared__ uint16_t s_first[kBuckets];  // per 64-byte bucket: the last span starting at or before it
     if (ctl->bad) return;
     const uint64_t n = *num_descs < desc_cap ? *num_descs : desc_cap;
     const uint64_t used = ctl->used < slab_bytes ? ctl->used : slab_bytes;
@@ -462,6 +465,19 @@ k_copy_vec(const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r, uint8_
             if (nb == 0) break;
             const uint64_t bhi = s_lo[nb];
             if (all_aligned) {
+                // One search per bucket instead of one per vector: a vector
+                // starts from its bucket's span and steps forward (aligned
+                // spans are at least 16 bytes, so at most three steps).
+                for (uint32_t b = threadIdx.x; b < (uint32_t)kBuckets; b += kThreads) {
+                    const uint64_t xs = lo + ((uint64_t)b << kBucketShift);
+                    int a = 0, z = nb;  // last span with s_lo <= xs
+                    while (z - a > 1) {
+                        const int m = (a + z) >> 1;
+                        if (s_lo[m] <= xs) a = m; else z = m;
+                    }
+                    s_first[b] = (uint16_t)a;
+                }
+                __syncthreads();
                 constexpr int U = kVecPerThread / 2;
                 for (uint64_t x = lo + (uint64_t)threadIdx.x * 16; x < bhi;
                      x += (uint64_t)kThreads * 16 * U) {
@@ -470,12 +486,10 @@ k_copy_vec(const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r, uint8_
 #pragma unroll
                     for (int u = 0; u < U; u++) {
                         const uint64_t xx = x + (uint64_t)u * kThreads * 16;
-                        int a = 0, z = nb;  // last span with s_lo <= xx
-                        while (z - a > 1) {
-                            const int m = (a + z) >> 1;
-                            if (s_lo[m] <= xx) a = m; else z = m;
-                        }
                         dst[u] = ~0ull;
+                        if (xx >= bhi) continue;
+                        int a = s_first[(xx - lo) >> kBucketShift];  // last span with s_lo <= xx
+                        while (a + 1 < nb && s_lo[a + 1] <= xx) a++;
                         if (xx < bhi && s_ok[a]) {
                             const uint64_t px = xx + s_delta[a];
                             v[u] = PACK ? ld_stream(pool_r + px) : ld_stream(slab_r + xx);
