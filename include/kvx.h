@@ -19,6 +19,10 @@
  *                    segments -> dense staging slab
  *   kvx_unpack       the inverse copy: slab -> a pool with the holder's layout
  *                    (not on the page; it closes the round trip)
+ *   kvx_copy_prepare, kvx_pack_prepared, kvx_unpack_prepared
+ *                    the same two copies split into a preparation (checks,
+ *                    tile lists) and the byte movement, so one copy can be
+ *                    prepared while another runs
  *
  * and the steps around it that the pages name next:
  *
@@ -86,7 +90,8 @@ typedef enum kvx_status {
 #define KVX_S_SPAN       32u   /* a run's remote span wraps or leaves the holder pool */
 #define KVX_S_STRIDE1    64u   /* a one-block run with a nonzero stride */
 #define KVX_S_BOUNDS     128u  /* a pointer or copy outside its slab/pool/group range */
-#define KVX_S_DESC       256u  /* descriptors do not tile the slab in order */
+#define KVX_S_DESC       256u  /* descriptors do not tile the slab in order, or a prepared
+                                  copy's lists were not made for it (kvx_copy_prepare) */
 #define KVX_S_CAPACITY   512u  /* a plan output exceeds its capacity, or the slab 2^63 bytes */
 #define KVX_S_TIMEOUT    1024u /* a copy kernel's bounded wait on its own bulk copy gave up
                                   (the GPU did not deliver the bytes; the copy is incomplete) */
@@ -382,6 +387,40 @@ kvx_status kvx_paged_writes(uint64_t page_len,
                             uint64_t dst_offset,
                             uint64_t num_pages, uint32_t *status,
                             void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * kvx_pack / kvx_unpack in two stages, so that the descriptor checks and the
+ * tile lists of a copy can be made while another copy runs (a receiver can
+ * prepare its unpack as soon as the plan is known, before the bytes arrive).
+ * No counterpart in the paper: a packaging of the same data movement (Requester
+ * step 4).
+ *
+ * kvx_copy_prepare runs the checks of kvx_pack / kvx_unpack (KVX_S_DESC,
+ * KVX_S_BOUNDS into *status) and writes the tile lists into ws.  pool and slab
+ * (device pointers, not dereferenced here) only decide whether the 16-byte
+ * bulk paths may be used; pass the buffers the copy will use, or any with the
+ * same alignment.  A following kvx_pack_prepared or kvx_unpack_prepared with
+ * the same descs, num_descs, desc_capacity, pool_bytes, slab_bytes and ws moves
+ * the bytes exactly as kvx_pack / kvx_unpack would; it must be ordered after
+ * the preparation (same stream, or an event), and the descriptors must not
+ * change in between.  One preparation serves one copy.  A copy along lists
+ * that were made for other arguments, or that another copy already used,
+ * moves nothing and raises KVX_S_DESC.  Arguments, sizes, ownership and
+ * return codes as for kvx_pack / kvx_unpack; ws is sized by
+ * kvx_copy_workspace_size(slab_bytes).
+ */
+kvx_status kvx_copy_prepare(const void *pool, uint64_t pool_bytes,
+                            const kvx_desc *descs, const uint64_t *num_descs,
+                            uint64_t desc_capacity, const void *slab, uint64_t slab_bytes,
+                            uint32_t *status, void *ws, size_t ws_bytes, void *stream);
+kvx_status kvx_pack_prepared(const uint8_t *pool, uint64_t pool_bytes,
+                             const kvx_desc *descs, const uint64_t *num_descs,
+                             uint64_t desc_capacity, uint8_t *slab, uint64_t slab_bytes,
+                             uint32_t *status, void *ws, size_t ws_bytes, void *stream);
+kvx_status kvx_unpack_prepared(const uint8_t *slab, uint64_t slab_bytes,
+                               const kvx_desc *descs, const uint64_t *num_descs,
+                               uint64_t desc_capacity, uint8_t *dst_pool, uint64_t pool_bytes,
+                               uint32_t *status, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * kvx_pack without a caller workspace, for callers that cannot allocate

@@ -52,6 +52,8 @@ struct CopyCtl {
     uint32_t next_job;        // next unclaimed TMA job
     uint32_t n_piece;         // descriptor pieces of shared tiles for the ring path
     ring::SegCtl seg;         // claim counter of the ring path
+    uint32_t users;           // bulk-kernel blocks that have started on these lists
+    unsigned long long key;   // the copy the lists were made for (see copy_key)
 };
 
 // A tile shared by several descriptors goes to the ring path of kvx_ring.cuh
@@ -146,7 +148,8 @@ k_copy_prep(const kvx_desc *__restrict__ descs, const uint64_t *__restrict__ num
             uint64_t desc_cap, uint64_t pool_bytes, uint64_t slab_bytes, bool bases_aligned,
             uint32_t *__restrict__ tile_desc, TmaJob *__restrict__ jobs,
             uint32_t *__restrict__ vec_tiles, TmaJob *__restrict__ pieces, CopyCtl *ctl,
-            uint32_t *status) {
+            uint32_t *status, unsigned long long key) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) ctl->key = key;
     const uint64_t n = *num_descs < desc_cap ? *num_descs : desc_cap;
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
     const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -393,10 +396,22 @@ static_assert(kStages * kTileBytes == ring::kRingWarps * ring::kRing * ring::kSt
 template <bool PACK>
 __global__ void __launch_bounds__(32 * kBulkWarps, kTmaCtasPerSm)
 k_copy_tma(const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r, uint8_t *slab_w,
-           const TmaJob *__restrict__ jobs, const TmaJob *pieces, CopyCtl *ctl, uint32_t *status) {
+           const TmaJob *__restrict__ jobs, const TmaJob *pieces, CopyCtl *ctl, uint32_t *status,
+           unsigned long long key) {
     extern __shared__ __align__(128) uint8_t ring[];
     __shared__ __align__(8) uint64_t bars[kStages];
     __shared__ ring::RingSmem rs[ring::kRingWarps];
+    __shared__ bool s_go;
+    // The lists must have been made for this copy, and serve one copy: a
+    // second launch on them finds the tile claims spent, so it stops here.
+    if (threadIdx.x == 0) {
+        const bool mine = ctl->key == key;
+        const bool first = atomicAdd(&ctl->users, 1u) < gridDim.x;
+        s_go = mine && first;
+        if (!s_go && blockIdx.x == 0) atomicOr(status, KVX_S_DESC);
+    }
+    __syncthreads();
+    if (!s_go) return;
     const uint32_t wid = threadIdx.x >> 5;
     if (wid == 0) tile_ring<PACK>(pool_r, pool_w, slab_r, slab_w, jobs, ctl, status, ring, bars);
     __syncthreads();  // the tile ring's copies are complete: its stages are free
@@ -421,12 +436,13 @@ k_copy_vec(const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r, uint8_
            uint64_t pool_bytes, uint64_t slab_bytes, bool bases_aligned,
            const kvx_desc *__restrict__ descs, const uint64_t *__restrict__ num_descs,
            uint64_t desc_cap, const uint32_t *__restrict__ tile_desc,
-           const uint32_t *__restrict__ vec_tiles, const CopyCtl *ctl) {
+           const uint32_t *__restrict__ vec_tiles, const CopyCtl *ctl, unsigned long long key,
+           uint32_t bulk_blocks) {
     __shared__ uint64_t s_lo[kThreads + 1];
     __shared__ uint64_t s_delta[kThreads];
     __shared__ uint8_t s_ok[kThreads];
     __shared__ uint16_t s_first[kBuckets];  // per 64-byte bucket: the last span starting at or before it
-    if (ctl->bad) return;
+    if (ctl->bad || ctl->key != key || ctl->users != bulk_blocks) return;
     const uint64_t n = *num_descs < desc_cap ? *num_descs : desc_cap;
     const uint64_t used = ctl->used < slab_bytes ? ctl->used : slab_bytes;
     const uint32_t nlist = ctl->n_vec;
@@ -535,46 +551,110 @@ cudaError_t set_tma_smem() {
     return e;
 }
 
-kvx_status launch(bool pack, const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r,
-                  uint8_t *slab_w, uint64_t pool_bytes, uint64_t slab_bytes, const kvx_desc *descs,
-                  const uint64_t *num_descs, uint64_t desc_cap, uint32_t *status, void *ws,
-                  size_t ws_bytes, void *stream) {
+// Identifies the copy a workspace's lists were made for: the descriptor
+// arrays, the sizes, whether the bases are 16-byte aligned, whether the piece
+// list is in use, and the workspace itself.  The pool and slab addresses enter
+// only through their alignment (the lists hold offsets), so one preparation
+// serves a pack or an unpack alike; it serves one copy.
+unsigned long long copy_key(const kvx_desc *descs, const uint64_t *num_descs, uint64_t desc_cap,
+                            uint64_t pool_bytes, uint64_t slab_bytes, bool aligned, bool pieces,
+                            const void *ws) {
+    const uint64_t parts[] = {reinterpret_cast<uintptr_t>(descs), reinterpret_cast<uintptr_t>(num_descs),
+                              desc_cap, pool_bytes, slab_bytes, (aligned ? 1u : 0u) | (pieces ? 2u : 0u),
+                              reinterpret_cast<uintptr_t>(ws)};
+    uint64_t h = 0x243F6A8885A308D3ull;
+    for (uint64_t x : parts) {  // splitmix64 finaliser over the running state
+        h ^= x + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+        h ^= h >> 30;
+        h *= 0xBF58476D1CE4E5B9ull;
+        h ^= h >> 27;
+        h *= 0x94D049BB133111EBull;
+        h ^= h >> 31;
+    }
+    return h | 1;  // a cleared workspace (key 0) matches no copy
+}
+
+// The host-side checks and the workspace layout shared by every copy call.
+struct CopySetup {
+    Ws w;
+    bool aligned;
+    unsigned long long key;
+};
+
+kvx_status setup(const void *pool, uint64_t pool_bytes, const void *slab, uint64_t slab_bytes,
+                 const kvx_desc *descs, const uint64_t *num_descs, uint64_t desc_cap, uint32_t *status,
+                 void *ws, size_t ws_bytes, CopySetup *cs) {
     if (!descs || !num_descs || !status || !ws) return KVX_EINVAL;
-    if ((pool_bytes && !(pool_r || pool_w)) || (slab_bytes && !(slab_r || slab_w))) return KVX_EINVAL;
+    if ((pool_bytes && !pool) || (slab_bytes && !slab)) return KVX_EINVAL;
     size_t need = 0, need_base = 0;
-    Ws w = carve(ws, slab_bytes, &need, &need_base);
+    cs->w = carve(ws, slab_bytes, &need, &need_base);
     if (ws_bytes < need_base) return KVX_EINVAL;
-    if (ws_bytes < need) w.pieces = nullptr;  // shared tiles stay on the register path
-    if ((pack ? set_tma_smem<true>() : set_tma_smem<false>()) != cudaSuccess) return KVX_ECUDA;
-    cudaStream_t s = as_stream(stream);
-    if (cudaMemsetAsync(w.ctl, 0, sizeof(CopyCtl), s) != cudaSuccess) return KVX_ECUDA;
-    const uintptr_t pa = reinterpret_cast<uintptr_t>(pool_r ? (const void *)pool_r : pool_w);
-    const uintptr_t sa = reinterpret_cast<uintptr_t>(slab_r ? (const void *)slab_r : slab_w);
-    const bool aligned = ((pa | sa) & 15) == 0;
-    const int sms = sm_count();
-    k_copy_prep<<<sms * 2, kThreads, 0, s>>>(descs, num_descs, desc_cap, pool_bytes, slab_bytes,
-                                              aligned, w.tile_desc, w.jobs, w.vec_tiles, w.pieces,
-                                              w.ctl, status);
+    if (ws_bytes < need) cs->w.pieces = nullptr;  // shared tiles stay on the register path
+    cs->aligned = ((reinterpret_cast<uintptr_t>(pool) | reinterpret_cast<uintptr_t>(slab)) & 15) == 0;
+    cs->key = copy_key(descs, num_descs, desc_cap, pool_bytes, slab_bytes, cs->aligned, cs->w.pieces != nullptr,
+                       ws);
+    return KVX_OK;
+}
+
+// The descriptor checks and the tile lists (clears the control block first).
+kvx_status launch_prep(const CopySetup &cs, uint64_t pool_bytes, uint64_t slab_bytes, const kvx_desc *descs,
+                       const uint64_t *num_descs, uint64_t desc_cap, uint32_t *status, cudaStream_t s) {
+    if (cudaMemsetAsync(cs.w.ctl, 0, sizeof(CopyCtl), s) != cudaSuccess) return KVX_ECUDA;
+    k_copy_prep<<<sm_count() * 2, kThreads, 0, s>>>(descs, num_descs, desc_cap, pool_bytes, slab_bytes,
+                                                     cs.aligned, cs.w.tile_desc, cs.w.jobs, cs.w.vec_tiles,
+                                                     cs.w.pieces, cs.w.ctl, status, cs.key);
     KVX_LAUNCHED();
+    return KVX_OK;
+}
+
+// The byte movement along prepared lists: the bulk kernel, then the vector path.
+kvx_status launch_copy(bool pack, const CopySetup &cs, const uint8_t *pool_r, uint8_t *pool_w,
+                       const uint8_t *slab_r, uint8_t *slab_w, uint64_t pool_bytes, uint64_t slab_bytes,
+                       const kvx_desc *descs, const uint64_t *num_descs, uint64_t desc_cap, uint32_t *status,
+                       cudaStream_t s) {
+    if ((pack ? set_tma_smem<true>() : set_tma_smem<false>()) != cudaSuccess) return KVX_ECUDA;
+    const int sms = sm_count();
+    const uint32_t bulk = (uint32_t)(sms * kTmaCtasPerSm);
     const size_t smem = (size_t)kStages * kTileBytes;
+    const Ws &w = cs.w;
     if (pack)
-        k_copy_tma<true><<<sms * kTmaCtasPerSm, 32 * kBulkWarps, smem, s>>>(pool_r, pool_w, slab_r, slab_w,
-                                                                            w.jobs, w.pieces, w.ctl, status);
+        k_copy_tma<true><<<bulk, 32 * kBulkWarps, smem, s>>>(pool_r, pool_w, slab_r, slab_w, w.jobs, w.pieces,
+                                                             w.ctl, status, cs.key);
     else
-        k_copy_tma<false><<<sms * kTmaCtasPerSm, 32 * kBulkWarps, smem, s>>>(pool_r, pool_w, slab_r, slab_w,
-                                                                             w.jobs, w.pieces, w.ctl, status);
+        k_copy_tma<false><<<bulk, 32 * kBulkWarps, smem, s>>>(pool_r, pool_w, slab_r, slab_w, w.jobs, w.pieces,
+                                                              w.ctl, status, cs.key);
     KVX_LAUNCHED();
     const uint32_t grid = (uint32_t)(sms * kCtasPerSm);
     if (pack)
-        k_copy_vec<true><<<grid, kThreads, 0, s>>>(pool_r, pool_w, slab_r, slab_w, pool_bytes,
-                                                   slab_bytes, aligned, descs, num_descs, desc_cap,
-                                                   w.tile_desc, w.vec_tiles, w.ctl);
+        k_copy_vec<true><<<grid, kThreads, 0, s>>>(pool_r, pool_w, slab_r, slab_w, pool_bytes, slab_bytes,
+                                                   cs.aligned, descs, num_descs, desc_cap, w.tile_desc,
+                                                   w.vec_tiles, w.ctl, cs.key, bulk);
     else
-        k_copy_vec<false><<<grid, kThreads, 0, s>>>(pool_r, pool_w, slab_r, slab_w, pool_bytes,
-                                                    slab_bytes, aligned, descs, num_descs, desc_cap,
-                                                    w.tile_desc, w.vec_tiles, w.ctl);
+        k_copy_vec<false><<<grid, kThreads, 0, s>>>(pool_r, pool_w, slab_r, slab_w, pool_bytes, slab_bytes,
+                                                    cs.aligned, descs, num_descs, desc_cap, w.tile_desc,
+                                                    w.vec_tiles, w.ctl, cs.key, bulk);
     KVX_LAUNCHED();
     return KVX_OK;
+}
+
+// mode: 0 = prepare and copy, 1 = prepare only, 2 = copy along prepared lists
+kvx_status launch(bool pack, int mode, const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r,
+                  uint8_t *slab_w, uint64_t pool_bytes, uint64_t slab_bytes, const kvx_desc *descs,
+                  const uint64_t *num_descs, uint64_t desc_cap, uint32_t *status, void *ws,
+                  size_t ws_bytes, void *stream) {
+    const void *pool = pool_r ? (const void *)pool_r : (const void *)pool_w;
+    const void *slab = slab_r ? (const void *)slab_r : (const void *)slab_w;
+    CopySetup cs;
+    kvx_status st = setup(pool, pool_bytes, slab, slab_bytes, descs, num_descs, desc_cap, status, ws, ws_bytes,
+                          &cs);
+    if (st != KVX_OK) return st;
+    cudaStream_t s = as_stream(stream);
+    if (mode != 2) {
+        st = launch_prep(cs, pool_bytes, slab_bytes, descs, num_descs, desc_cap, status, s);
+        if (st != KVX_OK || mode == 1) return st;
+    }
+    return launch_copy(pack, cs, pool_r, pool_w, slab_r, slab_w, pool_bytes, slab_bytes, descs, num_descs,
+                       desc_cap, status, s);
 }
 
 }  // namespace
@@ -592,7 +672,7 @@ extern "C" kvx_status kvx_pack(const uint8_t *pool, uint64_t pool_bytes, const k
                                const uint64_t *num_descs, uint64_t desc_capacity, uint8_t *slab,
                                uint64_t slab_bytes, uint32_t *status, void *ws, size_t ws_bytes,
                                void *stream) {
-    return launch(true, pool, nullptr, nullptr, slab, pool_bytes, slab_bytes, descs, num_descs,
+    return launch(true, 0, pool, nullptr, nullptr, slab, pool_bytes, slab_bytes, descs, num_descs,
                   desc_capacity, status, ws, ws_bytes, stream);
 }
 
@@ -600,8 +680,33 @@ extern "C" kvx_status kvx_unpack(const uint8_t *slab, uint64_t slab_bytes, const
                                  const uint64_t *num_descs, uint64_t desc_capacity,
                                  uint8_t *dst_pool, uint64_t pool_bytes, uint32_t *status,
                                  void *ws, size_t ws_bytes, void *stream) {
-    return launch(false, nullptr, dst_pool, slab, nullptr, pool_bytes, slab_bytes, descs,
+    return launch(false, 0, nullptr, dst_pool, slab, nullptr, pool_bytes, slab_bytes, descs,
                   num_descs, desc_capacity, status, ws, ws_bytes, stream);
+}
+
+extern "C" kvx_status kvx_copy_prepare(const void *pool, uint64_t pool_bytes, const kvx_desc *descs,
+                                       const uint64_t *num_descs, uint64_t desc_capacity, const void *slab,
+                                       uint64_t slab_bytes, uint32_t *status, void *ws, size_t ws_bytes,
+                                       void *stream) {
+    return launch(true, 1, static_cast<const uint8_t *>(pool), nullptr, static_cast<const uint8_t *>(slab),
+                  nullptr, pool_bytes, slab_bytes, descs, num_descs, desc_capacity, status, ws, ws_bytes,
+                  stream);
+}
+
+extern "C" kvx_status kvx_pack_prepared(const uint8_t *pool, uint64_t pool_bytes, const kvx_desc *descs,
+                                        const uint64_t *num_descs, uint64_t desc_capacity, uint8_t *slab,
+                                        uint64_t slab_bytes, uint32_t *status, void *ws, size_t ws_bytes,
+                                        void *stream) {
+    return launch(true, 2, pool, nullptr, nullptr, slab, pool_bytes, slab_bytes, descs, num_descs,
+                  desc_capacity, status, ws, ws_bytes, stream);
+}
+
+extern "C" kvx_status kvx_unpack_prepared(const uint8_t *slab, uint64_t slab_bytes, const kvx_desc *descs,
+                                          const uint64_t *num_descs, uint64_t desc_capacity,
+                                          uint8_t *dst_pool, uint64_t pool_bytes, uint32_t *status,
+                                          void *ws, size_t ws_bytes, void *stream) {
+    return launch(false, 2, nullptr, dst_pool, slab, nullptr, pool_bytes, slab_bytes, descs, num_descs,
+                  desc_capacity, status, ws, ws_bytes, stream);
 }
 
 // ------------------------------------------------------------ no-allocation pack
@@ -643,13 +748,14 @@ extern "C" kvx_status kvx_pack_noalloc(const uint8_t *pool, uint64_t pool_bytes,
                                        const kvx_desc *descs, const uint64_t *num_descs,
                                        uint64_t desc_capacity, uint8_t *slab, uint64_t slab_bytes,
                                        uint32_t *status, void *stream) {
-    // the scratch holds the tile lists (not the piece list: shared tiles take
-    // the register path here)
+    // the scratch always holds the tile lists, and the piece list too while it
+    // fits (slabs up to about 5000 tiles); beyond that, shared tiles take the
+    // register path
     size_t full = 0, base = 0;
     carve(nullptr, slab_bytes, &full, &base);
     if (base > kNoallocScratchBytes) return KVX_ECAPACITY;
     void *scratch = pack_scratch_address();
     if (!scratch) return KVX_ECUDA;
-    return launch(true, pool, nullptr, nullptr, slab, pool_bytes, slab_bytes, descs, num_descs,
+    return launch(true, 0, pool, nullptr, nullptr, slab, pool_bytes, slab_bytes, descs, num_descs,
                   desc_capacity, status, scratch, kNoallocScratchBytes, stream);
 }

@@ -53,6 +53,9 @@ _SIGS = {
     "kvx_pack": (ctypes.c_int, [_P, _U64, _P, _P, _U64, _P, _U64, _P, _P, _SZ, _P]),
     "kvx_unpack": (ctypes.c_int, [_P, _U64, _P, _P, _U64, _P, _U64, _P, _P, _SZ, _P]),
     "kvx_pack_noalloc": (ctypes.c_int, [_P, _U64, _P, _P, _U64, _P, _U64, _P, _P]),
+    "kvx_copy_prepare": (ctypes.c_int, [_P, _U64, _P, _P, _U64, _P, _U64, _P, _P, _SZ, _P]),
+    "kvx_pack_prepared": (ctypes.c_int, [_P, _U64, _P, _P, _U64, _P, _U64, _P, _P, _SZ, _P]),
+    "kvx_unpack_prepared": (ctypes.c_int, [_P, _U64, _P, _P, _U64, _P, _U64, _P, _P, _SZ, _P]),
     "kvx_verify_encode": (ctypes.c_int, [_P, _P, _P, _U32, _U32, _P, _P, _P, _P, _P, _U64, _P, _P,
                                          _P, _SZ, _P]),
     "kvx_segcopy_workspace_size": (_SZ, []),
@@ -176,6 +179,27 @@ def kvx_unpack(slab, slab_bytes, descs, num_descs, desc_capacity, dst_pool, pool
                             _stream(stream)), "kvx_unpack")
 
 
+def kvx_copy_prepare(pool, pool_bytes, descs, num_descs, desc_capacity, slab, slab_bytes, status, ws,
+                     stream=None):
+    _check(lib().kvx_copy_prepare(_ptr(pool), pool_bytes, _ptr(descs), _ptr(num_descs), desc_capacity,
+                                  _ptr(slab), slab_bytes, _ptr(status), _ptr(ws), ws.numel(),
+                                  _stream(stream)), "kvx_copy_prepare")
+
+
+def kvx_pack_prepared(pool, pool_bytes, descs, num_descs, desc_capacity, slab, slab_bytes, status, ws,
+                      stream=None):
+    _check(lib().kvx_pack_prepared(_ptr(pool), pool_bytes, _ptr(descs), _ptr(num_descs), desc_capacity,
+                                   _ptr(slab), slab_bytes, _ptr(status), _ptr(ws), ws.numel(),
+                                   _stream(stream)), "kvx_pack_prepared")
+
+
+def kvx_unpack_prepared(slab, slab_bytes, descs, num_descs, desc_capacity, dst_pool, pool_bytes, status,
+                        ws, stream=None):
+    _check(lib().kvx_unpack_prepared(_ptr(slab), slab_bytes, _ptr(descs), _ptr(num_descs), desc_capacity,
+                                     _ptr(dst_pool), pool_bytes, _ptr(status), _ptr(ws), ws.numel(),
+                                     _stream(stream)), "kvx_unpack_prepared")
+
+
 def kvx_pack_noalloc(pool, pool_bytes, descs, num_descs, desc_capacity, slab, slab_bytes, status,
                      stream=None):
     """kvx_pack with the library's own static scratch (no workspace argument)."""
@@ -284,6 +308,7 @@ class Transfer:
         self.plan_ws = torch.empty(kvx_plan_workspace_size(L, self.run_cap, self.pool_bytes),
                                    dtype=u8, device=dev)
         self.copy_ws = torch.empty(kvx_copy_workspace_size(self.slab_bytes), dtype=u8, device=dev)
+        self.unpack_ws = torch.empty_like(self.copy_ws)  # an unpack prepared while a pack runs
         self.seg_ws = torch.empty(kvx_segcopy_workspace_size(), dtype=u8, device=dev)
 
     # -- the five calls ------------------------------------------------
@@ -324,6 +349,24 @@ class Transfer:
     def unpack(self, slab, dst_pool, stream=None):
         kvx_unpack(slab, slab.numel(), self.descs, self.counts[1:], self.desc_cap, dst_pool,
                    dst_pool.numel(), self.status, self.copy_ws, stream)
+
+    def prepare_pack(self, pool, slab, stream=None):
+        """Checks and tile lists of the next pack (kvx_copy_prepare)."""
+        kvx_copy_prepare(pool, pool.numel(), self.descs, self.counts[1:], self.desc_cap, slab,
+                         slab.numel(), self.status, self.copy_ws, stream)
+
+    def prepare_unpack(self, slab, dst_pool, stream=None):
+        """Checks and tile lists of the next unpack, in their own workspace."""
+        kvx_copy_prepare(dst_pool, dst_pool.numel(), self.descs, self.counts[1:], self.desc_cap, slab,
+                         slab.numel(), self.status, self.unpack_ws, stream)
+
+    def pack_prepared(self, pool, slab, stream=None):
+        kvx_pack_prepared(pool, pool.numel(), self.descs, self.counts[1:], self.desc_cap, slab,
+                          slab.numel(), self.status, self.copy_ws, stream)
+
+    def unpack_prepared(self, slab, dst_pool, stream=None):
+        kvx_unpack_prepared(slab, slab.numel(), self.descs, self.counts[1:], self.desc_cap, dst_pool,
+                            dst_pool.numel(), self.status, self.unpack_ws, stream)
 
     def seal(self, slab, dst_addr, dst, stream=None, bulk=None):
         """Install every segment from the slab at dst[dst_addr[b][l]] (seal
@@ -397,10 +440,11 @@ def overlapped_steps(transfers, pool, slab, dst_pool, n, main, ctl, side):
     """n passes of the whole path over a stream of transfers, taking the
     Transfer objects in turn (at least two, each with its own metadata and
     the same table): the control path of a pass (encode, plan) runs on the
-    ctl stream while the previous pass copies on main, rebuild runs on side
-    next to pack, and a Transfer's next encode waits until its previous
-    pass's copies are done (they read its plan).  Every pass does all five
-    calls; only independent passes overlap."""
+    ctl stream while the previous pass copies on main; rebuild and the two
+    copies' preparations (checks and tile lists) run on side; main only moves
+    bytes.  A Transfer's next encode waits until its previous pass's copies
+    are done (they read its plan and its tile lists).  Every pass does all
+    five calls; only independent passes overlap."""
     k = len(transfers)
     assert k >= 2
     copied = [None] * k
@@ -417,15 +461,19 @@ def overlapped_steps(transfers, pool, slab, dst_pool, n, main, ctl, side):
         planned = torch.cuda.Event()
         planned.record(ctl)
         side.wait_event(planned)
+        tr.prepare_pack(pool, slab, stream=side)
+        tr.prepare_unpack(slab, dst_pool, stream=side)
+        prepared = torch.cuda.Event()
+        prepared.record(side)
         tr.rebuild(stream=side)
         rebuilt = torch.cuda.Event()
         rebuilt.record(side)
-        main.wait_event(planned)
-        tr.pack(pool, slab, stream=main)
-        tr.unpack(slab, dst_pool, stream=main)
+        main.wait_event(prepared)
+        tr.pack_prepared(pool, slab, stream=main)
+        tr.unpack_prepared(slab, dst_pool, stream=main)
         main.wait_event(rebuilt)
         done = torch.cuda.Event()
         done.record(main)
         copied[i % k] = done
-    # the last pass's plan and rebuild were joined into main above, so every
-    # operation on ctl and side is ordered before main's end
+    # the last pass's preparations and rebuild were joined into main above, so
+    # every operation on ctl and side is ordered before main's end

@@ -112,6 +112,17 @@ def test_copies_reject_small_workspaces():
     assert ws > 0
 
 
+def test_prepared_copies_reject_bad_arguments():
+    L = _lib()
+    slab = 1 << 30
+    ws = int(L.kvx_copy_workspace_size(slab))
+    for fn in (L.kvx_copy_prepare, L.kvx_pack_prepared, L.kvx_unpack_prepared):
+        assert fn(P, 1 << 31, P, P, 10, P, slab, P, P, 64, None) == EINVAL      # workspace too small
+        assert fn(P, 1 << 31, P, P, 10, P, slab, None, P, ws, None) == EINVAL   # no status word
+        assert fn(P, 1 << 31, None, P, 10, P, slab, P, P, ws, None) == EINVAL   # no descriptors
+        assert fn(None, 1 << 31, P, P, 10, P, slab, P, P, ws, None) == EINVAL   # pool bytes, no pool
+
+
 def test_noalloc_pack_rejects_slabs_beyond_its_scratch():
     L = _lib()
     assert L.kvx_pack_noalloc(P, 1 << 40, P, P, 10, P, 1 << 34, P, None) == ECAPACITY

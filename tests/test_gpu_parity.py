@@ -393,6 +393,93 @@ def test_copy_paths_descriptor_mix(mix):
     assert np.array_equal(dst.cpu().numpy(), want_pool)
 
 
+@pytest.mark.parametrize("mix", ["ring_4k", "ring_2k_6k", "short_mixed", "unaligned", "with_bad"])
+def test_prepared_copies_match_oracle(mix):
+    """The two-stage copies: kvx_copy_prepare, then kvx_pack_prepared and
+    kvx_unpack_prepared (each along its own preparation), bit-exact against
+    the oracle on every copy path; status bits as kvx_pack / kvx_unpack."""
+    rng = np.random.default_rng(sum(map(ord, mix)) + 1)
+    lens = {"ring_4k": [4096] * 700 + [1 << 20] * 3 + [4096] * 33,
+            "ring_2k_6k": list(rng.choice([2048, 6144, 10240], size=900)),
+            "short_mixed": list(rng.choice([1024, 4096, 512, 8192], size=900)),
+            "unaligned": list(rng.choice([4096, 4100, 2056], size=700)),
+            "with_bad": [4096] * 600}[mix]
+    bad = {5, 77, 301} if mix == "with_bad" else set()
+    d, slab_bytes, pool_bytes = _desc_list(rng, [int(x) for x in lens], bad)
+    host_pool = rng.integers(0, 256, pool_bytes, dtype=np.uint8)
+    want_slab = np.zeros(slab_bytes, np.uint8)
+    st_p = oracle.pack(host_pool, d, want_slab)
+    want_pool = np.full(pool_bytes, 0xA5, np.uint8)
+    st_u = oracle.unpack(want_slab, d, want_pool)
+    dd = torch.from_numpy(d.view(np.uint8).copy()).cuda()
+    nd = torch.tensor([len(d), 0, 0], dtype=torch.int64, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    wsb = kvx.kvx_copy_workspace_size(slab_bytes)
+    ws_p = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    ws_u = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    pool = torch.from_numpy(host_pool).cuda()
+    slab = torch.zeros(slab_bytes, dtype=torch.uint8, device="cuda")
+    dst = torch.full((pool_bytes,), 0xA5, dtype=torch.uint8, device="cuda")
+    # both preparations first, then both copies
+    kvx.kvx_copy_prepare(pool, pool_bytes, dd, nd, len(d), slab, slab_bytes, st, ws_p)
+    kvx.kvx_copy_prepare(dst, pool_bytes, dd, nd, len(d), slab, slab_bytes, st, ws_u)
+    torch.cuda.synchronize()
+    assert int(st.item()) == st_p == st_u  # the checks are the same in both directions
+    kvx.kvx_pack_prepared(pool, pool_bytes, dd, nd, len(d), slab, slab_bytes, st, ws_p)
+    kvx.kvx_unpack_prepared(slab, slab_bytes, dd, nd, len(d), dst, pool_bytes, st, ws_u)
+    torch.cuda.synchronize()
+    assert int(st.item()) == st_p
+    assert np.array_equal(slab.cpu().numpy(), want_slab)
+    assert np.array_equal(dst.cpu().numpy(), want_pool)
+
+
+def test_prepared_copy_misuse_moves_nothing():
+    """Lists serve the one copy they were made for: a second copy along the
+    same preparation, a copy along a workspace prepared for other
+    descriptors, and one along a workspace never prepared (cleared) each
+    move no byte and raise KVX_S_DESC; kvx_pack after all that is intact."""
+    rng = np.random.default_rng(11)
+    d, slab_bytes, pool_bytes = _desc_list(rng, [4096] * 300 + [65536] * 20 + [2048] * 100)
+    host_pool = rng.integers(0, 256, pool_bytes, dtype=np.uint8)
+    want = np.zeros(slab_bytes, np.uint8)
+    assert oracle.pack(host_pool, d, want) == 0
+    dd = torch.from_numpy(d.view(np.uint8).copy()).cuda()
+    dd2 = dd.clone()
+    nd = torch.tensor([len(d), 0, 0], dtype=torch.int64, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(kvx.kvx_copy_workspace_size(slab_bytes), dtype=torch.uint8, device="cuda")
+    pool = torch.from_numpy(host_pool).cuda()
+    slab = torch.zeros(slab_bytes, dtype=torch.uint8, device="cuda")
+
+    kvx.kvx_copy_prepare(pool, pool_bytes, dd, nd, len(d), slab, slab_bytes, st, ws)
+    kvx.kvx_pack_prepared(pool, pool_bytes, dd, nd, len(d), slab, slab_bytes, st, ws)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and np.array_equal(slab.cpu().numpy(), want)
+    # second use of the same lists
+    slab.zero_()
+    kvx.kvx_pack_prepared(pool, pool_bytes, dd, nd, len(d), slab, slab_bytes, st, ws)
+    torch.cuda.synchronize()
+    assert int(st.item()) == kvx.S_DESC and not slab.any().item()
+    # lists made for another descriptor array
+    st.zero_()
+    kvx.kvx_copy_prepare(pool, pool_bytes, dd2, nd, len(d), slab, slab_bytes, st, ws)
+    kvx.kvx_pack_prepared(pool, pool_bytes, dd, nd, len(d), slab, slab_bytes, st, ws)
+    torch.cuda.synchronize()
+    assert int(st.item()) == kvx.S_DESC and not slab.any().item()
+    # a workspace that was never prepared
+    st.zero_()
+    ws.zero_()
+    kvx.kvx_unpack_prepared(slab, slab_bytes, dd, nd, len(d), pool, pool_bytes, st, ws)
+    torch.cuda.synchronize()
+    assert int(st.item()) == kvx.S_DESC
+    assert np.array_equal(pool.cpu().numpy(), host_pool)
+    # the fused call is unaffected
+    st.zero_()
+    kvx.kvx_pack(pool, pool_bytes, dd, nd, len(d), slab, slab_bytes, st, ws)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and np.array_equal(slab.cpu().numpy(), want)
+
+
 # ------------------------------------------------------------ full sizes
 
 FULL = ["tiny", "default", "worst", "mixed", "many_small", "wide64k"]
