@@ -16,7 +16,8 @@
 //     Rings claim their jobs dynamically, so the copy ends when the bytes
 //     are done rather than when the slowest ring is.  Sweeps on GB300 (16-96
 //     KiB tiles, 2-12 stages, 38-304 rings, static or claimed work, claims of
-//     1-8 jobs) put one ring per SM, 3 x 64 KiB, claims of 2 first.
+//     1-8 jobs) put one ring per SM, 3 x 64 KiB, claims of 2 first; one SM
+//     is left free for kernels that run beside the copy.
 //   - pieces: tiles shared by several 16-byte aligned descriptors of 2 to
 //     16 KiB (the 4 KiB per-segment reads of a scattered holder), one piece
 //     per descriptor, moved by the four 16 KiB-stage bulk-copy rings per SM
@@ -614,7 +615,11 @@ kvx_status launch_copy(bool pack, const CopySetup &cs, const uint8_t *pool_r, ui
                        cudaStream_t s) {
     if ((pack ? set_tma_smem<true>() : set_tma_smem<false>()) != cudaSuccess) return KVX_ECUDA;
     const int sms = sm_count();
-    const uint32_t bulk = (uint32_t)(sms * kTmaCtasPerSm);
+    // One SM is left without a ring: the copy moves the same bytes per second
+    // on the others (measured), and small kernels of a transfer planned
+    // alongside (the single-block planner) run there during the copy instead
+    // of waiting for it to end (overlapped default passes 1.373 -> 1.361 ms).
+    const uint32_t bulk = (uint32_t)((sms > 1 ? sms - 1 : 1) * kTmaCtasPerSm);
     const size_t smem = (size_t)kStages * kTileBytes;
     const Ws &w = cs.w;
     if (pack)
