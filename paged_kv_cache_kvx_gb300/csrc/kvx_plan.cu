@@ -480,9 +480,8 @@ __device__ uint32_t active_digits(const PlanArgs &a, uint64_t R, uint32_t *act) 
 
 // Step 2: first block of each run, coverage, sort items, first histogram.
 __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, uint32_t nact,
-                           uint32_t dig0, ScanSmem &sm, const uint32_t *s_lf) {
+                           uint32_t dig0, ScanSmem &sm, const uint32_t *s_lf, uint32_t *s_hist) {
     const bool lf_smem = a.table_lanes + 1 <= kLaneSmem;
-    __shared__ uint32_t s_hist[kDigits];
     __shared__ uint32_t s_bits;
     if (threadIdx.x == 0) s_bits = 0;
     __syncthreads();
@@ -568,15 +567,22 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
 // scatter, and the next digit's histogram per output tile (atomics into Hn,
 // cleared one pass earlier).  Hz is cleared here for the pass after next.
 constexpr uint32_t kOwnChunk = 8;  // own tiles whose offsets are held at once
+
+// Per-block counters of a radix pass.
+struct SortCounters {
+    uint32_t wcnt[kT / 32][kDigits];  // per warp and digit
+    uint32_t s_off[kOwnChunk][kDigits];
+    uint32_t s_base[kDigits];
+};
 constexpr int kSweep = 32;         // histogram rows loaded at once in the offset sweep
 
 __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P,
                                 const SortItem *in, SortItem *out, const uint32_t *H,
                                 uint32_t *Hn, uint32_t *Hz, uint32_t dig, bool has_next,
-                                uint32_t ndig, bool clear_z) {
-    __shared__ uint32_t wcnt[kT / 32][kDigits];
-    __shared__ uint32_t s_off[kOwnChunk][kDigits];
-    __shared__ uint32_t s_base[kDigits];
+                                uint32_t ndig, bool clear_z, SortCounters &sc) {
+    uint32_t (*wcnt)[kDigits] = sc.wcnt;
+    uint32_t (*s_off)[kDigits] = sc.s_off;
+    uint32_t *s_base = sc.s_base;
     __shared__ uint64_t sh[33];
     static_assert(kT == kDigits, "one thread per digit");
     if (clear_z) {
@@ -1471,11 +1477,26 @@ __global__ void __launch_bounds__(kST, 1) k_plan_small(const __grid_constant__ P
     }
 }
 
+// Shared memory that two stages use in turn: lane_first and the first
+// histogram while the runs are decoded and keyed, then a radix pass's
+// counters.  Sharing it keeps the block at about 22 KB, small enough to sit
+// beside a bulk-copy block on one SM (a transfer can be planned while another
+// copies).
+struct KeyStage {
+    uint32_t lf[kLaneSmem];
+    uint32_t hist[kDigits];
+};
+union PlanStages {
+    KeyStage keys;
+    SortCounters sort;
+};
+
 __global__ void __launch_bounds__(kT, 2) k_plan(const __grid_constant__ PlanArgs a) {
     __shared__ ScanSmem sm;
     __shared__ uint32_t s_act[13];
     __shared__ uint32_t s_nact;
-    __shared__ uint32_t s_lf[kLaneSmem];
+    __shared__ PlanStages st;
+    uint32_t *s_lf = st.keys.lf;
     const uint64_t R_in = *a.num_runs;
     if (plan_is_small(a, R_in)) return;  // planned by k_plan_small
     const uint64_t R = R_in <= a.run_cap ? R_in : 0;
@@ -1492,7 +1513,7 @@ __global__ void __launch_bounds__(kT, 2) k_plan(const __grid_constant__ PlanArgs
     if (threadIdx.x == 0) s_nact = active_digits(a, R, s_act);
     __syncthreads();
     const uint32_t nact = s_nact;
-    phase_keys(a, R, nt, P, nact, nact ? s_act[0] : 0, sm, s_lf);
+    phase_keys(a, R, nt, P, nact, nact ? s_act[0] : 0, sm, s_lf, st.keys.hist);
     PLAN_BARRIER();
     if (__ldcg(&a.ctl->st) != 0) return;  // counts stay 0
 
@@ -1502,7 +1523,7 @@ __global__ void __launch_bounds__(kT, 2) k_plan(const __grid_constant__ PlanArgs
         const bool has_next = k + 1 < nact;
         phase_sort_pass(a, R, nt, P, in, out, a.hist[k % 3], a.hist[(k + 1) % 3],
                         a.hist[(k + 2) % 3], s_act[k], has_next, has_next ? s_act[k + 1] : 0,
-                        k + 2 < nact);
+                        k + 2 < nact, st.sort);
         PLAN_BARRIER();
     }
     const SortItem *sorted = (nact & 1) ? a.items1 : a.items0;
