@@ -1598,19 +1598,13 @@ Ws carve(void *base, uint64_t run_cap, size_t *bytes) {
     return w;
 }
 
-// Blocks of k_plan that can be resident at once (cooperative launch limit).
-int plan_max_blocks() {
-    static int cached[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_plan, kT, 0) != cudaSuccess || per_sm < 1)
-        per_sm = 1;
-    const int n = per_sm * sm_count();
-    if (dev >= 0 && dev < 64) cached[dev] = n;
-    return n;
-}
+// Blocks of k_plan that can be resident at once (cooperative launch limit),
+// at most one per SM: then the whole grid also fits beside a bulk copy (one
+// planner block fits next to a copy block), so a transfer is planned while
+// another copies.  Tables of more than one 2048-run tile per SM give a block
+// several tiles (many_small: 284 tiles, 2 per block; planned alone 236 -> 269
+// us, but overlapped passes 2.257 -> 2.175 ms).
+int plan_max_blocks() { return sm_count(); }
 
 }  // namespace
 }  // namespace kvx
