@@ -383,8 +383,9 @@ class Transfer:
 
     def step(self, pool, slab, dst_pool, stream=None, side=None):
         """One pass of the whole path: encode, plan, rebuild, pack, unpack.
-        With a side stream, rebuild (which needs only the plan) runs there
-        alongside pack and joins before the step ends."""
+        With a side stream, the unpack's preparation and the rebuild (which
+        need only the plan) run there alongside pack and join before the
+        unpack and the end of the step."""
         main = torch.cuda.current_stream(self.device) if stream is None else stream
         self.encode(stream=main)
         self.plan(stream=main)
@@ -396,11 +397,15 @@ class Transfer:
         planned = torch.cuda.Event()
         planned.record(main)
         side.wait_event(planned)
+        self.prepare_unpack(slab, dst_pool, stream=side)
+        prepared = torch.cuda.Event()
+        prepared.record(side)
         self.rebuild(stream=side)
         rebuilt = torch.cuda.Event()
         rebuilt.record(side)
         self.pack(pool, slab, stream=main)
-        self.unpack(slab, dst_pool, stream=main)
+        main.wait_event(prepared)
+        self.unpack_prepared(slab, dst_pool, stream=main)
         main.wait_event(rebuilt)
 
     def set_addr(self, addr_np: np.ndarray):
