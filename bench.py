@@ -105,6 +105,30 @@ def copy_kernel_hash(src=COPY_SRC):
     return h.hexdigest()[:16]
 
 
+def stage_roofline(med_ms, S, R, G, D, L, N, peak):
+    """Every stage of one pass against the HBM roofline: its algorithmic bytes
+    (what the step must read and write at least), those bytes over the
+    stage's median time, and that rate as a fraction of the measured peak.
+    encode: the address table read (8 B per segment), the run table written
+    (20 B per run, 4 B per lane); plan: the run table read, lane_first,
+    run_block / run_group / run_off (16 B per run), groups (48 B) and reads
+    (32 B) written; rebuild: a pointer per segment written (8 B), the per-run
+    records and groups read; pack, unpack: N read and N written."""
+    nbytes = {
+        "encode": 8 * S + 20 * R + 4 * L,
+        "plan": 20 * R + 4 * L + 4 * (L + 1) + 16 * R + 48 * G + 32 * D + 24,
+        "rebuild": 8 * S + 16 * R + 48 * G + 4 * (L + 1),
+        "pack": 2 * N,
+        "unpack": 2 * N,
+    }
+    out = {}
+    for i, name in enumerate(["encode", "plan", "rebuild", "pack", "unpack"]):
+        gbs = nbytes[name] / (float(med_ms[i]) / 1e3) / 1e9
+        out[name] = {"algorithmic_bytes": int(nbytes[name]), "gbs": gbs, "frac": gbs / peak,
+                     "bound": "hbm" if name in ("pack", "unpack") else "latency"}
+    return out
+
+
 def profiled_traffic(profile=PROFILE, src=COPY_SRC):
     """DRAM bytes per launch from a committed ncu summary, only while the
     kernel's source is the one that was profiled."""
@@ -427,6 +451,7 @@ def run_kvx(args):
         "encode_msegs_per_s": S / (mean[0] / 1e3) / 1e6,
         "stage_ms_mean": dict(zip(["encode", "plan", "rebuild", "pack", "unpack"], map(float, mean))),
         "stage_ms_median": dict(zip(["encode", "plan", "rebuild", "pack", "unpack"], map(float, med))),
+        "stage_roofline": stage_roofline(med, S, nruns, ngroups, ndescs, wl.lanes, N, peak),
         "memcpy_d2d_gbs": memcpy_gbs,
         "e2e": e2e,
         "gpu_launches": int(launches),
