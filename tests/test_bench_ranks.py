@@ -47,3 +47,17 @@ def test_single_process_is_identity_and_value_scales_with_ranks():
     one = bench.step_value(2_359_296_000, 10, 1, 15.0)
     assert one == pytest.approx(4 * 2_359_296_000 * 10 / 0.015 / 1e9)
     assert bench.step_value(2_359_296_000, 10, 4, 15.0) == pytest.approx(4 * one)
+
+
+def test_stage_roofline_bytes_and_fractions():
+    """The per-stage roofline of the bench line: algorithmic bytes from the
+    table's counts, the rate over the stage time, its fraction of the peak."""
+    S, R, G, D, L, N = 576000, 576, 2, 72, 576, 576000 * 4096
+    ms = [0.020, 0.020, 0.010, 0.700, 0.700]
+    r = bench.stage_roofline(ms, S, R, G, D, L, N, 7000.0)
+    assert r["encode"]["algorithmic_bytes"] == 8 * S + 20 * R + 4 * L
+    assert r["rebuild"]["algorithmic_bytes"] == 8 * S + 16 * R + 48 * G + 4 * (L + 1)
+    assert r["pack"]["algorithmic_bytes"] == r["unpack"]["algorithmic_bytes"] == 2 * N
+    assert r["pack"]["gbs"] == pytest.approx(2 * N / 0.7e-3 / 1e9)
+    assert r["pack"]["frac"] == pytest.approx(r["pack"]["gbs"] / 7000.0)
+    assert r["pack"]["bound"] == "hbm" and r["plan"]["bound"] == "latency"
