@@ -495,6 +495,38 @@ def _used_positions(wl):
     return out
 
 
+@pytest.mark.parametrize("name", ["worst", "many_small", "mixed"])
+def test_full_size_prepared_copies(name):
+    """At full size, the two-stage copies (both preparations first, as the
+    overlapped passes do) give the same slab and destination bytes as the
+    one-call copies, and both equal the holder's bytes where segments lie."""
+    wl = W.CONFIGS[name]()
+    tr = gpu_plan(wl.addr, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
+    assert tr.read_status() == 0
+    pool = torch.empty(wl.pool_bytes, dtype=torch.uint8, device="cuda")
+    W.fill_pool_torch(pool, wl.seed)
+    slab = torch.empty(tr.slab_bytes, dtype=torch.uint8, device="cuda")
+    tr.pack(pool, slab)
+    slab2 = torch.zeros_like(slab)
+    dst2 = torch.full((wl.pool_bytes,), W.CANARY, dtype=torch.uint8, device="cuda")
+    tr.prepare_pack(pool, slab2)
+    tr.prepare_unpack(slab2, dst2)
+    tr.pack_prepared(pool, slab2)
+    tr.unpack_prepared(slab2, dst2)
+    torch.cuda.synchronize()
+    assert tr.read_status() == 0
+    assert torch.equal(slab, slab2)
+    del slab, slab2
+    for base, chunk, used in _used_positions(wl):
+        n = used.size * chunk
+        a = pool[base:base + n].view(used.size, chunk)
+        d = dst2[base:base + n].view(used.size, chunk)
+        u = torch.from_numpy(used).cuda()
+        assert torch.equal(a[u], d[u])
+        if (~used).any():
+            assert bool((d[~u] == W.CANARY).all())
+
+
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_config(name):
     wl = W.CONFIGS[name]()
