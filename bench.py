@@ -210,21 +210,42 @@ def oracle_sample_step(wl, host_pool):
     return dt
 
 
-def oracle_baseline(target_s: float, max_blocks: int = 100):
-    """Oracle on the first `blocks` blocks of the default workload, repeated
-    for about target_s seconds.  Returns (GB/s, description, steps)."""
+def oracle_sample_workload(name: str):
+    """A bounded sample of a workload for the CPU oracle: the same generator
+    with fewer blocks (the table's per-block structure, slot template and
+    address pattern kept).  Returns (workload, full-size block count)."""
     from paged_kv_cache_kvx_gb300 import workloads as W
-    blocks = max_blocks
-    wl = W.bump("default_sample", blocks=blocks, slots=288, seg=4096, seed=2)
+    if name == "default":
+        return W.bump("default_sample", blocks=100, slots=288, seg=4096, seed=2), 1000
+    if name == "tiny":
+        return W.tiny(), 8
+    if name == "worst":
+        return W.worst(blocks=100, npos=248), 1000
+    if name == "mixed":
+        return W.mixed(blocks=256), 4096
+    if name == "many_small":
+        return W.many_small(blocks=5000, nreloc=250), 100_000
+    if name == "wide64k":
+        return W.bump("wide64k_sample", blocks=10, slots=288, seg=64 * 1024, nregions=2, seed=6), 200
+    if name == "konly":
+        return W.k_only("bump", name="default_sample", blocks=100), 1000
+    raise ValueError(name)
+
+
+def oracle_baseline(target_s: float, workload: str = "default"):
+    """The oracle on a bounded sample of the workload, repeated for about
+    target_s seconds.  Returns (GB/s, description, steps, seconds per pass)."""
+    from paged_kv_cache_kvx_gb300 import workloads as W
+    wl, full_blocks = oracle_sample_workload(workload)
     pool = W.holder_pool_np(wl)
     first = oracle_sample_step(wl, pool)
     n = max(1, int(target_s / max(first, 1e-6)))
     times = [oracle_sample_step(wl, pool) for _ in range(n)]
     per = statistics.median(times)
     gbs = 4 * wl.payload_bytes / per / 1e9
-    desc = ("oracle encode+plan+rebuild+pack+unpack on the first %d of 1000 blocks of the default "
-            "workload (%d segments, %.0f MiB), median of %d passes, single thread"
-            % (blocks, wl.segments, wl.payload_bytes / 2**20, n))
+    desc = ("oracle encode+plan+rebuild+pack+unpack on %d of the %d blocks of the %s workload's "
+            "generator (%d segments, %.0f MiB), median of %d passes, single thread"
+            % (wl.blocks, full_blocks, workload, wl.segments, wl.payload_bytes / 2**20, n))
     return gbs, desc, n, per
 
 
@@ -320,6 +341,9 @@ def run_kvx(args):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     build.build()
+    # the oracle leg runs on every workload's own sample unless --no-aux was
+    # given or the table is a reduced one for profiler captures
+    oracle_leg = not args.no_aux and args.blocks == 1000
     if args.workload == "konly":
         wl = W.k_only("bump", name="default")
         args.no_aux = True
@@ -328,7 +352,7 @@ def run_kvx(args):
         args.no_aux = True
     elif args.workload != "default":
         wl = W.CONFIGS[args.workload]()
-        args.no_aux = True  # the e2e / CPU legs are defined on the default workload
+        args.no_aux = True  # the e2e leg is defined on the default workload
     elif args.blocks == 1000:
         wl = W.default()
     else:
@@ -466,8 +490,8 @@ def run_kvx(args):
         line["config"]["bytes_moved_per_step"] = 4 * N
     elif args.blocks != 1000:
         line["config"]["workload"] = "reduced for profiling: %d of the default 1000 blocks" % args.blocks
-    if rank == 0 and world == 1 and not args.no_aux:
-        cb, desc, n, per = oracle_baseline(target_s=args.cpu_seconds)
+    if rank == 0 and world == 1 and oracle_leg:
+        cb, desc, n, per = oracle_baseline(target_s=args.cpu_seconds, workload=args.workload)
         line["cpu_baseline"] = {"value": cb, "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "host": host_info(),
                                 "sample": desc}
