@@ -24,11 +24,13 @@
 //     of kvx_ring.cuh.
 //   - vector tiles: the other shared tiles (512 B segment reads, 32 KiB
 //     block reads) and unaligned ones.  256 threads per tile; the tile's
-//     descriptors are staged in shared memory and each 16-byte vector finds
-//     its descriptor by binary search (byte copies when anything is
-//     unaligned).
-// The tile kernels walk their list round-robin over a persistent grid, so
-// the grid streams one window of the slab at a time.
+//     descriptors are staged in shared memory, a table gives each 64-byte
+//     bucket its first descriptor, and each 16-byte vector steps forward
+//     from there (byte copies when anything is unaligned).
+// The vector kernel walks its list round-robin over a persistent grid, so
+// the grid streams one window of the slab at a time.  The copies run in one
+// call (kvx_pack / kvx_unpack) or in two: the checks and lists first
+// (kvx_copy_prepare), the bytes later (kvx_pack_prepared / _unpack_prepared).
 #include <atomic>
 
 #include "kvx_ring.cuh"
@@ -276,7 +278,7 @@ k_copy_prep(const kvx_desc *__restrict__ descs, const uint64_t *__restrict__ num
 
 // ------------------------------------------------------------- TMA path
 
-// One warp per CTA, one CTA per SM; lane 0 drives the ring.  Jobs are handed
+// Warp 0 of each bulk-copy CTA; lane 0 drives the ring.  Jobs are handed
 // out dynamically: a ring claims kGrab consecutive jobs at a time from an
 // atomic counter (the warp loads their records, one per lane) and claims its
 // next batch while it works through the current one, so a ring that happens
@@ -385,7 +387,7 @@ struct PieceGen {
     __device__ uint32_t *status() const { return st; }
 };
 
-// The bulk-copy kernel, one CTA per SM: warp 0 streams the whole-tile jobs
+// The bulk-copy kernel, one CTA per SM but one: warp 0 streams the whole-tile jobs
 // through a ring of 3 x 64 KiB stages; then the same shared memory becomes
 // four rings of 3 x 16 KiB, one per remaining warp, for the pieces of shared
 // tiles.  One launch for both lists: an SM that runs out of tiles moves on
