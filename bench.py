@@ -350,6 +350,9 @@ def run_kvx(args):
     elif args.workload == "worst" and args.blocks != 1000:
         wl = W.worst(blocks=args.blocks, npos=2 * args.blocks + 48)  # reduced for profiler captures
         args.no_aux = True
+    elif args.workload == "many_small" and args.blocks != 1000:
+        wl = W.many_small(blocks=args.blocks, nreloc=args.blocks // 20)  # reduced for profiler captures
+        args.no_aux = True
     elif args.workload != "default":
         wl = W.CONFIGS[args.workload]()
         args.no_aux = True  # the e2e leg is defined on the default workload
@@ -920,8 +923,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work for the oracle baseline leg of the kvx arm")
     ap.add_argument("--blocks", type=int, default=1000,
-                    help="blocks of the default (or worst) shape (1000; fewer only for profiler "
-                         "captures)")
+                    help="blocks of the default, worst or many_small shape (fewer only for profiler "
+                         "captures; the full table otherwise)")
     ap.add_argument("--workload", default="default",
                     choices=["default", "tiny", "worst", "mixed", "many_small", "wide64k", "konly",
                              "paged", "seal", "verify"],
