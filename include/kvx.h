@@ -259,10 +259,13 @@ kvx_status kvx_plan_groups(const uint32_t *runs_per_lane, uint32_t table_lanes,
  * a dense group gives the page's local = group_local + (remote(b) -
  * group_remote) = G.local + i * G.stride + run_off[r]; a non-dense group
  * gives its dense local mirror, G.local + i * G.chunk + run_off[r].  Each
- * pointer is checked: the group index is below counts[0], b lies in the
- * group's block range, the segment [local, local + seg_len[l]) lies inside
- * block i's chunk of the group carve, and the carve ends within slab_bytes.
- * A failing entry is set to UINT64_MAX and KVX_S_BOUNDS is raised.
+ * pointer is checked: the group index is below counts[0], the run starts at
+ * the group's first block (as every run of a planned group does), b lies in
+ * the group's block range, the segment [local, local + seg_len[l]) lies
+ * inside block i's chunk of the group carve, and the carve ends within
+ * slab_bytes.  A failing entry is set to UINT64_MAX and KVX_S_BOUNDS is
+ * raised.  The runs' own strides are not passed: a dense group's stride
+ * stands for them.
  *
  * Inputs: lane_first [L + 1], run_block, run_group, run_off [run_capacity]
  * and groups as kvx_plan_groups wrote them; counts (device, [0] = groups);
