@@ -124,6 +124,7 @@ struct PlanArgs {
     uint64_t *run_off;
     uint64_t *counts;
     uint32_t *status;
+    uint32_t out16;  // groups and descs start on 16-byte boundaries: records move in 16-byte pieces
     // workspace
     PlanCtl *ctl;
     uint32_t *run_lane;
@@ -291,6 +292,48 @@ __device__ __forceinline__ void raise_plan(const PlanArgs &a, uint32_t bits) {
     if (bits) {
         atomicOr(a.status, bits);
         atomicOr(&a.ctl->st, bits);
+    }
+}
+
+// Group and descriptor records in the caller's arrays: three or two 16-byte
+// pieces when the arrays are 16-byte aligned (fewer, wider stores), else the
+// plain struct copy.
+__device__ __forceinline__ uint4 u4(uint64_t x, uint64_t y) {
+    return make_uint4((uint32_t)x, (uint32_t)(x >> 32), (uint32_t)y, (uint32_t)(y >> 32));
+}
+__device__ __forceinline__ void st_group(const PlanArgs &a, uint64_t gid, const kvx_group &G) {
+    if (a.out16) {
+        uint4 *dst = reinterpret_cast<uint4 *>(a.groups + gid);
+        dst[0] = u4(G.base, (uint64_t)G.stride);
+        dst[1] = u4(G.chunk, G.local);
+        dst[2] = make_uint4(G.block, G.count, G.node, G.dense);
+    } else {
+        a.groups[gid] = G;
+    }
+}
+__device__ __forceinline__ kvx_group ld_group(const PlanArgs &a, uint64_t gid) {
+    if (!a.out16) return ld_cg(a.groups + gid);
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.groups + gid);
+    const uint4 p0 = __ldcg(src), p1 = __ldcg(src + 1), p2 = __ldcg(src + 2);
+    kvx_group G;
+    G.base = (uint64_t)p0.x | (uint64_t)p0.y << 32;
+    G.stride = (int64_t)((uint64_t)p0.z | (uint64_t)p0.w << 32);
+    G.chunk = (uint64_t)p1.x | (uint64_t)p1.y << 32;
+    G.local = (uint64_t)p1.z | (uint64_t)p1.w << 32;
+    G.block = p2.x;
+    G.count = p2.y;
+    G.node = p2.z;
+    G.dense = p2.w;
+    return G;
+}
+__device__ __forceinline__ void st_desc(const PlanArgs &a, uint64_t d, uint64_t remote, uint64_t local,
+                                        uint64_t len, uint32_t gid) {
+    if (a.out16) {
+        uint4 *dst = reinterpret_cast<uint4 *>(a.descs + d);
+        dst[0] = u4(remote, local);
+        dst[1] = make_uint4((uint32_t)len, (uint32_t)(len >> 32), gid, 0u);
+    } else {
+        a.descs[d] = kvx_desc{remote, local, len, gid, 0};
     }
 }
 
@@ -929,7 +972,7 @@ __device__ void phase_groups(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
                 G.count = (uint32_t)g_count;
                 G.node = (uint32_t)g_node;
                 G.dense = group_dense(G.count, G.stride, G.chunk) ? 1u : 0u;
-                a.groups[gid] = G;
+                st_group(a, gid, G);
                 c.bytes += (uint64_t)G.count * G.chunk;
                 c.descs += group_pieces(G);
             }
@@ -965,7 +1008,7 @@ __device__ void phase_emit(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
         for (int j = 0; j < kIPT; j++) {
             if (p0 + j < R && (fl >> j & 1u)) n++;
             gids[j] = (uint32_t)(n - 1);
-            if (p0 + j < R && (fl >> (j + 1) & 1u)) G[j] = ld_cg(a.groups + gids[j]);
+            if (p0 + j < R && (fl >> (j + 1) & 1u)) G[j] = ld_group(a, gids[j]);
         }
         CAgg cur = COp()(carry, cex);
         const uint64_t M = KVX_MAX_READ_BYTES;
@@ -980,13 +1023,13 @@ __device__ void phase_emit(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
             if (g.dense) {
                 const uint64_t total = (uint64_t)g.count * g.chunk;
                 for (uint64_t o = 0; o < total; o += M, d++)
-                    a.descs[d] = kvx_desc{g.base + o, g.local + o, total - o < M ? total - o : M, gid, 0};
+                    st_desc(a, d, g.base + o, g.local + o, total - o < M ? total - o : M, gid);
             } else if (g.chunk > 0) {  // a group of empty runs has no read
                 for (uint64_t i = 0; i < g.count; i++) {
                     const uint64_t rb = g.base + i * (uint64_t)g.stride;
                     const uint64_t lb = g.local + i * g.chunk;
                     for (uint64_t o = 0; o < g.chunk; o += M, d++)
-                        a.descs[d] = kvx_desc{rb + o, lb + o, g.chunk - o < M ? g.chunk - o : M, gid, 0};
+                        st_desc(a, d, rb + o, lb + o, g.chunk - o < M ? g.chunk - o : M, gid);
                 }
             }
             cur.bytes += (uint64_t)g.count * g.chunk;
@@ -1671,6 +1714,7 @@ extern "C" kvx_status kvx_plan_groups(const uint32_t *runs_per_lane, uint32_t ta
     a.run_off = run_off;
     a.counts = counts;
     a.status = status;
+    a.out16 = ((reinterpret_cast<uintptr_t>(groups) | reinterpret_cast<uintptr_t>(descs)) & 15) == 0;
     a.ctl = w.ctl;
     a.run_lane = w.run_lane;
     a.seg = w.seg;
