@@ -133,6 +133,37 @@ def _gpu_plan_table(B, seg_len, numa, pool, rpl, base, stride, count, num_runs=N
     return tr
 
 
+@pytest.mark.parametrize("name", ["worst", "many_small"])
+def test_plan_into_arrays_off_16_byte_boundaries(name):
+    """Group and descriptor arrays that start 8 bytes past a 16-byte boundary
+    (the planner then writes its records field by field instead of in
+    16-byte pieces): the same plan as the oracle's, from the single-block
+    planner (worst: 1116 runs) and the cooperative one (many_small: 4368)."""
+    wl = {v.name: v for v in W.small_variants()}[name]
+    B, L = wl.addr.shape
+    t = oracle.encode_runs(wl.addr)
+    p = oracle.plan(t, B, wl.seg_len, wl.numa, wl.pool_bytes)
+    tr = kvx.Transfer(B, wl.seg_len, wl.numa, wl.pool_bytes)
+    tr.set_addr(wl.addr)
+    tr.encode()
+    gbuf = torch.zeros(tr.groups.numel() + 16, dtype=torch.uint8, device="cuda")
+    dbuf = torch.zeros(tr.descs.numel() + 16, dtype=torch.uint8, device="cuda")
+    g_ptr, d_ptr = gbuf.data_ptr() + 8, dbuf.data_ptr() + 8
+    assert g_ptr % 16 == 8 and d_ptr % 16 == 8
+    kvx.kvx_plan_groups(tr.runs_per_lane, tr.L, tr.run_base, tr.run_stride, tr.run_count, tr.num_runs,
+                        tr.run_cap, tr.B, tr.seg_len, tr.numa, tr.L, tr.pool_bytes, g_ptr, tr.group_cap,
+                        d_ptr, tr.desc_cap, tr.lane_first, tr.run_block, tr.run_group, tr.run_off,
+                        tr.counts, tr.status, tr.plan_ws)
+    torch.cuda.synchronize()
+    assert tr.read_status() == 0
+    ng, nd, slab = tr.read_counts()
+    assert (ng, nd, slab) == (len(p.groups), len(p.descs), p.slab_bytes)
+    got_g = gbuf.cpu().numpy()[8: 8 + ng * oracle.GROUP_DTYPE.itemsize]
+    got_d = dbuf.cpu().numpy()[8: 8 + nd * oracle.DESC_DTYPE.itemsize]
+    assert got_g.tobytes() == p.groups.tobytes()
+    assert got_d.tobytes() == p.descs.tobytes()
+
+
 def _validation_cases_match(B, seg_len0, numa, pool0, t):
     """Corrupt the table one class at a time; the CUDA planner must report
     exactly the oracle's status bits and plan nothing."""
