@@ -108,13 +108,17 @@ __device__ __forceinline__ bool in_range(uint64_t off, uint64_t len, uint64_t si
     return off <= size && len <= size - off;
 }
 
-// The fields of a descriptor the tile lists need, in two loads.
+// The fields of a descriptor the tile lists need: two loads when the array
+// starts on a 16-byte boundary (remote and local together), else three.
 struct DescView {
     uint64_t remote, local, len;
 };
-__device__ __forceinline__ DescView load_desc(const kvx_desc *d) {
-    const ulonglong2 rl = __ldg(reinterpret_cast<const ulonglong2 *>(d));  // remote, local
-    return DescView{rl.x, rl.y, __ldg(&d->len)};
+__device__ __forceinline__ DescView load_desc(const kvx_desc *d, bool d16) {
+    if (d16) {
+        const ulonglong2 rl = __ldg(reinterpret_cast<const ulonglong2 *>(d));  // remote, local
+        return DescView{rl.x, rl.y, __ldg(&d->len)};
+    }
+    return DescView{__ldg(&d->remote), __ldg(&d->local), __ldg(&d->len)};
 }
 
 // The descriptors from a on that start below hi, at most kWalkMax of them,
@@ -126,14 +130,14 @@ constexpr int kWalkBatch = 4;
 constexpr uint64_t kWalkMax = kPiecesPerTile + 1;
 
 template <class F>
-__device__ __forceinline__ bool walk_tile_descs(const kvx_desc *__restrict__ descs, uint64_t n, uint64_t a,
-                                                uint64_t hi, F &&f) {
+__device__ __forceinline__ bool walk_tile_descs(const kvx_desc *__restrict__ descs, bool d16, uint64_t n,
+                                                uint64_t a, uint64_t hi, F &&f) {
     const uint64_t end = n - a < kWalkMax ? n : a + kWalkMax;
     for (uint64_t k0 = a; k0 < end; k0 += kWalkBatch) {
         DescView e[kWalkBatch];
 #pragma unroll
         for (int j = 0; j < kWalkBatch; j++)
-            if (k0 + j < end) e[j] = load_desc(descs + k0 + j);
+            if (k0 + j < end) e[j] = load_desc(descs + k0 + j, d16);
 #pragma unroll
         for (int j = 0; j < kWalkBatch; j++) {
             if (k0 + j >= end || e[j].local >= hi) return true;
@@ -153,6 +157,7 @@ k_copy_prep(const kvx_desc *__restrict__ descs, const uint64_t *__restrict__ num
             uint32_t *__restrict__ vec_tiles, TmaJob *__restrict__ pieces, CopyCtl *ctl,
             uint32_t *status, unsigned long long key) {
     if (blockIdx.x == 0 && threadIdx.x == 0) ctl->key = key;
+    const bool d16 = (reinterpret_cast<uintptr_t>(descs) & 15) == 0;  // descriptors need only 8-byte alignment
     const uint64_t n = *num_descs < desc_cap ? *num_descs : desc_cap;
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
     const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -220,7 +225,7 @@ k_copy_prep(const kvx_desc *__restrict__ descs, const uint64_t *__restrict__ num
                     // and long enough for the bulk engine
                     bool fit = true, short_desc = false;
                     uint32_t np = 0;
-                    const bool whole = walk_tile_descs(descs, n, a, hi, [&](const DescView &e) {
+                    const bool whole = walk_tile_descs(descs, d16, n, a, hi, [&](const DescView &e) {
                         const uint64_t plo = e.local > lo ? e.local : lo;
                         const uint64_t phi = e.len < hi - e.local ? e.local + e.len : hi;
                         if (plo >= phi) return true;
@@ -260,7 +265,7 @@ k_copy_prep(const kvx_desc *__restrict__ descs, const uint64_t *__restrict__ num
             bp = __shfl_sync(0xFFFFFFFFu, bp, 0) + incl - npieces;
             if (npieces) {
                 const uint64_t cap = (uint64_t)kPiecesPerTile * ntiles;
-                walk_tile_descs(descs, n, a, hi, [&](const DescView &e) {
+                walk_tile_descs(descs, d16, n, a, hi, [&](const DescView &e) {
                     const uint64_t plo = e.local > lo ? e.local : lo;
                     const uint64_t phi = e.len < hi - e.local ? e.local + e.len : hi;
                     if (plo >= phi) return true;

@@ -464,6 +464,44 @@ def test_prepared_copies_match_oracle(mix):
     assert np.array_equal(dst.cpu().numpy(), want_pool)
 
 
+@pytest.mark.parametrize("prepared", [False, True])
+def test_copies_with_descriptors_off_16_byte_boundaries(prepared):
+    """A descriptor array that starts 8 bytes past a 16-byte boundary (the ABI
+    asks only for the struct's own alignment): every copy path, one-call and
+    two-stage, bit-exact against the oracle."""
+    rng = np.random.default_rng(23)
+    lens = [4096] * 400 + [1 << 20] * 2 + list(rng.choice([512, 2048, 6144, 32768], size=300))
+    d, slab_bytes, pool_bytes = _desc_list(rng, [int(x) for x in lens])
+    host_pool = rng.integers(0, 256, pool_bytes, dtype=np.uint8)
+    want_slab = np.zeros(slab_bytes, np.uint8)
+    assert oracle.pack(host_pool, d, want_slab) == 0
+    want_pool = np.full(pool_bytes, 0xA5, np.uint8)
+    assert oracle.unpack(want_slab, d, want_pool) == 0
+    raw = torch.zeros(d.nbytes + 16, dtype=torch.uint8, device="cuda")
+    off = 8 if raw.data_ptr() % 16 == 0 else 0
+    raw[off: off + d.nbytes].copy_(torch.from_numpy(d.view(np.uint8).copy()))
+    dd = raw.data_ptr() + off
+    assert dd % 16 == 8
+    nd = torch.tensor([len(d), 0, 0], dtype=torch.int64, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(kvx.kvx_copy_workspace_size(slab_bytes), dtype=torch.uint8, device="cuda")
+    pool = torch.from_numpy(host_pool).cuda()
+    slab = torch.zeros(slab_bytes, dtype=torch.uint8, device="cuda")
+    dst = torch.full((pool_bytes,), 0xA5, dtype=torch.uint8, device="cuda")
+    if prepared:
+        kvx.kvx_copy_prepare(pool, pool_bytes, dd, nd, len(d), slab, slab_bytes, st, ws)
+        kvx.kvx_pack_prepared(pool, pool_bytes, dd, nd, len(d), slab, slab_bytes, st, ws)
+        kvx.kvx_copy_prepare(dst, pool_bytes, dd, nd, len(d), slab, slab_bytes, st, ws)
+        kvx.kvx_unpack_prepared(slab, slab_bytes, dd, nd, len(d), dst, pool_bytes, st, ws)
+    else:
+        kvx.kvx_pack(pool, pool_bytes, dd, nd, len(d), slab, slab_bytes, st, ws)
+        kvx.kvx_unpack(slab, slab_bytes, dd, nd, len(d), dst, pool_bytes, st, ws)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert np.array_equal(slab.cpu().numpy(), want_slab)
+    assert np.array_equal(dst.cpu().numpy(), want_pool)
+
+
 def test_prepared_copy_misuse_moves_nothing():
     """Lists serve the one copy they were made for: a second copy along the
     same preparation, a copy along a workspace prepared for other
