@@ -502,6 +502,43 @@ def test_copies_with_descriptors_off_16_byte_boundaries(prepared):
     assert np.array_equal(dst.cpu().numpy(), want_pool)
 
 
+@pytest.mark.parametrize("prepared", [False, True])
+def test_copies_with_pool_and_slab_off_16_byte_boundaries(prepared):
+    """Pool and slab buffers that start one byte past a 16-byte boundary: no
+    bulk copy may run (every tile takes the register path's byte copies), and
+    the bytes still match the oracle's."""
+    rng = np.random.default_rng(29)
+    lens = [4096] * 64 + [65536] * 4 + [512] * 32
+    d, slab_bytes, pool_bytes = _desc_list(rng, lens)
+    host_pool = rng.integers(0, 256, pool_bytes, dtype=np.uint8)
+    want_slab = np.zeros(slab_bytes, np.uint8)
+    assert oracle.pack(host_pool, d, want_slab) == 0
+    want_pool = np.full(pool_bytes, 0xA5, np.uint8)
+    assert oracle.unpack(want_slab, d, want_pool) == 0
+    dd = torch.from_numpy(d.view(np.uint8).copy()).cuda()
+    nd = torch.tensor([len(d), 0, 0], dtype=torch.int64, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(kvx.kvx_copy_workspace_size(slab_bytes), dtype=torch.uint8, device="cuda")
+    pool_raw = torch.zeros(pool_bytes + 1, dtype=torch.uint8, device="cuda")
+    pool_raw[1:].copy_(torch.from_numpy(host_pool))
+    slab_raw = torch.zeros(slab_bytes + 1, dtype=torch.uint8, device="cuda")
+    dst_raw = torch.full((pool_bytes + 1,), 0xA5, dtype=torch.uint8, device="cuda")
+    pool, slab, dst = pool_raw.data_ptr() + 1, slab_raw.data_ptr() + 1, dst_raw.data_ptr() + 1
+    assert pool % 16 and slab % 16 and dst % 16
+    if prepared:
+        kvx.kvx_copy_prepare(pool, pool_bytes, dd, nd, len(d), slab, slab_bytes, st, ws)
+        kvx.kvx_pack_prepared(pool, pool_bytes, dd, nd, len(d), slab, slab_bytes, st, ws)
+        kvx.kvx_copy_prepare(dst, pool_bytes, dd, nd, len(d), slab, slab_bytes, st, ws)
+        kvx.kvx_unpack_prepared(slab, slab_bytes, dd, nd, len(d), dst, pool_bytes, st, ws)
+    else:
+        kvx.kvx_pack(pool, pool_bytes, dd, nd, len(d), slab, slab_bytes, st, ws)
+        kvx.kvx_unpack(slab, slab_bytes, dd, nd, len(d), dst, pool_bytes, st, ws)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert np.array_equal(slab_raw.cpu().numpy()[1:], want_slab)
+    assert np.array_equal(dst_raw.cpu().numpy()[1:], want_pool)
+
+
 def test_prepared_copy_misuse_moves_nothing():
     """Lists serve the one copy they were made for: a second copy along the
     same preparation, a copy along a workspace prepared for other
