@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from paged_kv_cache_kvx_gb300 import kvx, workloads as W
-from tables import random_holder, random_lanes
+from tables import random_holder, random_holder_large, random_lanes
 from gpu_helpers import (assert_plan_equal, assert_table_equal, check_all, gpu_plan,
                          oracle_all)
 
@@ -30,6 +30,34 @@ def test_random_holders_bit_exact():
         B = int(rng.integers(1, 40))
         addr, seg_len, numa, pool = random_holder(rng, B, int(rng.integers(1, 9)), int(rng.integers(1, 4)))
         check_all(addr, B, seg_len, numa, pool)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_large_holders_bit_exact(seed):
+    """Seeded holders of up to ~90 MB with every feature mixed: 1-3 NUMA
+    regions, bump or permuted placement with spill moves, 512 B to 8 KiB
+    segments, K-only caches; most take the cooperative planner and several
+    copy paths.  Every output of the five calls equals the oracle's, and the
+    two-stage copies give the oracle's slab and destination too."""
+    addr, seg_len, numa, pool = random_holder_large(np.random.default_rng(2025 + seed))
+    B = addr.shape[0]
+    tr, t, p, local = check_all(addr, B, seg_len, numa, pool)
+    host_pool = W.pool_bytes_np(99, 0, pool)
+    want_slab = np.zeros(p.slab_bytes, dtype=np.uint8)
+    assert oracle.pack(host_pool, p.descs, want_slab) == 0
+    want_dst = np.full(pool, W.CANARY, dtype=np.uint8)
+    assert oracle.unpack(want_slab, p.descs, want_dst) == 0
+    dpool = torch.from_numpy(host_pool).cuda()
+    slab = torch.zeros(max(1, tr.slab_bytes), dtype=torch.uint8, device="cuda")[: tr.slab_bytes]
+    dst = torch.full((pool,), W.CANARY, dtype=torch.uint8, device="cuda")
+    tr.prepare_pack(dpool, slab)
+    tr.prepare_unpack(slab, dst)
+    tr.pack_prepared(dpool, slab)
+    tr.unpack_prepared(slab, dst)
+    torch.cuda.synchronize()
+    assert tr.read_status() == 0
+    assert np.array_equal(slab.cpu().numpy(), want_slab)
+    assert np.array_equal(dst.cpu().numpy(), want_dst)
 
 
 def test_chunk_outgrows_stride_long_stretch():
