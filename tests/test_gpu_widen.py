@@ -12,7 +12,7 @@ import oracle
 from paged_kv_cache_kvx_gb300 import kvx, workloads as W
 from conftest import GOLDEN
 from gpu_helpers import gpu_plan
-from tables import random_holder
+from tables import random_holder, random_holder_large
 
 pytestmark = pytest.mark.gpu
 
@@ -443,3 +443,21 @@ def test_k_only_full_size(layout):
     size 0): every run-table, plan and rebuild array bit-exact."""
     wl = W.k_only(layout)
     check_all(wl.addr, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes, data=False)
+
+
+# ------------------------------------------------------------ fuzz
+
+@pytest.mark.parametrize("seed", range(10))
+def test_seal_and_verify_random_large_holders(seed):
+    """Seeded large holders (as in the parity fuzz): the seal into a permuted
+    receiver layout on both copy paths, and the template check with a size
+    mismatch planted at a seeded block, both equal the oracle's."""
+    rng = np.random.default_rng(7000 + seed)
+    addr, seg_len, numa, pool = random_holder_large(rng, max_bytes=32 << 20)
+    B, L = addr.shape
+    dst_addr, size = receiver_layout(B, seg_len, rng)
+    assert check_seal(addr, B, seg_len, numa, pool, dst_addr, size) == 0
+    sizes = np.tile(seg_len, (B, 1))
+    b = int(rng.integers(0, B))
+    sizes[b, int(rng.integers(0, L))] += 16
+    assert check_verify(addr, sizes, seg_len) == b
