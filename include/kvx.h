@@ -233,8 +233,9 @@ size_t kvx_plan_workspace_size(uint32_t L, uint64_t run_capacity, uint64_t pool_
  * lane_first[table_lanes + 1] (index of each lane's first run, exclusive
  * prefix of runs_per_lane); per run run_block (decoded first block),
  * run_group, run_off (run base - group base);
- * counts[3] = {groups, descriptors, slab bytes} (device).  run_capacity must
- * be <= 2^31 (else KVX_EINVAL).  Capacities below
+ * counts[3] = {groups, descriptors, slab bytes} (device).  groups and descs
+ * need their structs' 8-byte alignment; 16-byte aligned arrays are written in
+ * 16-byte pieces.  run_capacity must be <= 2^31 (else KVX_EINVAL).  Capacities below
  * run_capacity groups or kvx_desc_capacity() descriptors may end in
  * KVX_S_CAPACITY on the device.
  */
