@@ -39,10 +39,13 @@ NOMINAL_HBM_GBS = 8000.0      # the ~8 TB/s nominal HBM3e figure
 FALLBACK_HBM_GBS = 6800.0     # profiling recipe's fallback when no measured peak exists
 WORKLOAD = ("default: 1000 blocks x 288 slots x 2 segments (K,V) x 4 KiB uint8 = 576,000 "
             "segments, 2250 MiB, bump-allocated holder, slots 0-143 / 144-287 in two NUMA regions")
-COPY_SRC = os.path.join(ROOT, "paged_kv_cache_kvx_gb300", "csrc", "kvx_copy.cu")
+# the copy kernels' translation units: the kernel file, then the headers it
+# compiles with (a change to any of them can change the kernel)
+COPY_SRC = [os.path.join(ROOT, "paged_kv_cache_kvx_gb300", "csrc", f)
+            for f in ("kvx_copy.cu", "kvx_ring.cuh", "kvx_common.cuh")]
 PROFILE = os.path.join(ROOT, "profiles", "copy_default.md")
 SEGCOPY_SRC = [os.path.join(ROOT, "paged_kv_cache_kvx_gb300", "csrc", f)
-               for f in ("kvx_segcopy.cu", "kvx_ring.cuh")]
+               for f in ("kvx_segcopy.cu", "kvx_ring.cuh", "kvx_common.cuh")]
 
 
 def dist_env():

@@ -21,8 +21,10 @@
 //   emit     step 4: slab carve (groups back to back) and descriptors (one
 //            per dense group / per block, split at 32 MiB)
 //
-// Runs are cut into tiles of 2048 (8 per thread of a 256-thread block); only
-// as many blocks as there are tiles take part, each owning tiles b, b+P, ...
+// Runs are cut into tiles of 2048 (8 per thread of a 256-thread block), or
+// of 1024 when the table has no more 1024-run tiles than the grid has blocks;
+// only as many blocks as there are tiles take part, each owning tiles b,
+// b+P, ...
 // A block gets the carry for its tile by an ordered reduction of the earlier
 // tiles' aggregates, so scans cost no extra barrier.  Every read of data
 // another block wrote in this kernel bypasses L1.  Tables of up to 2048 runs
@@ -34,8 +36,14 @@ namespace kvx {
 namespace {
 
 constexpr int kT = 256;
+// Runs per thread: 8 (2048-run tiles) in general; 4 or 2 (1024- or 512-run
+// tiles) for tables small enough that every such tile still has a block of
+// its own: each phase's per-thread chains shrink, and no block takes a second
+// tile.  The smaller tiles serve at most kSmallTiles tiles, which bounds the
+// per-tile workspace.
 constexpr int kIPT = 8;
 constexpr uint32_t kTile = kT * kIPT;
+constexpr uint64_t kSmallTiles = 256;
 constexpr uint32_t kDigits = 256;
 
 struct PlanCtl {
@@ -405,6 +413,7 @@ __device__ void phase_init(const PlanArgs &a, uint64_t R) {
 }
 
 // Step 1 per run; lanes; per-tile segmented count sums; key bits.
+template <int IPT>
 __device__ void phase_decode(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, ScanSmem &sm,
                              uint32_t *s_lf) {
     __shared__ uint32_t s_bits;
@@ -427,13 +436,13 @@ __device__ void phase_decode(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
     uint32_t on = 0, ann = ~0u, oe = 0, ae = 1;
     for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
         Seg agg{0, 0, 0};
-        const uint64_t r0 = (uint64_t)tile * kTile + (uint64_t)threadIdx.x * kIPT;
+        const uint64_t r0 = (uint64_t)tile * (kT * IPT) + (uint64_t)threadIdx.x * IPT;
         // all loads of this thread's runs first, then the checks
-        uint32_t lanes[kIPT], cnts[kIPT], lens[kIPT], nodes[kIPT];
-        uint64_t bases[kIPT];
-        int64_t strides[kIPT];
+        uint32_t lanes[IPT], cnts[IPT], lens[IPT], nodes[IPT];
+        uint64_t bases[IPT];
+        int64_t strides[IPT];
 #pragma unroll
-        for (int j = 0; j < kIPT; j++) {
+        for (int j = 0; j < IPT; j++) {
             const uint64_t r = r0 + j;
             lanes[j] = 0;
             if (r < R) {
@@ -445,14 +454,14 @@ __device__ void phase_decode(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
             }
         }
 #pragma unroll
-        for (int j = 0; j < kIPT; j++) {
+        for (int j = 0; j < IPT; j++) {
             if (r0 + j < R) {
                 lens[j] = __ldg(a.seg_len + lanes[j]);
                 nodes[j] = __ldg(a.numa + lanes[j]);
             }
         }
 #pragma unroll
-        for (int j = 0; j < kIPT; j++) {
+        for (int j = 0; j < IPT; j++) {
             const uint64_t r = r0 + j;
             if (r >= R) continue;
             const uint32_t l = lanes[j];
@@ -522,6 +531,7 @@ __device__ uint32_t active_digits(const PlanArgs &a, uint64_t R, uint32_t *act) 
 }
 
 // Step 2: first block of each run, coverage, sort items, first histogram.
+template <int IPT>
 __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, uint32_t nact,
                            uint32_t dig0, ScanSmem &sm, const uint32_t *s_lf, uint32_t *s_hist) {
     const bool lf_smem = a.table_lanes + 1 <= kLaneSmem;
@@ -532,13 +542,13 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
     for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
         for (uint32_t d = threadIdx.x; d < kDigits; d += blockDim.x) s_hist[d] = 0;
         const Seg carry = reduce_prefix(a.seg, tile, SegOp(), Seg{0, 0, 0}, sm.seg);
-        const uint64_t r0 = (uint64_t)tile * kTile + (uint64_t)threadIdx.x * kIPT;
+        const uint64_t r0 = (uint64_t)tile * (kT * IPT) + (uint64_t)threadIdx.x * IPT;
         Seg agg{0, 0, 0};
-        uint32_t cnts[kIPT], lanes[kIPT], nodes[kIPT], empty[kIPT];
-        uint64_t bases[kIPT];
+        uint32_t cnts[IPT], lanes[IPT], nodes[IPT], empty[IPT];
+        uint64_t bases[IPT];
         uint32_t heads = 0;
 #pragma unroll
-        for (int j = 0; j < kIPT; j++) {
+        for (int j = 0; j < IPT; j++) {
             const uint64_t r = r0 + j;
             cnts[j] = 0;
             lanes[j] = 0;
@@ -549,7 +559,7 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
             }
         }
 #pragma unroll
-        for (int j = 0; j < kIPT; j++) {
+        for (int j = 0; j < IPT; j++) {
             const uint64_t r = r0 + j;
             if (r >= R) continue;
             nodes[j] = __ldg(a.numa + lanes[j]);
@@ -562,7 +572,7 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
         block_scan(agg, SegOp(), Seg{0, 0, 0}, sm.seg, &ex, &tot);
         uint64_t blk = SegOp()(carry, ex).sum;  // blocks before this thread's first run
 #pragma unroll
-        for (int j = 0; j < kIPT; j++) {
+        for (int j = 0; j < IPT; j++) {
             const uint64_t r = r0 + j;
             if (r >= R) continue;
             if (heads >> j & 1u) blk = 0;
@@ -577,7 +587,7 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
             // histogram of the first active digit; one shared atomic per distinct
             // digit in each warp round
 #pragma unroll
-            for (int j = 0; j < kIPT; j++) {
+            for (int j = 0; j < IPT; j++) {
                 const uint64_t r = r0 + j;
                 const uint32_t d = r < R ? digit_of(bases[j], nodes[j], empty[j], dig0) : kDigits;
                 const uint32_t peers = __match_any_sync(0xFFFFFFFFu, d);
@@ -619,6 +629,7 @@ struct SortCounters {
 };
 constexpr int kSweep = 32;         // histogram rows loaded at once in the offset sweep
 
+template <int IPT>
 __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P,
                                 const SortItem *in, SortItem *out, const uint32_t *H,
                                 uint32_t *Hn, uint32_t *Hz, uint32_t dig, bool has_next,
@@ -668,11 +679,11 @@ __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint
             const uint32_t tile = blockIdx.x + (c0 + slot) * P;
             for (uint32_t i = threadIdx.x; i < (kT / 32) * kDigits; i += blockDim.x) (&wcnt[0][0])[i] = 0;
             __syncthreads();
-            SortItem it[kIPT];
-            uint32_t d[kIPT], pos[kIPT];
-            const uint64_t t0 = (uint64_t)tile * kTile + (uint64_t)w * (32 * kIPT);
+            SortItem it[IPT];
+            uint32_t d[IPT], pos[IPT];
+            const uint64_t t0 = (uint64_t)tile * (kT * IPT) + (uint64_t)w * (32 * IPT);
 #pragma unroll
-            for (int j = 0; j < kIPT; j++) {
+            for (int j = 0; j < IPT; j++) {
                 const uint64_t idx = t0 + (uint64_t)j * 32 + lane;
                 if (idx < R) {
                     it[j] = ld_cg(in + idx);
@@ -682,7 +693,7 @@ __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint
                 }
             }
 #pragma unroll
-            for (int j = 0; j < kIPT; j++) {
+            for (int j = 0; j < IPT; j++) {
                 const uint32_t peers = __match_any_sync(0xFFFFFFFFu, d[j]);
                 const uint32_t rank = __popc(peers & lt_mask);
                 const uint32_t before = d[j] < kDigits ? wcnt[w][d[j]] : 0;
@@ -702,14 +713,14 @@ __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint
             }
             __syncthreads();
 #pragma unroll
-            for (int j = 0; j < kIPT; j++) {
+            for (int j = 0; j < IPT; j++) {
                 uint64_t key = ~0ull;  // next-histogram bin of this item
                 if (d[j] < kDigits) {
                     const uint64_t dst = (uint64_t)s_base[d[j]] + s_off[slot][d[j]] + wcnt[w][d[j]] + pos[j];
                     if (dst < R) {  // always: the offsets are a permutation of [0, R)
                         out[dst] = it[j];
                         if (has_next)
-                            key = (dst / kTile) * kDigits + digit_of(it[j].base, it[j].node, it[j].r >> 31, ndig);
+                            key = (dst / (kT * IPT)) * kDigits + digit_of(it[j].base, it[j].node, it[j].r >> 31, ndig);
                     }
                 }
                 if (has_next) {  // one atomic per distinct bin in the warp
@@ -738,20 +749,21 @@ __device__ __forceinline__ Rec make_rec(const PlanArgs &a, SortItem it, uint64_t
 }
 
 // Step 3: sorted records and compat flags; per tile, its last stretch start.
+template <int IPT>
 __device__ void phase_adjacent(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P,
                                const SortItem *sorted, ScanSmem &sm) {
     for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
         int64_t mx = -1;
-        const uint64_t p0 = (uint64_t)tile * kTile + (uint64_t)threadIdx.x * kIPT;
+        const uint64_t p0 = (uint64_t)tile * (kT * IPT) + (uint64_t)threadIdx.x * IPT;
         Rec prev;
         bool have_prev = false;
         if (p0 > 0 && p0 < R) {
             prev = make_rec(a, ld_cg(sorted + p0 - 1), R);
             have_prev = true;
         }
-        SortItem its[kIPT];
+        SortItem its[IPT];
 #pragma unroll
-        for (int j = 0; j < kIPT; j++) {
+        for (int j = 0; j < IPT; j++) {
             its[j].r = 0;
             if (p0 + j < R) {
                 its[j] = ld_cg(sorted + p0 + j);
@@ -759,10 +771,10 @@ __device__ void phase_adjacent(const PlanArgs &a, uint64_t R, uint32_t nt, uint3
                 if (its[j].r >= R) its[j].r = 0;  // never taken: a permutation of the runs
             }
         }
-        int64_t strides[kIPT];
-        uint32_t counts[kIPT], blocks[kIPT], lanes[kIPT], lens[kIPT];
+        int64_t strides[IPT];
+        uint32_t counts[IPT], blocks[IPT], lanes[IPT], lens[IPT];
 #pragma unroll
-        for (int j = 0; j < kIPT; j++) {
+        for (int j = 0; j < IPT; j++) {
             if (p0 + j >= R) continue;
             const uint32_t r = its[j].r;
             strides[j] = a.run_stride[r];
@@ -771,10 +783,10 @@ __device__ void phase_adjacent(const PlanArgs &a, uint64_t R, uint32_t nt, uint3
             lanes[j] = __ldcg(a.run_lane + r);
         }
 #pragma unroll
-        for (int j = 0; j < kIPT; j++)
+        for (int j = 0; j < IPT; j++)
             if (p0 + j < R) lens[j] = __ldg(a.seg_len + lanes[j]);
 #pragma unroll
-        for (int j = 0; j < kIPT; j++) {
+        for (int j = 0; j < IPT; j++) {
             const uint64_t p = p0 + j;
             if (p >= R) continue;
             Rec x;
@@ -800,17 +812,18 @@ __device__ void phase_adjacent(const PlanArgs &a, uint64_t R, uint32_t nt, uint3
 }
 
 // Step 3: group starts.
+template <int IPT>
 __device__ void phase_cut(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, ScanSmem &sm) {
     for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
         const int64_t carry = reduce_prefix(a.segmax, tile, MaxOp(), (int64_t)-1, sm.i64);
-        const uint64_t p0 = (uint64_t)tile * kTile + (uint64_t)threadIdx.x * kIPT;
+        const uint64_t p0 = (uint64_t)tile * (kT * IPT) + (uint64_t)threadIdx.x * IPT;
         // every load of this thread's runs first
         uint32_t cm = 0;  // bit j: position p0 + j is compatible with its predecessor
-        uint64_t xb[kIPT];
-        int64_t xs[kIPT];
-        uint32_t xc[kIPT], xl[kIPT];
+        uint64_t xb[IPT];
+        int64_t xs[IPT];
+        uint32_t xc[IPT], xl[IPT];
 #pragma unroll
-        for (int j = 0; j < kIPT; j++) {
+        for (int j = 0; j < IPT; j++) {
             const uint64_t p = p0 + j;
             if (p < R) {
                 const Rec *q = a.rec + p;
@@ -823,7 +836,7 @@ __device__ void phase_cut(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P
         }
         int64_t mx = -1;
 #pragma unroll
-        for (int j = 0; j < kIPT; j++)
+        for (int j = 0; j < IPT; j++)
             if (p0 + j < R && !(cm >> j & 1u)) mx = (int64_t)(p0 + j);
         int64_t ex, tot;
         block_scan(mx, MaxOp(), (int64_t)-1, sm.i64, &ex, &tot);
@@ -831,7 +844,7 @@ __device__ void phase_cut(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P
         uint64_t s_base = 0;                          // base of the current stretch's first run
         if (p0 < R && (cm & 1u)) s_base = __ldcg(&a.rec[s0 > 0 ? s0 : 0].base);
 #pragma unroll
-        for (int j = 0; j < kIPT; j++) {
+        for (int j = 0; j < IPT; j++) {
             const uint64_t p = p0 + j;
             if (p >= R) break;
             const bool c = cm >> j & 1u;
@@ -870,11 +883,12 @@ __device__ void phase_cut(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P
     }
 }
 
+template <int IPT>
 __device__ void phase_count(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, ScanSmem &sm) {
     for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
         GAgg g{0, -1};
-        const uint64_t p0 = (uint64_t)tile * kTile + (uint64_t)threadIdx.x * kIPT;
-        for (int j = 0; j < kIPT; j++) {
+        const uint64_t p0 = (uint64_t)tile * (kT * IPT) + (uint64_t)threadIdx.x * IPT;
+        for (int j = 0; j < IPT; j++) {
             const uint64_t p = p0 + j;
             if (p < R && __ldcg(a.gflag + p)) {
                 g.n++;
@@ -892,23 +906,24 @@ __device__ void phase_count(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t
 // runs, and the fields of the runs that start groups), so a thread pays one
 // round trip per dependency level rather than one per run.  The thread's
 // group count and carve prefix inside the tile are kept for the emit phase.
+template <int IPT>
 __device__ void phase_groups(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, ScanSmem &sm) {
     for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
         const GAgg carry = reduce_prefix(a.gagg, tile, GOp(), GAgg{0, -1}, sm.g);
-        const uint64_t p0 = (uint64_t)tile * kTile + (uint64_t)threadIdx.x * kIPT;
-        uint32_t fl = 0;  // bit j: position p0 + j starts a group (bit kIPT: the next one, or R)
+        const uint64_t p0 = (uint64_t)tile * (kT * IPT) + (uint64_t)threadIdx.x * IPT;
+        uint32_t fl = 0;  // bit j: position p0 + j starts a group (bit IPT: the next one, or R)
 #pragma unroll
-        for (int j = 0; j <= kIPT; j++) {
+        for (int j = 0; j <= IPT; j++) {
             const uint64_t p = p0 + j;
             const uint32_t v = p < R ? (__ldcg(a.gflag + p) ? 1u : 0u) : (p == R ? 1u : 0u);
             fl |= v << j;
         }
-        uint64_t xb[kIPT];
-        uint32_t xr[kIPT], xl[kIPT];
-        int64_t gs[kIPT];
-        uint32_t gb[kIPT], gc[kIPT], gn[kIPT];
+        uint64_t xb[IPT];
+        uint32_t xr[IPT], xl[IPT];
+        int64_t gs[IPT];
+        uint32_t gb[IPT], gc[IPT], gn[IPT];
 #pragma unroll
-        for (int j = 0; j < kIPT; j++) {
+        for (int j = 0; j < IPT; j++) {
             const uint64_t p = p0 + j;
             if (p < R) {
                 const Rec *q = a.rec + p;
@@ -925,7 +940,7 @@ __device__ void phase_groups(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
         }
         GAgg g{0, -1};
 #pragma unroll
-        for (int j = 0; j < kIPT; j++)
+        for (int j = 0; j < IPT; j++)
             if (p0 + j < R && (fl >> j & 1u)) {
                 g.n++;
                 g.last = (int64_t)(p0 + j);
@@ -947,7 +962,7 @@ __device__ void phase_groups(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
         }
         CAgg c{0, 0};
 #pragma unroll
-        for (int j = 0; j < kIPT; j++) {
+        for (int j = 0; j < IPT; j++) {
             const uint64_t p = p0 + j;
             if (p >= R) break;
             if (fl >> j & 1u) {
@@ -987,25 +1002,26 @@ __device__ void phase_groups(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
 // Step 4: carve and descriptors.  A thread takes its group count and carve
 // prefix from the groups phase, so each group end costs one load of its
 // record (all of them issued at once).
+template <int IPT>
 __device__ void phase_emit(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, ScanSmem &sm) {
     for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
         const CAgg carry = reduce_prefix(a.cagg, tile, COp(), CAgg{0, 0}, sm.c);
-        const uint64_t p0 = (uint64_t)tile * kTile + (uint64_t)threadIdx.x * kIPT;
+        const uint64_t p0 = (uint64_t)tile * (kT * IPT) + (uint64_t)threadIdx.x * IPT;
         if (p0 >= R) continue;
         uint32_t fl = 0;
 #pragma unroll
-        for (int j = 0; j <= kIPT; j++) {
+        for (int j = 0; j <= IPT; j++) {
             const uint64_t p = p0 + j;
             const uint32_t v = p < R ? (__ldcg(a.gflag + p) ? 1u : 0u) : (p == R ? 1u : 0u);
             fl |= v << j;
         }
         const GAgg run0 = ld_cg(a.gthr + (uint64_t)tile * kT + threadIdx.x);
         const CAgg cex = ld_cg(a.cthr + (uint64_t)tile * kT + threadIdx.x);
-        uint32_t gids[kIPT];
-        kvx_group G[kIPT];
+        uint32_t gids[IPT];
+        kvx_group G[IPT];
         uint64_t n = run0.n;
 #pragma unroll
-        for (int j = 0; j < kIPT; j++) {
+        for (int j = 0; j < IPT; j++) {
             if (p0 + j < R && (fl >> j & 1u)) n++;
             gids[j] = (uint32_t)(n - 1);
             if (p0 + j < R && (fl >> (j + 1) & 1u)) G[j] = ld_group(a, gids[j]);
@@ -1013,7 +1029,7 @@ __device__ void phase_emit(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
         CAgg cur = COp()(carry, cex);
         const uint64_t M = KVX_MAX_READ_BYTES;
 #pragma unroll
-        for (int j = 0; j < kIPT; j++) {
+        for (int j = 0; j < IPT; j++) {
             if (p0 + j >= R || !(fl >> (j + 1) & 1u)) continue;
             kvx_group g = G[j];
             const uint32_t gid = gids[j];
@@ -1522,7 +1538,7 @@ __global__ void __launch_bounds__(kST, 1) k_plan_small(const __grid_constant__ P
 
 // Shared memory that two stages use in turn: lane_first and the first
 // histogram while the runs are decoded and keyed, then a radix pass's
-// counters.  Sharing it keeps the block at about 22 KB, small enough to sit
+// counters.  Sharing it keeps the block at about 23 KB, small enough to sit
 // beside a bulk-copy block on one SM (a transfer can be planned while another
 // copies).
 struct KeyStage {
@@ -1534,16 +1550,13 @@ union PlanStages {
     SortCounters sort;
 };
 
-__global__ void __launch_bounds__(kT, 2) k_plan(const __grid_constant__ PlanArgs a) {
-    __shared__ ScanSmem sm;
-    __shared__ uint32_t s_act[13];
-    __shared__ uint32_t s_nact;
-    __shared__ PlanStages st;
+// Every phase over tiles of kT * IPT runs.  The shared memory is the
+// kernel's: every tile size uses the same 23 KB.
+template <int IPT>
+__device__ void plan_tiles(const PlanArgs &a, uint64_t R_in, uint64_t R, ScanSmem &sm, uint32_t *s_act,
+                           uint32_t &s_nact, PlanStages &st) {
     uint32_t *s_lf = st.keys.lf;
-    const uint64_t R_in = *a.num_runs;
-    if (plan_is_small(a, R_in)) return;  // planned by k_plan_small
-    const uint64_t R = R_in <= a.run_cap ? R_in : 0;
-    const uint32_t nt = (uint32_t)ceil_div(R, kTile);
+    const uint32_t nt = (uint32_t)ceil_div(R, kT * IPT);
     const uint32_t P = nt < gridDim.x ? (nt ? nt : 1) : gridDim.x;
     if (blockIdx.x >= P) return;
 
@@ -1551,12 +1564,12 @@ __global__ void __launch_bounds__(kT, 2) k_plan(const __grid_constant__ PlanArgs
     PLAN_BARRIER();
     if (__ldcg(&a.ctl->fail)) return;
 
-    phase_decode(a, R, nt, P, sm, s_lf);
+    phase_decode<IPT>(a, R, nt, P, sm, s_lf);
     PLAN_BARRIER();
     if (threadIdx.x == 0) s_nact = active_digits(a, R, s_act);
     __syncthreads();
     const uint32_t nact = s_nact;
-    phase_keys(a, R, nt, P, nact, nact ? s_act[0] : 0, sm, s_lf, st.keys.hist);
+    phase_keys<IPT>(a, R, nt, P, nact, nact ? s_act[0] : 0, sm, s_lf, st.keys.hist);
     PLAN_BARRIER();
     if (__ldcg(&a.ctl->st) != 0) return;  // counts stay 0
 
@@ -1564,18 +1577,18 @@ __global__ void __launch_bounds__(kT, 2) k_plan(const __grid_constant__ PlanArgs
         const SortItem *in = (k & 1) ? a.items1 : a.items0;
         SortItem *out = (k & 1) ? a.items0 : a.items1;
         const bool has_next = k + 1 < nact;
-        phase_sort_pass(a, R, nt, P, in, out, a.hist[k % 3], a.hist[(k + 1) % 3],
+        phase_sort_pass<IPT>(a, R, nt, P, in, out, a.hist[k % 3], a.hist[(k + 1) % 3],
                         a.hist[(k + 2) % 3], s_act[k], has_next, has_next ? s_act[k + 1] : 0,
                         k + 2 < nact, st.sort);
         PLAN_BARRIER();
     }
     const SortItem *sorted = (nact & 1) ? a.items1 : a.items0;
 
-    phase_adjacent(a, R, nt, P, sorted, sm);
+    phase_adjacent<IPT>(a, R, nt, P, sorted, sm);
     PLAN_BARRIER();
-    phase_cut(a, R, nt, P, sm);
+    phase_cut<IPT>(a, R, nt, P, sm);
     PLAN_BARRIER();
-    phase_count(a, R, nt, P, sm);
+    phase_count<IPT>(a, R, nt, P, sm);
     PLAN_BARRIER();
     const GAgg gall = reduce_prefix(a.gagg, nt, GOp(), GAgg{0, -1}, sm.g);
     if (gall.n > a.group_cap) {
@@ -1585,7 +1598,7 @@ __global__ void __launch_bounds__(kT, 2) k_plan(const __grid_constant__ PlanArgs
         }
         return;
     }
-    phase_groups(a, R, nt, P, sm);
+    phase_groups<IPT>(a, R, nt, P, sm);
     PLAN_BARRIER();
     const CAgg call = reduce_prefix(a.cagg, nt, COp(), CAgg{0, 0}, sm.c);
     if (call.descs > a.desc_cap) {
@@ -1600,7 +1613,46 @@ __global__ void __launch_bounds__(kT, 2) k_plan(const __grid_constant__ PlanArgs
         a.counts[1] = call.descs;
         a.counts[2] = call.bytes;
     }
-    phase_emit(a, R, nt, P, sm);
+    phase_emit<IPT>(a, R, nt, P, sm);
+}
+
+// The tile size follows the run count, which only the device knows: the
+// smallest of 512, 1024 and 2048 runs whose tiles all get a block.
+__host__ __device__ __forceinline__ bool tiles_fit(uint64_t R, int ipt, uint64_t blocks) {
+    const uint64_t n = ceil_div(R, (uint64_t)kT * ipt);
+    return n <= kSmallTiles && n <= blocks;
+}
+
+// The block's shared memory, at namespace scope so that the out-of-line
+// bodies below address it as shared memory; one copy per block.
+__shared__ ScanSmem g_sm;
+__shared__ uint32_t g_act[13];
+__shared__ uint32_t g_nact;
+__shared__ PlanStages g_st;
+__shared__ PlanArgs g_args;  // the launch's arguments, for the out-of-line bodies
+
+// The 512- and 1024-run tile bodies are called, not inlined: inlined next to
+// the 2048-run body they made the kernel plan 2048-run tables 5 % slower.
+template <int IPT>
+__device__ __noinline__ void plan_tiles_call(uint64_t R_in, uint64_t R) {
+    plan_tiles<IPT>(g_args, R_in, R, g_sm, g_act, g_nact, g_st);
+}
+
+__global__ void __launch_bounds__(kT, 2) k_plan(const __grid_constant__ PlanArgs a) {
+    const uint64_t R_in = *a.num_runs;
+    if (plan_is_small(a, R_in)) return;  // planned by k_plan_small
+    const uint64_t R = R_in <= a.run_cap ? R_in : 0;
+    const int ipt = tiles_fit(R, 2, gridDim.x) ? 2 : tiles_fit(R, 4, gridDim.x) ? 4 : kIPT;
+    if (ipt == kIPT) {
+        plan_tiles<kIPT>(a, R_in, R, g_sm, g_act, g_nact, g_st);
+        return;
+    }
+    if (threadIdx.x == 0) g_args = a;
+    __syncthreads();
+    if (ipt == 2)
+        plan_tiles_call<2>(R_in, R);
+    else
+        plan_tiles_call<4>(R_in, R);
 }
 
 struct Ws {
@@ -1619,8 +1671,15 @@ struct Ws {
     CAgg *cthr;
 };
 
+// Tiles a table of up to run_cap runs can be cut into (any tile size).
+uint64_t tile_cap(uint64_t run_cap) {
+    const uint64_t big = ceil_div(run_cap ? run_cap : 1, kTile);
+    const uint64_t small = ceil_div(run_cap ? run_cap : 1, (uint64_t)kT * 2);
+    return big > kSmallTiles ? big : (small < kSmallTiles ? small : kSmallTiles);
+}
+
 Ws carve(void *base, uint64_t run_cap, size_t *bytes) {
-    const uint64_t ntc = ceil_div(run_cap ? run_cap : 1, kTile);
+    const uint64_t ntc = tile_cap(run_cap);
     Carver c(base);
     Ws w;
     w.ctl = c.take<PlanCtl>(1);
@@ -1742,7 +1801,7 @@ extern "C" kvx_status kvx_plan_groups(const uint32_t *runs_per_lane, uint32_t ta
     k_plan_small<<<1, kST, sizeof(SmallSmem), s>>>(a);
     KVX_LAUNCHED();
     if (cudaMemsetAsync(w.ctl, 0, sizeof(PlanCtl), s) != cudaSuccess) return KVX_ECUDA;
-    const uint64_t ntc = ceil_div(run_capacity ? run_capacity : 1, kTile);
+    const uint64_t ntc = tile_cap(run_capacity);
     const int maxb = plan_max_blocks();
     const unsigned grid = (unsigned)(ntc < (uint64_t)maxb ? ntc : (uint64_t)maxb);
     void *args[] = {&a};

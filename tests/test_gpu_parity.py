@@ -84,6 +84,25 @@ def test_random_lanes_many_tiles_all_radix_digits():
         assert np.array_equal(tr.read_local(), local)
 
 
+@pytest.mark.parametrize("per_sm,extra", [(512, -2), (512, 0), (512, 2), (1024, 0), (1024, 2)])
+def test_planner_tile_size_boundary(per_sm, extra):
+    """Around 512 and 1024 runs per SM: the cooperative planner cuts the runs
+    into the smallest tiles (512, 1024 or 2048 runs) of which there are no
+    more than blocks (extra 0 uses every block).  Both sides of each boundary
+    equal the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    L = 64
+    B = per_sm * sms // 32 + extra  # pair runs: R = 32 * B
+    addr, seg_len, numa, pool = random_lanes(np.random.default_rng(4242 + per_sm + extra), B, L)
+    t, p, st, local = oracle_all(addr, B, seg_len, numa, pool)
+    assert t.num_runs == L * ((B + 1) // 2)
+    tr = gpu_plan(addr, B, seg_len, numa, pool)
+    assert_table_equal(tr, t)
+    assert p.status == 0 and tr.read_status() == 0
+    assert_plan_equal(tr, p)
+    assert np.array_equal(tr.read_local(), local)
+
+
 @pytest.mark.parametrize("B,L,kind", [(20011, 6, "random"), (30013, 9, "random"), (40960, 4, "bump"),
                                       (9001, 2, "bump")])
 def test_tall_tables_block_per_lane_scan(B, L, kind):
