@@ -263,8 +263,8 @@ def run_reference(args):
     probe = W.bump("default_probe", blocks=20, slots=288, seg=4096, seed=2)
     ppool = W.holder_pool_np(probe)
     t_probe = oracle_sample_step(probe, ppool) / 20.0
-    budget = 60.0
-    blocks = int(max(2, min(1000, budget / max(1e-9, t_probe * (args.steps + args.warmup)))))
+    target_s = 60.0
+    blocks = int(max(2, min(1000, target_s / max(1e-9, t_probe * (args.steps + args.warmup)))))
     wl = W.bump("default_sample", blocks=blocks, slots=288, seg=4096, seed=2)
     pool = W.holder_pool_np(wl)
     for _ in range(args.warmup):
