@@ -356,6 +356,9 @@ def run_kvx(args):
     elif args.workload == "many_small" and args.blocks != 1000:
         wl = W.many_small(blocks=args.blocks, nreloc=args.blocks // 20)  # reduced for profiler captures
         args.no_aux = True
+    elif args.workload == "mixed" and args.blocks != 1000:
+        wl = W.mixed(blocks=args.blocks)  # reduced for profiler captures
+        args.no_aux = True
     elif args.workload != "default":
         wl = W.CONFIGS[args.workload]()
         args.no_aux = True  # the e2e leg is defined on the default workload
@@ -466,7 +469,10 @@ def run_kvx(args):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
         "config": {"workload": WORKLOAD, "bytes_moved_per_step": 4 * N,
-                   "l2": "inputs larger than L2 (2250 MiB pool and slab vs 129 MB), no flush",
+                   "l2": ("inputs larger than L2 (%.0f MiB pool, %.0f MiB slab vs 129 MB), no flush"
+                          if min(wl.pool_bytes, N) > 129e6 else
+                          "inputs of %.2f MiB pool, %.2f MiB slab stay in L2 (not flushed: a parity "
+                          "configuration, not the headline)") % (wl.pool_bytes / 2**20, N / 2**20),
                    "runs": nruns, "groups": ngroups, "descs": ndescs},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
@@ -926,7 +932,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work for the oracle baseline leg of the kvx arm")
     ap.add_argument("--blocks", type=int, default=1000,
-                    help="blocks of the default, worst or many_small shape (fewer only for profiler "
+                    help="blocks of the default, worst, mixed or many_small shape (fewer only for profiler "
                          "captures; the full table otherwise)")
     ap.add_argument("--workload", default="default",
                     choices=["default", "tiny", "worst", "mixed", "many_small", "wide64k", "konly",
