@@ -51,10 +51,20 @@
  *     and reads it after synchronising).  A nonzero status means the outputs
  *     of that call are undefined, except as stated per call.  No call traps
  *     or asserts.  Thread blocks wait on one another only at the grid
- *     barriers of cooperative launches (encode, plan), each bounded by one
- *     second of wall time, after which the kernel ORs KVX_S_TIMEOUT and
- *     returns: bad input cannot hang or fault the GPU; every global access
- *     is checked against the capacities passed in.
+ *     barriers of cooperative launches (encode, verify-encode, plan), each
+ *     bounded by one second of wall time, after which the kernel ORs
+ *     KVX_S_TIMEOUT and returns: bad input cannot hang or fault the GPU;
+ *     every global access is checked against the capacities passed in.
+ *   - Co-scheduling: the grid of a cooperative launch is sized to fit on
+ *     the device, but while other kernels occupy SMs (the library's own
+ *     copies included: these calls are meant to run beside them) some of its
+ *     blocks start only when room frees up.  If other work keeps the SMs so full
+ *     that some block of kvx_encode_runs, kvx_verify_encode or
+ *     kvx_plan_groups waits more than a second for room while the others
+ *     wait at a grid barrier, the call ends with KVX_S_TIMEOUT and invalid
+ *     outputs (reported, never silent).  Callers that run kernels lasting
+ *     a second or more beside these calls should order them (a stream or
+ *     an event) or re-run the call when KVX_S_TIMEOUT comes back.
  *   - Outputs must not alias inputs.
  *
  * Layouts: the address table and the rebuilt local pointers are block-major,
@@ -195,6 +205,26 @@ kvx_status kvx_verify_encode(const uint64_t *addr, const uint32_t *seg_size,
  * plus one extra piece per 32 MiB of slab.  seg_bytes_sum = sum of the
  * template's segment lengths. */
 uint64_t kvx_desc_capacity(uint32_t B, uint32_t L, uint64_t seg_bytes_sum);
+
+/*
+ * Host-only helper, no device work: the output capacities kvx_plan_groups
+ * needs for a table of B blocks and L lanes (Requester steps 3-4: at most one
+ * group per run; at most one read per segment plus one extra piece per
+ * 32 MiB of slab).
+ *
+ *   num_runs             the table's run count when the host knows it, or 0
+ *                        for "unknown" (the greedy bound kvx_run_capacity(B,
+ *                        L) is used instead).
+ *   max_seg_bytes_total  sum of the template's segment lengths (bytes per
+ *                        block).
+ *   group_cap, desc_cap  out (host pointers): groups and descriptors to
+ *                        allocate; equal to the bounds the plan checks.
+ * Returns KVX_EINVAL for a null output pointer or a num_runs above
+ * kvx_run_capacity(B, L) (no greedy encoding of B blocks has that many).
+ */
+kvx_status kvx_plan_bounds(uint32_t B, uint32_t L, uint64_t num_runs,
+                           uint64_t max_seg_bytes_total, uint64_t *group_cap,
+                           uint64_t *desc_cap);
 
 size_t kvx_plan_workspace_size(uint32_t L, uint64_t run_capacity, uint64_t pool_bytes);
 

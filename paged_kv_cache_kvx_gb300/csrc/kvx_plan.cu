@@ -1718,6 +1718,18 @@ extern "C" uint64_t kvx_desc_capacity(uint32_t B, uint32_t L, uint64_t seg_bytes
     return (uint64_t)B * L + (uint64_t)((slab + KVX_MAX_READ_BYTES - 1) / KVX_MAX_READ_BYTES);
 }
 
+extern "C" kvx_status kvx_plan_bounds(uint32_t B, uint32_t L, uint64_t num_runs,
+                                      uint64_t max_seg_bytes_total, uint64_t *group_cap,
+                                      uint64_t *desc_cap) {
+    if (!group_cap || !desc_cap) return KVX_EINVAL;
+    const uint64_t runs_max = kvx_run_capacity(B, L);
+    if (num_runs > runs_max) return KVX_EINVAL;  // no greedy encoding of B blocks has that many
+    // every group holds at least one run
+    *group_cap = num_runs ? num_runs : runs_max;
+    *desc_cap = kvx_desc_capacity(B, L, max_seg_bytes_total);
+    return KVX_OK;
+}
+
 extern "C" size_t kvx_plan_workspace_size(uint32_t L, uint64_t run_capacity, uint64_t pool_bytes) {
     (void)L;
     (void)pool_bytes;

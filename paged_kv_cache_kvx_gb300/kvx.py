@@ -44,6 +44,7 @@ _SIGS = {
     "kvx_encode_workspace_size": (_SZ, [_U32, _U32]),
     "kvx_encode_runs": (ctypes.c_int, [_P, _U32, _U32, _P, _P, _P, _P, _U64, _P, _P, _P, _SZ, _P]),
     "kvx_desc_capacity": (_U64, [_U32, _U32, _U64]),
+    "kvx_plan_bounds": (ctypes.c_int, [_U32, _U32, _U64, _U64, _P, _P]),
     "kvx_plan_workspace_size": (_SZ, [_U32, _U64, _U64]),
     "kvx_plan_groups": (ctypes.c_int, [_P, _U32, _P, _P, _P, _P, _U64, _U32, _P, _P, _U32, _U64,
                                        _P, _U64, _P, _U64, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -134,6 +135,14 @@ def kvx_encode_runs(addr, B, L, runs_per_lane, run_base, run_stride, run_count, 
 
 def kvx_desc_capacity(B: int, L: int, seg_bytes_sum: int) -> int:
     return int(lib().kvx_desc_capacity(B, L, seg_bytes_sum))
+
+
+def kvx_plan_bounds(B: int, L: int, num_runs: int, max_seg_bytes_total: int):
+    """(group_cap, desc_cap) for kvx_plan_groups; num_runs 0 = unknown."""
+    g, d = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    _check(lib().kvx_plan_bounds(B, L, num_runs, max_seg_bytes_total, ctypes.addressof(g),
+                                 ctypes.addressof(d)), "kvx_plan_bounds")
+    return int(g.value), int(d.value)
 
 
 def kvx_plan_workspace_size(L: int, run_capacity: int, pool_bytes: int) -> int:
@@ -283,8 +292,9 @@ class Transfer:
         seg_sum = int(seg_len.astype(np.uint64).sum())
         self.slab_bytes = self.B * seg_sum
         self.run_cap = kvx_run_capacity(self.B, L)
-        self.group_cap = max(1, self.run_cap)
-        self.desc_cap = max(1, kvx_desc_capacity(self.B, L, seg_sum))
+        group_cap, desc_cap = kvx_plan_bounds(self.B, L, 0, seg_sum)
+        self.group_cap = max(1, group_cap)
+        self.desc_cap = max(1, desc_cap)
         i32, i64, u8 = torch.int32, torch.int64, torch.uint8
         n = max(1, self.run_cap)
         self.seg_len = torch.from_numpy(seg_len.view(np.int32).copy()).to(dev)

@@ -15,7 +15,8 @@ def _declared():
 
 def test_header_declares_the_five_calls():
     names = _declared()
-    for n in ("kvx_encode_runs", "kvx_plan_groups", "kvx_rebuild", "kvx_pack", "kvx_unpack"):
+    for n in ("kvx_encode_runs", "kvx_plan_bounds", "kvx_plan_groups", "kvx_rebuild", "kvx_pack",
+              "kvx_unpack"):
         assert n in names
 
 
@@ -39,6 +40,25 @@ def test_library_loads_and_answers_host_queries():
     assert kvx.kvx_encode_workspace_size(1000, 576) > 0
     assert kvx.kvx_plan_workspace_size(576, 288000, 2**31) > 0
     assert kvx.kvx_copy_workspace_size(2**31) >= 4 * (2**31 // 32768)
+
+
+def test_plan_bounds_through_the_c_abi():
+    """kvx_plan_bounds: one group per run at most (the greedy bound when the
+    run count is unknown), one read per segment plus one piece per 32 MiB."""
+    import ctypes
+    from paged_kv_cache_kvx_gb300 import kvx
+    L = kvx.lib()
+    g, d = ctypes.c_uint64(7), ctypes.c_uint64(7)
+    assert L.kvx_plan_bounds(1000, 576, 0, 576 * 4096, ctypes.addressof(g), ctypes.addressof(d)) == 0
+    assert (g.value, d.value) == (576 * 500, 576000 + 71)
+    # the default table's 576 runs (one per lane)
+    assert kvx.kvx_plan_bounds(1000, 576, 576, 576 * 4096) == (576, 576000 + 71)
+    assert kvx.kvx_plan_bounds(0, 0, 0, 0) == (0, 0)
+    # more runs than any greedy encoding of B blocks has, or a missing output
+    assert L.kvx_plan_bounds(1000, 576, 576 * 500 + 1, 4096, ctypes.addressof(g),
+                             ctypes.addressof(d)) == EINVAL
+    assert L.kvx_plan_bounds(1000, 576, 576, 4096, None, ctypes.addressof(d)) == EINVAL
+    assert L.kvx_plan_bounds(1000, 576, 576, 4096, ctypes.addressof(g), None) == EINVAL
 
 
 def test_binding_has_no_cpu_fallback():
