@@ -31,7 +31,6 @@
 // the grid streams one window of the slab at a time.  The copies run in one
 // call (kvx_pack / kvx_unpack) or in two: the checks and lists first
 // (kvx_copy_prepare), the bytes later (kvx_pack_prepared / _unpack_prepared).
-#include <atomic>
 
 #include "kvx_ring.cuh"
 
@@ -737,20 +736,20 @@ namespace {
 constexpr size_t kNoallocScratchBytes = (size_t)4 << 20;  // 4 MiB
 static __device__ __align__(256) unsigned char g_pack_scratch[kNoallocScratchBytes];
 
-// Device address of g_pack_scratch on the current device.  The name is only
-// a host-side stand-in, so the address is looked up once per device, with
-// that device current, on the first call there.
+// Device address of g_pack_scratch in the current context.  The name is only
+// a host-side stand-in, so the address is looked up on every call, with the
+// caller's device and context current: an address remembered from an earlier
+// call could belong to a context that has since been reset or to another
+// context on the same device.  Once this file's module is loaded in a
+// context (its first call there, or any earlier launch of a kernel of this
+// file), the lookup is a host-side table search that touches no device
+// memory.
 void *pack_scratch_address() {
-    static std::atomic<void *> addr[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    void *p = addr[dev].load(std::memory_order_acquire);
-    if (p) return p;
+    void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_pack_scratch) != cudaSuccess) {
         (void)cudaGetLastError();
         return nullptr;
     }
-    addr[dev].store(p, std::memory_order_release);
     return p;
 }
 
