@@ -286,30 +286,30 @@ kvx_status kvx_plan_groups(const uint32_t *runs_per_lane, uint32_t table_lanes,
 
 /*
  * Rebuild every segment's slab pointer arithmetically (Requester step 5).
- * With r the run of lane l covering block b, G its group and i = b - G.block:
- * a dense group gives the page's local = group_local + (remote(b) -
- * group_remote) = G.local + i * G.stride + run_off[r]; a non-dense group
- * gives its dense local mirror, G.local + i * G.chunk + run_off[r].  Each
- * pointer is checked: the group index is below counts[0], the run starts at
- * the group's first block (as every run of a planned group does), b lies in
- * the group's block range, the segment [local, local + seg_len[l]) lies
- * inside block i's chunk of the group carve, and the carve ends within
- * slab_bytes.  A failing entry is set to UINT64_MAX and KVX_S_BOUNDS is
- * raised.  The runs' own strides are not passed: a dense group's stride
- * stands for them.
+ * With r the run of lane l covering block b, G its group, i = b - G.block
+ * and remote(b) = run_base[r] + (b - run_block[r]) * run_stride[r] (the run
+ * arithmetic, wrapping in 64 bits): a dense group gives the page's local =
+ * group_local + (remote(b) - group_remote) = G.local + (remote(b) - G.base);
+ * a non-dense group gives its dense local mirror, G.local + i * G.chunk +
+ * (remote(b) - (G.base + i * G.stride)).  Both are evaluated exactly.  Each
+ * pointer is checked: the group index is below counts[0], b lies in the
+ * group's block range, the segment [local, local + seg_len[l]) lies inside
+ * block i's chunk of the group carve, and the carve ends within slab_bytes.
+ * A failing entry is set to UINT64_MAX and KVX_S_BOUNDS is raised.
  *
- * Inputs: lane_first [L + 1], run_block, run_group, run_off [run_capacity]
- * and groups as kvx_plan_groups wrote them; counts (device, [0] = groups);
- * seg_len [L]; slab_bytes (the slab buffer's size).
+ * Inputs: lane_first [L + 1], run_block, run_group [run_capacity] and groups
+ * as kvx_plan_groups wrote them; run_base, run_stride [run_capacity] as
+ * kvx_encode_runs wrote them (the table that was planned); counts (device,
+ * [0] = groups); seg_len [L]; slab_bytes (the slab buffer's size).
  * Output: local [B][L] uint64 (block-major).
  */
 kvx_status kvx_rebuild(const uint32_t *lane_first, const uint32_t *run_block,
-                       const uint32_t *run_group, const uint64_t *run_off,
-                       uint64_t run_capacity, const kvx_group *groups,
-                       uint64_t group_capacity, const uint64_t *counts,
-                       uint32_t B, uint32_t L, const uint32_t *seg_len,
-                       uint64_t slab_bytes, uint64_t *local,
-                       uint32_t *status, void *stream);
+                       const uint64_t *run_base, const int64_t *run_stride,
+                       const uint32_t *run_group, uint64_t run_capacity,
+                       const kvx_group *groups, uint64_t group_capacity,
+                       const uint64_t *counts, uint32_t B, uint32_t L,
+                       const uint32_t *seg_len, uint64_t slab_bytes,
+                       uint64_t *local, uint32_t *status, void *stream);
 
 /* ------------------------------------------------------------ pack/unpack */
 
@@ -368,7 +368,8 @@ size_t kvx_segcopy_workspace_size(void);
  * others are copied.  dst_addr = the holder table gives the bytes kvx_unpack
  * writes.
  *
- * Inputs: the plan outputs as for kvx_rebuild; the slab (read, slab_bytes);
+ * Inputs: the run table and plan outputs as for kvx_rebuild; the slab
+ * (read, slab_bytes);
  * dst_addr [B][L] uint64 byte offsets into dst (block-major); dst, dst_bytes.
  * Destination ranges must not overlap each other (else the overlap holds
  * undefined bytes) and must not overlap the slab.
@@ -382,8 +383,9 @@ size_t kvx_segcopy_workspace_size(void);
  * ones.  One launch (plus a memset of ws).
  */
 kvx_status kvx_seal_blocks(const uint32_t *lane_first, const uint32_t *run_block,
-                           const uint32_t *run_group, const uint64_t *run_off,
-                           uint64_t run_capacity, const kvx_group *groups,
+                           const uint64_t *run_base, const int64_t *run_stride,
+                           const uint32_t *run_group, uint64_t run_capacity,
+                           const kvx_group *groups,
                            uint64_t group_capacity, const uint64_t *counts,
                            uint32_t B, uint32_t L, const uint32_t *seg_len,
                            const uint8_t *slab, uint64_t slab_bytes,
@@ -464,13 +466,23 @@ kvx_status kvx_unpack_prepared(const uint8_t *slab, uint64_t slab_bytes,
  * kvx_pack.  Same arguments and results as kvx_pack, minus ws / ws_bytes.
  *
  * Its scratch is a 4 MiB file-scope device array inside libkvx, held on
- * every GPU that loads the library until the process exits.  That covers
- * slabs up to 131,048 tiles of 64 KiB (about 8 GiB); a larger slab_bytes
- * returns KVX_ECAPACITY and enqueues nothing.  The first call on a device
- * looks up the array's device address (with that device current); make that
- * first call before any stream capture.  Every call shares the array: calls
- * that overlap on the GPU race and must be serialised by the caller.  The
- * call allocates nothing and calls no allocating routine.
+ * every GPU that loads the library until the process exits.  It always
+ * holds the slab's tile lists, which covers slabs up to 131,048 tiles of
+ * 64 KiB (about 8 GiB); a larger slab_bytes returns KVX_ECAPACITY and
+ * enqueues nothing.  For slabs up to about 5,000 tiles (about 330 MB) it
+ * also holds the piece list, so tiles shared by several descriptors take the
+ * bulk-copy rings as in kvx_pack; above that they take the register path
+ * (same bytes).
+ * Every call looks up the array's device address in the current context
+ * (the caller's device and context must be current), so a context that was
+ * reset, or another context on the same device, gets its own copy.  The
+ * first call in a context may load this part of the library's device code
+ * into that context, which the CUDA driver does with an allocation of its
+ * own: make one call (or any other kvx_pack call) at initialisation, before
+ * any stream capture and before the phase that must not allocate.  Every
+ * call shares the array: calls that overlap on the GPU race and must be
+ * serialised by the caller.  Apart from that first module load, the call
+ * allocates nothing and calls no allocating routine.
  */
 kvx_status kvx_pack_noalloc(const uint8_t *pool, uint64_t pool_bytes,
                             const kvx_desc *descs, const uint64_t *num_descs,

@@ -2,16 +2,16 @@
 // Requester step 5: local(b) = group_local + (remote(b) - group_remote),
 // every pointer bounds-checked).
 //
-// With run r of lane l covering block b, G = its group and i = b - G.block:
+// With run r of lane l covering block b, G = its group and i = b - G.block,
+// remote(b) = run_base[r] + (b - run_block[r]) * run_stride[r] (the run
+// arithmetic, wrapping in 64 bits) and
 //   dense group:     local = G.local + (remote(b) - G.base)
-//                          = G.local + i * G.stride + run_off[r]
-//   non-dense group: local = G.local + i * G.chunk + run_off[r]
-// (the page's formula, and its dense local mirror of each remote block).
-// The checks: the group index is valid, the run starts at the group's first
-// block, b is inside the group's block range, [local, local + len) lies
-// inside block i's slice [G.local + i*chunk, G.local + (i+1)*chunk) of the
-// carve, and the carve ends inside the slab.  The call is not given the runs'
-// strides: a dense group's stride stands for them.
+//   non-dense group: local = G.local + i * G.chunk + (remote(b) - (G.base + i * G.stride))
+// (the page's formula, and its dense local mirror of each remote block),
+// evaluated exactly.  The checks: the group index is valid, b is inside the
+// group's block range, [local, local + len) lies inside block i's slice
+// [G.local + i*chunk, G.local + (i+1)*chunk) of the carve, and the carve ends
+// inside the slab.
 //
 // Thread layout as in the encoder: a CTA is 8 warps; lane t of warp w handles
 // lane l0 + t over K consecutive blocks, so each warp store is one coalesced
@@ -80,8 +80,8 @@ __device__ __forceinline__ uint64_t find_run(const uint32_t *__restrict__ run_bl
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 k_rebuild(const uint32_t *__restrict__ lane_first, const uint32_t *__restrict__ run_block,
-          const uint32_t *__restrict__ run_group, const uint64_t *__restrict__ run_off,
-          uint64_t run_cap, const kvx_group *__restrict__ groups, uint64_t group_cap,
+          const uint64_t *__restrict__ run_base, const int64_t *__restrict__ run_stride,
+          const uint32_t *__restrict__ run_group, uint64_t run_cap, const kvx_group *__restrict__ groups, uint64_t group_cap,
           const uint64_t *__restrict__ counts, uint32_t B, uint32_t L,
           const uint32_t *__restrict__ seg_len, uint64_t slab_bytes, uint64_t *__restrict__ local,
           uint32_t *status, Geometry g) {
@@ -99,15 +99,16 @@ k_rebuild(const uint32_t *__restrict__ lane_first, const uint32_t *__restrict__ 
     uint64_t r = lane_ok ? find_run(run_block, lo, hi, b0, B) : lo;
     uint32_t bad = 0;
     // Per run, everything that does not depend on the block is settled once.
-    // Every valid group advances its local pointer by the chunk per block (a
-    // dense group's stride equals its chunk, and a one-block group has no
-    // step), so local(b) = G.local + (b - G.block)*chunk + off on the run's
-    // window [vs, ve) of blocks inside the group, when off + len <= chunk and
-    // the carve ends inside the slab; the loop then only compares and adds,
-    // and all lanes still store row b together.  A dense group whose stride
-    // differs from its chunk is checked block by block (general).
-    uint64_t vs = 0, ve = 0, v = 0, g_chunk = 0, g_local = 0, g_block = 0, g_count = 0, off = 0, rb = 0;
-    int64_t g_stride = 0;
+    // When the run's stride equals the remote step of the group's blocks (a
+    // dense group's chunk, a non-dense group's stride: true of every run of a
+    // planned group of more than one block) and its addresses do not wrap,
+    // local - slice is the same constant c for every block of the run, so
+    // local(b) = G.local + (b - G.block)*chunk + c on the window [vs, ve) of
+    // blocks in both the run and the group, and the loop only compares and
+    // adds while all lanes still store row b together.  Any other run (a
+    // one-block group, a corrupt record) is evaluated block by block with the
+    // exact formula (general).
+    uint64_t vs = 0, ve = 0, v = 0, g_chunk = 0;
     bool general = false;
     // the run after r: its first block and group index, loaded together
     uint64_t nb = ~0ull;
@@ -121,25 +122,36 @@ k_rebuild(const uint32_t *__restrict__ lane_first, const uint32_t *__restrict__ 
         general = false;
         if (!lane_ok || gi >= ngroups) return;
         const kvx_group G = groups[gi];
-        g_local = G.local;
+        const uint64_t rbase = run_base[r], rb = run_block[r];
+        const int64_t rstr = run_stride[r];
         g_chunk = G.chunk;
-        g_stride = G.stride;
-        g_block = G.block;
-        g_count = G.count;
-        off = run_off[r];
-        rb = run_block[r];
-        // the carve of the group ends inside the slab, and the run starts at
-        // the group's first block (every run of a group does)
-        if ((__int128)g_local + (__int128)G.count * (__int128)g_chunk > (__int128)slab_bytes) return;
-        if (rb != g_block) return;
-        if (G.dense && G.count > 1 && (__int128)g_stride != (__int128)g_chunk) {
+        // the carve of the group ends inside the slab
+        if ((__int128)G.local + (__int128)G.count * (__int128)G.chunk > (__int128)slab_bytes) return;
+        // the run's blocks from b on that lie in the group: [lo, we)
+        uint64_t lo = b > G.block ? b : G.block;
+        if (lo < rb) lo = rb;
+        uint64_t we = (uint64_t)G.block + G.count;
+        if (nb < we) we = nb;
+        if (b1 < we) we = b1;
+        if (lo >= we) return;
+        // the run's stride equals the group's remote step e (a dense group's
+        // chunk, a non-dense group's stride) ...
+        const bool step_ok = G.dense ? (rstr >= 0 && (uint64_t)rstr == G.chunk) : rstr == G.stride;
+        // ... and its addresses do not wrap over the window: they move
+        // monotonically, so only the far end (block we - 1) can leave [0, 2^64)
+        const uint64_t n = we - 1 - rb, m = rstr < 0 ? 0ull - (uint64_t)rstr : (uint64_t)rstr;
+        const uint64_t span = n * m;
+        const bool no_wrap = __umul64hi(n, m) == 0 && (rstr < 0 ? span <= rbase : span <= ~rbase);
+        if (!step_ok || !no_wrap) {
             general = true;
             return;
         }
-        if (!(off <= g_chunk && len <= g_chunk - off)) return;  // the segment overruns its slice
-        vs = g_block > b ? g_block : b;
-        ve = g_block + g_count;
-        if (vs < ve) v = g_local + (vs - g_block) * g_chunk + off;
+        const __int128 e = G.dense ? (__int128)G.chunk : (__int128)G.stride;
+        const __int128 c = (__int128)rbase - (__int128)G.base + ((__int128)G.block - (__int128)rb) * e;
+        if (c < 0 || c + (__int128)len > (__int128)G.chunk) return;  // every block overruns its slice
+        vs = lo;
+        ve = we;
+        v = G.local + (vs - G.block) * G.chunk + (uint64_t)c;
     };
     enter(b0);
     uint64_t *dst = local + b0 * L + l;
@@ -160,12 +172,19 @@ k_rebuild(const uint32_t *__restrict__ lane_first, const uint32_t *__restrict__ 
         if (b >= vs && b < ve) {
             out = v;
             v += g_chunk;
-        } else if (general && b >= g_block && b - g_block < g_count) {
-            // dense: remote(b) - group_remote advances by the stride
-            const uint64_t i = b - g_block;
-            const __int128 loc = (__int128)g_local + (__int128)i * g_stride + (__int128)off;
-            const __int128 slice = (__int128)g_local + (__int128)i * g_chunk;  // block i's part of the carve
-            if (loc >= slice && loc + (__int128)len <= slice + (__int128)g_chunk) out = (uint64_t)loc;
+        } else if (general) {
+            // the exact formula: remote(b) from the run, then the group's (a
+            // cold path: its inputs are loaded again rather than kept live)
+            const kvx_group G = groups[gi];
+            const uint64_t rb = run_block[r];
+            const uint64_t remote = run_base[r] + (b - rb) * (uint64_t)run_stride[r];
+            const __int128 gb = (__int128)b - (__int128)G.block;
+            const __int128 slice = (__int128)G.local + gb * (__int128)G.chunk;  // block gb's part of the carve
+            const __int128 loc = G.dense ? (__int128)G.local + ((__int128)remote - (__int128)G.base)
+                                         : slice + ((__int128)remote - ((__int128)G.base + gb * (__int128)G.stride));
+            if (b >= rb && gb >= 0 && gb < (__int128)G.count && loc >= slice &&
+                loc + (__int128)len <= slice + (__int128)G.chunk)
+                out = (uint64_t)loc;
         }
         if (out == ~0ull) bad = KVX_S_BOUNDS;
         *dst = out;
@@ -179,17 +198,18 @@ k_rebuild(const uint32_t *__restrict__ lane_first, const uint32_t *__restrict__ 
 using namespace kvx;
 
 extern "C" kvx_status kvx_rebuild(const uint32_t *lane_first, const uint32_t *run_block,
-                                  const uint32_t *run_group, const uint64_t *run_off,
-                                  uint64_t run_capacity, const kvx_group *groups,
+                                  const uint64_t *run_base, const int64_t *run_stride,
+                                  const uint32_t *run_group, uint64_t run_capacity, const kvx_group *groups,
                                   uint64_t group_capacity, const uint64_t *counts, uint32_t B,
                                   uint32_t L, const uint32_t *seg_len, uint64_t slab_bytes,
                                   uint64_t *local, uint32_t *status, void *stream) {
     if (!lane_first || !counts || !status) return KVX_EINVAL;
     if ((uint64_t)B * L == 0) return KVX_OK;
-    if (!run_block || !run_group || !run_off || !groups || !seg_len || !local) return KVX_EINVAL;
+    if (!run_block || !run_base || !run_stride || !run_group || !groups || !seg_len || !local)
+        return KVX_EINVAL;
     const Geometry g = geometry(B, L, (uint64_t)sm_count() * kCtasPerSm);
     k_rebuild<<<g.ntl * g.ntr, kThreads, 0, as_stream(stream)>>>(
-        lane_first, run_block, run_group, run_off, run_capacity, groups, group_capacity, counts, B,
+        lane_first, run_block, run_base, run_stride, run_group, run_capacity, groups, group_capacity, counts, B,
         L, seg_len, slab_bytes, local, status, g);
     KVX_LAUNCHED();
     return KVX_OK;

@@ -7,8 +7,8 @@
 //   kvx_seal_blocks  -- seal from template metadata (pegaflow PR #350, the
 //       follow-up named after the stage breakdown): segment (b, l) moves from
 //       the slab at its rebuilt offset to the receiver's dst_addr[b][l]; the
-//       offset comes from the group carve and run_off, so no per-segment
-//       local table is ever written.
+//       offset comes from the run arithmetic and the group carve, so no
+//       per-segment local table is ever written.
 //
 // HBM-bound copies, one warp per batch of 32 segments (pages longer than 4 KiB
 // count as several 4 KiB segments, so that batches stay small and many
@@ -87,8 +87,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_paged_writes(const __g
 // ----------------------------------------------------------------- seal
 
 struct SealArgs {
-    const uint32_t *lane_first, *run_block, *run_group;
-    const uint64_t *run_off;
+    const uint32_t *lane_first, *run_block;
+    const uint64_t *run_base;
+    const int64_t *run_stride;
+    const uint32_t *run_group;
     uint64_t run_cap;
     const kvx_group *groups;
     uint64_t group_cap;
@@ -104,9 +106,12 @@ struct SealArgs {
 };
 
 // Segment s = b*L + l: its rebuilt slab offset (the rebuild's arithmetic and
-// checks: run of lane l covering b by binary search, group index valid, b in
-// the group's block range, the segment inside block i's slice of the carve,
-// the carve inside the slab) and its destination range.
+// checks: the run of lane l covering b by binary search, remote(b) from the
+// run's base and stride, then local = G.local + (remote(b) - G.base) for a
+// dense group or G.local + i*G.chunk + (remote(b) - (G.base + i*G.stride))
+// otherwise, exactly; group index valid, b in the group's block range, the
+// segment inside block i's slice of the carve, the carve inside the slab)
+// and its destination range.
 __device__ __forceinline__ Seg seal_seg(const SealArgs &a, uint64_t s, uint64_t ngroups, uint32_t &bad) {
     const uint32_t b = (uint32_t)(s / a.L), l = (uint32_t)(s % a.L);
     const uint64_t len = a.seg_len[l];
@@ -124,13 +129,13 @@ __device__ __forceinline__ Seg seal_seg(const SealArgs &a, uint64_t s, uint64_t 
         if (gi < ngroups && rb <= b) {
             const kvx_group G = a.groups[gi];
             const __int128 g_local = (__int128)G.local, g_chunk = (__int128)G.chunk;
-            // the run starts at the group's first block (every run of a group does)
-            if (rb == G.block && b >= G.block && b - G.block < G.count &&
+            if (b >= G.block && b - G.block < G.count &&
                 g_local + (__int128)G.count * g_chunk <= (__int128)a.slab_bytes) {
+                const uint64_t remote = a.run_base[x] + (uint64_t)(b - rb) * (uint64_t)a.run_stride[x];
                 const __int128 i = (__int128)(b - G.block);
-                const __int128 step = G.dense ? (__int128)G.stride : g_chunk;
-                const __int128 v = g_local + i * step + (__int128)a.run_off[x];
                 const __int128 slice = g_local + i * g_chunk;
+                const __int128 v = G.dense ? g_local + ((__int128)remote - (__int128)G.base)
+                                           : slice + ((__int128)remote - ((__int128)G.base + i * (__int128)G.stride));
                 if (v >= slice && v + (__int128)len <= slice + g_chunk) {
                     ok = true;
                     loc = (uint64_t)v;
@@ -245,8 +250,8 @@ extern "C" kvx_status kvx_paged_writes(uint64_t page_len, const uint8_t *src, ui
 }
 
 extern "C" kvx_status kvx_seal_blocks(const uint32_t *lane_first, const uint32_t *run_block,
-                                      const uint32_t *run_group, const uint64_t *run_off,
-                                      uint64_t run_capacity, const kvx_group *groups,
+                                      const uint64_t *run_base, const int64_t *run_stride,
+                                      const uint32_t *run_group, uint64_t run_capacity, const kvx_group *groups,
                                       uint64_t group_capacity, const uint64_t *counts, uint32_t B,
                                       uint32_t L, const uint32_t *seg_len, const uint8_t *slab,
                                       uint64_t slab_bytes, const uint64_t *dst_addr, uint8_t *dst,
@@ -255,11 +260,11 @@ extern "C" kvx_status kvx_seal_blocks(const uint32_t *lane_first, const uint32_t
     if (!lane_first || !counts || !status) return KVX_EINVAL;
     if (ws && ws_bytes < kvx_segcopy_workspace_size()) return KVX_EINVAL;
     if ((uint64_t)B * L == 0) return KVX_OK;
-    if (!run_block || !run_group || !run_off || !groups || !seg_len || !dst_addr ||
+    if (!run_block || !run_base || !run_stride || !run_group || !groups || !seg_len || !dst_addr ||
         (slab_bytes && !slab) || (dst_bytes && !dst))
         return KVX_EINVAL;
     static int cache[64] = {};
-    SealArgs a{lane_first, run_block, run_group, run_off, run_capacity, groups, group_capacity,
+    SealArgs a{lane_first, run_block, run_base, run_stride, run_group, run_capacity, groups, group_capacity,
                counts, B, L, seg_len, slab, slab_bytes, dst_addr, dst, dst_bytes, status};
     cudaStream_t s = as_stream(stream);
     if (ws) return launch_bulk(SealGen{a}, ws, s);

@@ -48,8 +48,8 @@ _SIGS = {
     "kvx_plan_workspace_size": (_SZ, [_U32, _U64, _U64]),
     "kvx_plan_groups": (ctypes.c_int, [_P, _U32, _P, _P, _P, _P, _U64, _U32, _P, _P, _U32, _U64,
                                        _P, _U64, _P, _U64, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
-    "kvx_rebuild": (ctypes.c_int, [_P, _P, _P, _P, _U64, _P, _U64, _P, _U32, _U32, _P, _U64, _P,
-                                   _P, _P]),
+    "kvx_rebuild": (ctypes.c_int, [_P, _P, _P, _P, _P, _U64, _P, _U64, _P, _U32, _U32, _P, _U64,
+                                   _P, _P, _P]),
     "kvx_copy_workspace_size": (_SZ, [_U64]),
     "kvx_pack": (ctypes.c_int, [_P, _U64, _P, _P, _U64, _P, _U64, _P, _P, _SZ, _P]),
     "kvx_unpack": (ctypes.c_int, [_P, _U64, _P, _P, _U64, _P, _U64, _P, _P, _SZ, _P]),
@@ -60,8 +60,8 @@ _SIGS = {
     "kvx_verify_encode": (ctypes.c_int, [_P, _P, _P, _U32, _U32, _P, _P, _P, _P, _P, _U64, _P, _P,
                                          _P, _SZ, _P]),
     "kvx_segcopy_workspace_size": (_SZ, []),
-    "kvx_seal_blocks": (ctypes.c_int, [_P, _P, _P, _P, _U64, _P, _U64, _P, _U32, _U32, _P, _P, _U64,
-                                       _P, _P, _U64, _P, _P, _SZ, _P]),
+    "kvx_seal_blocks": (ctypes.c_int, [_P, _P, _P, _P, _P, _U64, _P, _U64, _P, _U32, _U32, _P, _P,
+                                       _U64, _P, _P, _U64, _P, _P, _SZ, _P]),
     "kvx_paged_writes": (ctypes.c_int, [_U64, _P, _U64, _P, _U64, _U64, _P, _U64, _P, _U64, _U64,
                                         _U64, _P, _P, _SZ, _P]),
     "kvx_selftest_timeouts": (ctypes.c_int, [_P, _P]),
@@ -162,12 +162,12 @@ def kvx_plan_groups(runs_per_lane, table_lanes, run_base, run_stride, run_count,
                                  _stream(stream)), "kvx_plan_groups")
 
 
-def kvx_rebuild(lane_first, run_block, run_group, run_off, run_capacity, groups, group_capacity,
-                counts, B, L, seg_len, slab_bytes, local, status, stream=None):
-    _check(lib().kvx_rebuild(_ptr(lane_first), _ptr(run_block), _ptr(run_group), _ptr(run_off),
-                             run_capacity, _ptr(groups), group_capacity, _ptr(counts), B, L,
-                             _ptr(seg_len), slab_bytes, _ptr(local), _ptr(status),
-                             _stream(stream)), "kvx_rebuild")
+def kvx_rebuild(lane_first, run_block, run_base, run_stride, run_group, run_capacity, groups,
+                group_capacity, counts, B, L, seg_len, slab_bytes, local, status, stream=None):
+    _check(lib().kvx_rebuild(_ptr(lane_first), _ptr(run_block), _ptr(run_base), _ptr(run_stride),
+                             _ptr(run_group), run_capacity, _ptr(groups), group_capacity,
+                             _ptr(counts), B, L, _ptr(seg_len), slab_bytes, _ptr(local),
+                             _ptr(status), _stream(stream)), "kvx_rebuild")
 
 
 def kvx_copy_workspace_size(slab_bytes: int) -> int:
@@ -230,14 +230,15 @@ def kvx_segcopy_workspace_size() -> int:
     return int(lib().kvx_segcopy_workspace_size())
 
 
-def kvx_seal_blocks(lane_first, run_block, run_group, run_off, run_capacity, groups,
+def kvx_seal_blocks(lane_first, run_block, run_base, run_stride, run_group, run_capacity, groups,
                     group_capacity, counts, B, L, seg_len, slab, slab_bytes, dst_addr, dst,
                     dst_bytes, status, ws=None, stream=None):
     """ws (a uint8 device tensor of kvx_segcopy_workspace_size() bytes) selects the
     bulk-copy path; None the register path."""
-    _check(lib().kvx_seal_blocks(_ptr(lane_first), _ptr(run_block), _ptr(run_group), _ptr(run_off),
-                                 run_capacity, _ptr(groups), group_capacity, _ptr(counts), B, L,
-                                 _ptr(seg_len), _ptr(slab), slab_bytes, _ptr(dst_addr), _ptr(dst),
+    _check(lib().kvx_seal_blocks(_ptr(lane_first), _ptr(run_block), _ptr(run_base),
+                                 _ptr(run_stride), _ptr(run_group), run_capacity, _ptr(groups),
+                                 group_capacity, _ptr(counts), B, L, _ptr(seg_len), _ptr(slab),
+                                 slab_bytes, _ptr(dst_addr), _ptr(dst),
                                  dst_bytes, _ptr(status), _ptr(ws), 0 if ws is None else ws.numel(),
                                  _stream(stream)), "kvx_seal_blocks")
 
@@ -347,10 +348,10 @@ class Transfer:
                         self.counts, self.status, self.plan_ws, stream)
 
     def rebuild(self, stream=None, slab_bytes=None):
-        kvx_rebuild(self.lane_first, self.run_block, self.run_group, self.run_off, self.run_cap,
-                    self.groups, self.group_cap, self.counts, self.B, self.L, self.seg_len,
-                    self.slab_bytes if slab_bytes is None else slab_bytes, self.local,
-                    self.status, stream)
+        kvx_rebuild(self.lane_first, self.run_block, self.run_base, self.run_stride, self.run_group,
+                    self.run_cap, self.groups, self.group_cap, self.counts, self.B, self.L,
+                    self.seg_len, self.slab_bytes if slab_bytes is None else slab_bytes,
+                    self.local, self.status, stream)
 
     def pack(self, pool, slab, stream=None):
         kvx_pack(pool, pool.numel(), self.descs, self.counts[1:], self.desc_cap, slab,
@@ -386,10 +387,10 @@ class Transfer:
         if bulk is None:
             sl = self.seg_len_host[self.seg_len_host > 0]
             bulk = bool(sl.size) and int(sl.min()) >= 2048
-        kvx_seal_blocks(self.lane_first, self.run_block, self.run_group, self.run_off, self.run_cap,
-                        self.groups, self.group_cap, self.counts, self.B, self.L, self.seg_len,
-                        slab, slab.numel(), dst_addr, dst, dst.numel(), self.status,
-                        self.seg_ws if bulk else None, stream)
+        kvx_seal_blocks(self.lane_first, self.run_block, self.run_base, self.run_stride,
+                        self.run_group, self.run_cap, self.groups, self.group_cap, self.counts,
+                        self.B, self.L, self.seg_len, slab, slab.numel(), dst_addr, dst,
+                        dst.numel(), self.status, self.seg_ws if bulk else None, stream)
 
     def step(self, pool, slab, dst_pool, stream=None, side=None):
         """One pass of the whole path: encode, plan, rebuild, pack, unpack.

@@ -69,3 +69,30 @@ def check_all(addr, B, seg_len, numa, pool, data=True):
         assert oracle.unpack(want_slab, p.descs, want_dst) == 0
         assert np.array_equal(dst.cpu().numpy(), want_dst)
     return tr, t, p, local
+
+
+def assert_equal_chunked(dev: torch.Tensor, want: np.ndarray, chunk: int = 1 << 30):
+    """Every byte of a device buffer equals the host array (compared a chunk
+    at a time, so the host holds one extra chunk, not a second copy)."""
+    assert dev.numel() == want.size, (dev.numel(), want.size)
+    for a in range(0, want.size, chunk):
+        b = min(want.size, a + chunk)
+        got = dev[a:b].cpu().numpy()
+        if not np.array_equal(got, want[a:b]):
+            k = int(np.flatnonzero(got != want[a:b])[0])
+            raise AssertionError("first difference at byte %d: %d != %d" % (a + k, got[k], want[a + k]))
+
+
+def host_generator_bytes(dev_pool: torch.Tensor, seed: int, probes: int = 8) -> np.ndarray:
+    """The holder pool's bytes on the host, copied from the device buffer that
+    workloads.fill_pool_torch filled, with a few 64 KiB windows checked
+    against the numpy generator (so they are the generator's bytes, not
+    anything the CUDA path wrote)."""
+    host = dev_pool.cpu().numpy()
+    rng = np.random.default_rng(seed)
+    n = host.size
+    for a in rng.integers(0, max(1, n - 65536), size=probes):
+        a = int(a) & ~7
+        m = min(65536, n - a)
+        assert np.array_equal(host[a:a + m], W.pool_bytes_np(seed, a, m)), a
+    return host

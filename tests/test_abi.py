@@ -127,7 +127,7 @@ def test_copies_reject_small_workspaces():
     # nothing to copy: returns at once, no launch
     assert L.kvx_paged_writes(4096, P, 1 << 20, P, 4096, 0, P, 1 << 20, P, 4096, 0, 0, P, None, 0,
                               None) == 0
-    assert L.kvx_seal_blocks(P, P, P, P, 10, P, 10, P, 4, 4, P, P, 1 << 20, P, P, 1 << 20, P, P,
+    assert L.kvx_seal_blocks(P, P, P, P, P, 10, P, 10, P, 4, 4, P, P, 1 << 20, P, P, 1 << 20, P, P,
                              seg_ws - 1, None) == EINVAL
     assert ws > 0
 

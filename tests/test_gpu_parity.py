@@ -13,7 +13,8 @@ import torch
 import oracle
 from paged_kv_cache_kvx_gb300 import kvx, workloads as W
 from tables import random_holder, random_holder_large, random_lanes
-from gpu_helpers import (assert_plan_equal, assert_table_equal, check_all, gpu_plan,
+from gpu_helpers import (assert_equal_chunked, assert_plan_equal, assert_table_equal, check_all,
+                         gpu_plan, host_generator_bytes,
                          oracle_all)
 
 pytestmark = pytest.mark.gpu
@@ -341,16 +342,35 @@ def test_rebuild_bounds_match_oracle():
     assert np.array_equal(tr.read_local(), want)
 
 
-@pytest.mark.parametrize("mutate", ["block", "count", "dense", "off", "chunk_small", "local"])
+# mutation -> (small variant, status the oracle's rebuild gives)
+CORRUPT_GROUPS = {
+    "block": ("default_s", oracle.S_BOUNDS),
+    "count": ("default_s", oracle.S_BOUNDS),
+    "dense": ("many_small", oracle.S_BOUNDS),
+    "off": ("default_s", oracle.S_BOUNDS),
+    "chunk_small": ("default_s", oracle.S_BOUNDS),
+    "local": ("default_s", oracle.S_BOUNDS),
+    # the page's dense formula reads remote(b) - group_remote from the runs,
+    # so a dense group's stride field takes no part: same pointers, no error
+    "stride_dense": ("default_s", 0),
+    # a non-dense group's mirror subtracts G.base + i*G.stride: blocks after
+    # the first move out of their slices
+    "stride_nondense": ("worst", oracle.S_BOUNDS),
+}
+
+
+@pytest.mark.parametrize("mutate", sorted(CORRUPT_GROUPS))
 def test_rebuild_corrupt_groups_match_oracle(mutate):
     """Group records that break one check each, on groups of many blocks: the
     first block moved (its runs no longer start there), the block count cut,
     a non-dense group marked dense (its stride then differs from its chunk
     and every block is checked on its own), the chunk one byte short of its
-    last run's end, a chunk shorter than the segments, a carve past the slab.
+    last run's end, a chunk shorter than the segments, a carve past the slab,
+    and the stride field alone altered on a dense and on a non-dense group.
     Every pointer and the status word match the oracle's rebuild of the same
     records, which works from the runs' own addresses."""
-    wl = {v.name: v for v in W.small_variants()}["many_small" if mutate == "dense" else "default_s"]
+    name, want_status = CORRUPT_GROUPS[mutate]
+    wl = {v.name: v for v in W.small_variants()}[name]
     B, L = wl.addr.shape
     t, p, st, local = oracle_all(wl.addr, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
     tr = gpu_plan(wl.addr, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
@@ -367,16 +387,27 @@ def test_rebuild_corrupt_groups_match_oracle(mutate):
         g["chunk"][k] -= 1
     elif mutate == "chunk_small":
         g["chunk"][k] = max(1, int(g["chunk"][k]) // 3)
-    else:
+    elif mutate == "local":
         g["local"][k] += np.uint64(p.slab_bytes)
+    elif mutate == "stride_dense":
+        assert g["dense"][k] == 1
+        g["stride"][k] += 4096
+    else:
+        nd = np.flatnonzero((g["dense"] == 0) & (g["count"] > 1) & (g["stride"] > 0))
+        k = int(nd[0])
+        g["stride"][k] += 4096
     tr.groups[: g.nbytes].copy_(torch.from_numpy(g.view(np.uint8)))
     tr.status.zero_()
     tr.rebuild()
     torch.cuda.synchronize()
     stw, want = oracle.rebuild(t, p, B, L, wl.seg_len, groups=g)
-    assert stw == oracle.S_BOUNDS
+    assert stw == want_status
     assert tr.read_status() == stw
     assert np.array_equal(tr.read_local(), want)
+    if want_status:
+        # only the altered group's pointers are rejected
+        bad = want == np.uint64(2**64 - 1)
+        assert bad.any() and not bad.all()
 
 
 def test_pack_descriptor_checks_match_oracle():
@@ -682,6 +713,10 @@ def test_full_size_prepared_copies(name):
 
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_config(name):
+    """Every configuration at its full size: the run table, the plan and the
+    rebuilt pointers element by element, then every byte of the packed slab
+    against the oracle's pack of the same holder bytes, and every byte of the
+    unpacked destination pool (canary-filled) against the oracle's unpack."""
     wl = W.CONFIGS[name]()
     t, p, st, local = oracle_all(wl.addr, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
     assert p.status == 0 and st == 0
@@ -694,29 +729,22 @@ def test_full_size_config(name):
     pool = torch.empty(wl.pool_bytes, dtype=torch.uint8, device="cuda")
     W.fill_pool_torch(pool, wl.seed)
     slab = torch.empty(tr.slab_bytes, dtype=torch.uint8, device="cuda")
-    tr.pack(pool, slab)
-    torch.cuda.synchronize()
-    assert tr.read_status() == 0
-    # sampled segments against the generator's bytes at their addresses
-    rng = np.random.default_rng(1)
-    B, L = wl.addr.shape
-    bs = rng.integers(0, B, size=400)
-    ls = rng.integers(0, L, size=400)
-    for b, l in zip(bs, ls):
-        a, lo, n = int(wl.addr[b, l]), int(local[b, l]), int(wl.seg_len[l])
-        got = slab[lo:lo + n].cpu().numpy()
-        assert np.array_equal(got, W.pool_bytes_np(wl.seed, a, n)), (b, l)
     dst = torch.full((wl.pool_bytes,), W.CANARY, dtype=torch.uint8, device="cuda")
+    tr.pack(pool, slab)
     tr.unpack(slab, dst)
     torch.cuda.synchronize()
     assert tr.read_status() == 0
+    host_pool = host_generator_bytes(pool, wl.seed)
+    del pool
+    want_slab = np.empty(p.slab_bytes, dtype=np.uint8)
+    assert oracle.pack(host_pool, p.descs, want_slab) == 0
+    del host_pool
+    assert_equal_chunked(slab, want_slab)
     del slab
-    for base, chunk, used in _used_positions(wl):
-        n = used.size * chunk
-        a = pool[base:base + n].view(used.size, chunk)
-        d = dst[base:base + n].view(used.size, chunk)
-        u = torch.from_numpy(used).cuda()
-        assert torch.equal(a[u], d[u])
-        if (~used).any():
-            assert bool((d[~u] == W.CANARY).all())
+    want_dst = np.full(wl.pool_bytes, W.CANARY, dtype=np.uint8)
+    assert oracle.unpack(want_slab, p.descs, want_dst) == 0
+    del want_slab
+    assert_equal_chunked(dst, want_dst)
+    del dst, want_dst
+    torch.cuda.empty_cache()
     assert wl.pool_bytes == sum(r[3] * 2 * r[1] * wl.seg for r in wl.regions)

@@ -11,7 +11,7 @@ import torch
 import oracle
 from paged_kv_cache_kvx_gb300 import kvx, workloads as W
 from conftest import GOLDEN
-from gpu_helpers import gpu_plan
+from gpu_helpers import assert_equal_chunked, gpu_plan, host_generator_bytes
 from tables import random_holder, random_holder_large
 
 pytestmark = pytest.mark.gpu
@@ -130,9 +130,9 @@ def test_paged_empty():
 @pytest.mark.parametrize("bulk", [True, False])
 def test_paged_full_size(bulk):
     """The benchmark's paged workload (576,000 pages of 4 KiB, 2250 MiB moved
-    between two page pools by permuted page tables): every destination page
-    checked against the generator's bytes of its source page on the device,
-    untouched pages keep the canary."""
+    between two page pools by permuted page tables): every byte of the
+    destination pool compared with the oracle's paged write of the same
+    source bytes into a canary-filled pool."""
     wl = W.paged_default()
     src = torch.empty(wl.src_bytes, dtype=torch.uint8, device="cuda")
     W.fill_pool_torch(src, wl.seed)
@@ -143,21 +143,13 @@ def test_paged_full_size(bulk):
                          wl.dst_offset, wl.num_pages, status, _seg_ws() if bulk else None)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    P = wl.page_len
-    s0 = torch.from_numpy(wl.src_offset + wl.src_idx.astype(np.int64) * wl.src_stride).cuda()
-    d0 = torch.from_numpy(wl.dst_offset + wl.dst_idx.astype(np.int64) * wl.dst_stride).cuda()
-    ar = torch.arange(P, device="cuda")
-    for c in range(0, wl.num_pages, 8192):
-        sl = slice(c, min(wl.num_pages, c + 8192))
-        got = dst[(d0[sl, None] + ar).reshape(-1)]
-        want = src[(s0[sl, None] + ar).reshape(-1)]
-        assert torch.equal(got, want)
-    # bytes outside every destination page are untouched
-    mask = torch.ones(wl.dst_bytes, dtype=torch.bool, device="cuda")
-    for c in range(0, wl.num_pages, 8192):
-        sl = slice(c, min(wl.num_pages, c + 8192))
-        mask[(d0[sl, None] + ar).reshape(-1)] = False
-    assert bool((dst[mask] == W.CANARY).all())
+    host_src = host_generator_bytes(src, wl.seed)
+    del src
+    want = np.full(wl.dst_bytes, W.CANARY, dtype=np.uint8)
+    assert oracle.paged_writes(wl.page_len, host_src, wl.src_idx, wl.src_stride, wl.src_offset,
+                               want, wl.dst_idx, wl.dst_stride, wl.dst_offset) == 0
+    del host_src
+    assert_equal_chunked(dst, want)
 
 
 # -------------------------------------------------------------------- seal
@@ -199,9 +191,9 @@ def check_seal(addr, B, seg_len, numa, pool_bytes, dst_addr, dst_bytes, groups=N
     for bulk in (True, False):
         ddst = torch.full((max(1, dst_bytes),), 0xA5, dtype=torch.uint8, device="cuda")
         tr.status.zero_()
-        kvx.kvx_seal_blocks(tr.lane_first, tr.run_block, tr.run_group, tr.run_off, tr.run_cap,
-                            tr.groups, tr.group_cap, tr.counts, B, L, tr.seg_len, dslab, sb, daddr,
-                            ddst, dst_bytes, tr.status, _seg_ws() if bulk else None)
+        kvx.kvx_seal_blocks(tr.lane_first, tr.run_block, tr.run_base, tr.run_stride, tr.run_group,
+                            tr.run_cap, tr.groups, tr.group_cap, tr.counts, B, L, tr.seg_len, dslab,
+                            sb, daddr, ddst, dst_bytes, tr.status, _seg_ws() if bulk else None)
         torch.cuda.synchronize()
         assert tr.read_status() == st_o, bulk
         assert np.array_equal(ddst.cpu().numpy(), want), bulk
@@ -295,34 +287,61 @@ def test_seal_group_block_moved():
                       groups=groups) == oracle.S_BOUNDS
 
 
+@pytest.mark.parametrize("kind", ["dense", "nondense"])
+def test_seal_group_stride_altered(kind):
+    """The stride field of one group altered: on a dense group it takes no
+    part in the page's formula (same bytes, no error); on a non-dense group
+    the blocks after its first leave their slices.  Both copy paths match the
+    oracle's seal, byte for byte and in the status word."""
+    wl = {v.name: v for v in W.small_variants()}["default_s" if kind == "dense" else "worst"]
+    B, L = wl.addr.shape
+    p = oracle.plan(oracle.encode_runs(wl.addr), B, wl.seg_len, wl.numa, wl.pool_bytes)
+    groups = p.groups.copy()
+    sel = (groups["count"] > 1) & (groups["dense"] == (1 if kind == "dense" else 0))
+    if kind == "nondense":
+        sel &= groups["stride"] > 0
+    k = int(np.flatnonzero(sel)[0])
+    groups["stride"][k] += 4096
+    dst_addr, size = receiver_layout(B, wl.seg_len)
+    want = 0 if kind == "dense" else oracle.S_BOUNDS
+    assert check_seal(wl.addr, B, wl.seg_len, wl.numa, wl.pool_bytes, dst_addr, size,
+                      groups=groups) == want
+
+
 @pytest.mark.parametrize("bulk", [True, False])
 def test_seal_full_size_default(bulk):
     """The default workload end to end on the device: pack, then seal into a
-    lane-major receiver layout; every segment compared on the device with
-    the holder bytes it came from."""
+    lane-major receiver layout; every byte of the destination compared with
+    the oracle's seal of the oracle's slab (the oracle's pack of the same
+    holder bytes along the oracle's plan)."""
     wl = W.default()
     B, L = wl.addr.shape
     seg = int(wl.seg_len[0])
+    t = oracle.encode_runs(wl.addr)
+    p = oracle.plan(t, B, wl.seg_len, wl.numa, wl.pool_bytes)
+    assert p.status == 0
     tr = gpu_plan(wl.addr, B, wl.seg_len, wl.numa, wl.pool_bytes)
     assert tr.read_status() == 0
     pool = torch.empty(wl.pool_bytes, dtype=torch.uint8, device="cuda")
     W.fill_pool_torch(pool, wl.seed)
     slab = torch.empty(tr.slab_bytes, dtype=torch.uint8, device="cuda")
     tr.pack(pool, slab)
-    b = torch.arange(B, dtype=torch.int64, device="cuda")[:, None]
-    l = torch.arange(L, dtype=torch.int64, device="cuda")[None, :]
-    dst_addr = ((l * B + b) * seg).reshape(-1).contiguous()
-    dst = torch.empty(B * L * seg, dtype=torch.uint8, device="cuda")
+    dst_addr_np = ((np.arange(L, dtype=np.uint64)[None, :] * np.uint64(B)
+                    + np.arange(B, dtype=np.uint64)[:, None]) * np.uint64(seg))
+    dst_addr = torch.from_numpy(dst_addr_np.view(np.int64).reshape(-1).copy()).cuda()
+    dst = torch.full((B * L * seg,), W.CANARY, dtype=torch.uint8, device="cuda")
     tr.seal(slab, dst_addr, dst, bulk=bulk)
     torch.cuda.synchronize()
     assert tr.read_status() == 0
-    src_addr = torch.from_numpy(wl.addr.view(np.int64)).cuda()
-    # lane-major destination: row l of dst holds lane l's blocks in order
-    for l0 in range(0, L, 8):
-        lanes = slice(l0, min(L, l0 + 8))
-        want = pool[(src_addr[:, lanes].T.reshape(-1, 1) + torch.arange(seg, device="cuda")).reshape(-1)]
-        got = dst[l0 * B * seg: min(L, l0 + 8) * B * seg]
-        assert torch.equal(got, want)
+    host_pool = host_generator_bytes(pool, wl.seed)
+    del pool, slab
+    want_slab = np.empty(p.slab_bytes, dtype=np.uint8)
+    assert oracle.pack(host_pool, p.descs, want_slab) == 0
+    del host_pool
+    want = np.full(B * L * seg, W.CANARY, dtype=np.uint8)
+    assert oracle.seal_blocks(t, p, B, L, wl.seg_len, want_slab, dst_addr_np, want) == 0
+    del want_slab
+    assert_equal_chunked(dst, want)
 
 
 # ------------------------------------------------------------ verify + encode
