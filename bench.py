@@ -116,11 +116,12 @@ def stage_roofline(med_ms, S, R, G, D, L, N, peak):
     (20 B per run, 4 B per lane); plan: the run table read, lane_first,
     run_block / run_group / run_off (16 B per run), groups (48 B) and reads
     (32 B) written; rebuild: a pointer per segment written (8 B), the per-run
-    records and groups read; pack, unpack: N read and N written."""
+    records (first block, group, base, stride: 24 B) and groups read; pack,
+    unpack: N read and N written."""
     nbytes = {
         "encode": 8 * S + 20 * R + 4 * L,
         "plan": 20 * R + 4 * L + 4 * (L + 1) + 16 * R + 48 * G + 32 * D + 24,
-        "rebuild": 8 * S + 16 * R + 48 * G + 4 * (L + 1),
+        "rebuild": 8 * S + 24 * R + 48 * G + 4 * (L + 1),
         "pack": 2 * N,
         "unpack": 2 * N,
     }
@@ -333,41 +334,56 @@ def pool_identity(wl, pool, dst):
     return True
 
 
-def run_kvx(args):
-    import torch
-    import torch.distributed as dist
-    from paged_kv_cache_kvx_gb300 import kvx, workloads as W, build
+# the workloads the default run also measures (each its own entry of
+# per_workload), then the calls beyond the main path
+PER_WORKLOAD = ["worst", "mixed", "many_small", "wide64k", "tiny", "konly"]
+PER_CALL = ["seal", "paged", "verify"]
 
-    rank, world, local_rank = dist_env()
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    build.build()
-    # the oracle leg runs on every workload's own sample unless --no-aux was
-    # given or the table is a reduced one for profiler captures
-    oracle_leg = not args.no_aux and args.blocks == 1000
-    if args.workload == "konly":
-        wl = W.k_only("bump", name="default")
-        args.no_aux = True
-    elif args.workload == "worst" and args.blocks != 1000:
-        wl = W.worst(blocks=args.blocks, npos=2 * args.blocks + 48)  # reduced for profiler captures
-        args.no_aux = True
-    elif args.workload == "many_small" and args.blocks != 1000:
-        wl = W.many_small(blocks=args.blocks, nreloc=args.blocks // 20)  # reduced for profiler captures
-        args.no_aux = True
-    elif args.workload == "mixed" and args.blocks != 1000:
-        wl = W.mixed(blocks=args.blocks)  # reduced for profiler captures
-        args.no_aux = True
-    elif args.workload != "default":
-        wl = W.CONFIGS[args.workload]()
-        args.no_aux = True  # the e2e leg is defined on the default workload
-    elif args.blocks == 1000:
-        wl = W.default()
-    else:
-        wl = W.bump("default", blocks=args.blocks, slots=288, seg=4096, nregions=2, seed=2)
+
+def make_workload(name: str, blocks: int = 1000):
+    """A workload by name (blocks != 1000 gives the reduced tables used for
+    profiler captures)."""
+    from paged_kv_cache_kvx_gb300 import workloads as W
+    if name == "konly":
+        return W.k_only("bump", name="default")
+    if blocks != 1000:
+        if name == "worst":
+            return W.worst(blocks=blocks, npos=2 * blocks + 48)
+        if name == "many_small":
+            return W.many_small(blocks=blocks, nreloc=blocks // 20)
+        if name == "mixed":
+            return W.mixed(blocks=blocks)
+        if name == "default":
+            return W.bump("default", blocks=blocks, slots=288, seg=4096, nregions=2, seed=2)
+    return W.CONFIGS[name]()
+
+
+def describe(name: str, wl) -> str:
+    if name == "default":
+        return WORKLOAD
+    if name == "konly":
+        return ("konly: the default shape as a K-only cache (1000 blocks x 288 slots, K 4 KiB, "
+                "V 0 B), 1125 MiB per copy")
+    return "%s: %d blocks x %d slots x 2 x %d B, %d segments, %.1f MiB payload" % (
+        name, wl.blocks, wl.slots, wl.seg, wl.segments, wl.payload_bytes / 2**20)
+
+
+def l2_note(wl) -> str:
     N = wl.payload_bytes
-    S = wl.segments
+    if min(wl.pool_bytes, N) > 129e6:
+        return ("inputs larger than L2 (%.0f MiB pool, %.0f MiB slab vs 129 MB), no flush"
+                % (wl.pool_bytes / 2**20, N / 2**20))
+    return ("inputs of %.2f MiB pool, %.2f MiB slab stay in L2 (not flushed: a parity configuration, "
+            "not the headline)" % (wl.pool_bytes / 2**20, N / 2**20))
+
+
+def measure_path(wl, K, warmup, dev, world, sample_clocks):
+    """The whole path on one workload: one step checked against the oracle
+    first, then K steps launched call by call with an event between calls, K
+    replays of one captured step, and K independent transfers back to back
+    (overlapped graph).  Returns the buffers and every raw figure."""
+    import torch
+    from paged_kv_cache_kvx_gb300 import kvx, workloads as W
     tr = kvx.Transfer(wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes, device=dev)
     tr.set_addr(wl.addr)
     pool = torch.empty(wl.pool_bytes, dtype=torch.uint8, device=dev)
@@ -382,16 +398,16 @@ def run_kvx(args):
     torch.cuda.synchronize()
     ndescs, ngroups, nruns = check_parity(tr, wl, pool, slab, dst)
 
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         tr.step(pool, slab, dst, stream=stream)
     torch.cuda.synchronize()
 
-    K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local_rank) if rank == 0 else None
+    sampler = ClockSampler(dev.index or 0) if sample_clocks else None
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
     if sampler:
@@ -415,6 +431,7 @@ def run_kvx(args):
     torch.cuda.synchronize()
     launches = kvx.kvx_launch_count() - launches0
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     total_ms = start.elapsed_time(end)
     stage = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(5)] for e in ev])  # ms
@@ -436,77 +453,155 @@ def run_kvx(args):
     if over_ms is not None:
         over_ms = max_over_ranks(over_ms, device=dev)
     clocks = sampler.stop() if sampler else None  # sampled over all three timed regions
+    del tr2
+    return dict(tr=tr, pool=pool, slab=slab, dst=dst, stream=stream, nruns=nruns, ngroups=ngroups,
+                ndescs=ndescs, total_ms=total_ms, stage=stage, launches=launches,
+                graph_ms=graph_ms, graph_launches=graph_launches, over_ms=over_ms,
+                over_launches=over_launches, clocks=clocks)
+
+
+def path_figures(wl, m, K, world, peak, peak_kind):
+    """Every figure of one measured workload: the fastest of the three launch
+    modes as the value, each stage's mean and median time, pack and unpack
+    against the HBM roofline (2 N bytes over the call's mean time), encode
+    Msegments/s and every stage against its algorithmic bytes."""
+    N, S = wl.payload_bytes, wl.segments
+    total_ms, launch_mode, launches = m["total_ms"], "stream", m["launches"]
+    stream_value = step_value(N, K, world, total_ms)
+    graph_ms, over_ms = m["graph_ms"], m["over_ms"]
+    graph_value = step_value(N, K, world, graph_ms) if graph_ms is not None else None
+    if graph_ms is not None and graph_ms < total_ms:
+        total_ms, launch_mode, launches = graph_ms, "cuda_graph", m["graph_launches"]
+    if over_ms is not None and over_ms < total_ms:
+        total_ms, launch_mode, launches = over_ms, "cuda_graph_overlapped", m["over_launches"]
+    med = np.median(m["stage"], axis=0)
+    mean = m["stage"].mean(axis=0)
+    pack_gbs = 2.0 * N / (mean[3] / 1e3) / 1e9
+    unpack_gbs = 2.0 * N / (mean[4] / 1e3) / 1e9
+    both = 4.0 * N / ((mean[3] + mean[4]) / 1e3) / 1e9
+    dom = 3 if mean[3] >= mean[4] else 4
+    achieved = 2.0 * N / (mean[dom] / 1e3) / 1e9
+    names = ["encode", "plan", "rebuild", "pack", "unpack"]
+    return {
+        "value": step_value(N, K, world, total_ms), "ms_per_step": total_ms / K,
+        "launch_mode": launch_mode, "gpu_launches": int(launches),
+        "value_stream_launched": stream_value, "value_graph_one_transfer_at_a_time": graph_value,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "kvx_pack" if dom == 3 else "kvx_unpack",
+                     "peak_source": "%s hbm_gbs" % peak_kind},
+        "pack_gbs": pack_gbs, "unpack_gbs": unpack_gbs, "pack_unpack_gbs": both,
+        "frac_of_%s_peak" % peak_kind: both / peak,
+        "frac_of_nominal_8tbs": both / NOMINAL_HBM_GBS,
+        "encode_msegs_per_s": S / (mean[0] / 1e3) / 1e6,
+        "stage_ms_mean": dict(zip(names, map(float, mean))),
+        "stage_ms_median": dict(zip(names, map(float, med))),
+        "stage_roofline": stage_roofline(med, S, m["nruns"], m["ngroups"], m["ndescs"], wl.lanes, N,
+                                         peak),
+    }
+
+
+def workload_entry(name, args, dev, peak, peak_kind):
+    """One entry of per_workload: the workload's full step checked against
+    the oracle, measured as the headline is, with the oracle's rate on a
+    bounded sample of the same generator."""
+    import torch
+    wl = make_workload(name)
+    m = measure_path(wl, args.steps, args.warmup, dev, 1, True)
+    entry = {"workload": describe(name, wl), "segments": wl.segments,
+             "payload_bytes": wl.payload_bytes, "bytes_moved_per_step": 4 * wl.payload_bytes,
+             "runs": m["nruns"], "groups": m["ngroups"], "descs": m["ndescs"],
+             "parity": ("run table, plan and rebuilt pointers equal to the oracle's; sampled slab "
+                        "segments equal to the generator's bytes; every used pool position "
+                        "restored by unpack"),
+             "l2": l2_note(wl)}
+    entry.update(path_figures(wl, m, args.steps, 1, peak, peak_kind))
+    entry["clocks"] = m["clocks"]
+    for k in ("tr", "pool", "slab", "dst"):
+        m.pop(k)
+    del m
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    cb, desc, n, per = oracle_baseline(target_s=args.aux_cpu_seconds, workload=name)
+    entry["cpu_baseline"] = {"value": cb, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "host": host_info(), "sample": desc}
+    return entry
+
+
+def run_kvx(args):
+    import torch
+    import torch.distributed as dist
+    from paged_kv_cache_kvx_gb300 import build
+
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    build.build()
+    reduced = args.blocks != 1000
+    # e2e, the memcpy comparator and the oracle leg are measured on the
+    # default workload's own line; profiler captures (--no-aux, reduced
+    # tables) skip them
+    headline = args.workload == "default" and not reduced
+    aux = headline and not args.no_aux
+    oracle_leg = not args.no_aux and not reduced
+    wl = make_workload(args.workload, args.blocks)
+    N = wl.payload_bytes
+    K = args.steps
+    m = measure_path(wl, K, args.warmup, dev, world, rank == 0)
+    tr, pool, slab, dst, stream = m["tr"], m["pool"], m["slab"], m["dst"], m["stream"]
 
     # end to end through the same calls with host buffers
-    e2e = measure_e2e(tr, wl, pool, slab, dst, stream, args, dev) if not args.no_aux else None
+    e2e = measure_e2e(tr, wl, pool, slab, dst, stream, args, dev) if aux else None
     # comparator: one plain device-to-device copy of N bytes
-    memcpy_gbs = measure_memcpy(pool, slab, N, stream) if not args.no_aux else None
+    memcpy_gbs = measure_memcpy(pool, slab, N, stream) if aux else None
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return 0
     peak, peak_kind = load_peak()
-    stream_value = step_value(N, K, world, total_ms)
-    launch_mode = "stream"
-    graph_value = step_value(N, K, world, graph_ms) if graph_ms is not None else None
-    if graph_ms is not None and graph_ms < total_ms:
-        total_ms, launch_mode, launches = graph_ms, "cuda_graph", graph_launches
-    if over_ms is not None and over_ms < total_ms:
-        total_ms, launch_mode, launches = over_ms, "cuda_graph_overlapped", over_launches
-    ms_step = total_ms / K
-    value = step_value(N, K, world, total_ms)
-    med = np.median(stage, axis=0)
-    mean = stage.mean(axis=0)
-    pack_gbs = 2.0 * N / (mean[3] / 1e3) / 1e9
-    unpack_gbs = 2.0 * N / (mean[4] / 1e3) / 1e9
-    dom = 3 if mean[3] >= mean[4] else 4
-    achieved = 2.0 * N / (mean[dom] / 1e3) / 1e9
+    fig = path_figures(wl, m, K, world, peak, peak_kind)
     # the committed counters are per launch of the default workload only
-    traffic = profiled_traffic() if args.workload == "default" and args.blocks == 1000 else None
+    fig["roofline"]["traffic"] = profiled_traffic() if headline else None
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "metric": METRIC, "value": fig.pop("value"), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": fig.pop("ms_per_step"), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "bytes_moved_per_step": 4 * N,
-                   "l2": ("inputs larger than L2 (%.0f MiB pool, %.0f MiB slab vs 129 MB), no flush"
-                          if min(wl.pool_bytes, N) > 129e6 else
-                          "inputs of %.2f MiB pool, %.2f MiB slab stay in L2 (not flushed: a parity "
-                          "configuration, not the headline)") % (wl.pool_bytes / 2**20, N / 2**20),
-                   "runs": nruns, "groups": ngroups, "descs": ndescs},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "kvx_pack" if dom == 3 else "kvx_unpack",
-                     "peak_source": "%s hbm_gbs" % peak_kind},
-        "launch_mode": launch_mode, "value_stream_launched": stream_value,
-        "value_graph_one_transfer_at_a_time": graph_value,
-        "pack_gbs": pack_gbs, "unpack_gbs": unpack_gbs,
-        "pack_unpack_gbs": 4.0 * N / ((mean[3] + mean[4]) / 1e3) / 1e9,
-        "frac_of_%s_peak" % peak_kind: 4.0 * N / ((mean[3] + mean[4]) / 1e3) / 1e9 / peak,
-        "frac_of_nominal_8tbs": 4.0 * N / ((mean[3] + mean[4]) / 1e3) / 1e9 / NOMINAL_HBM_GBS,
-        "encode_msegs_per_s": S / (mean[0] / 1e3) / 1e6,
-        "stage_ms_mean": dict(zip(["encode", "plan", "rebuild", "pack", "unpack"], map(float, mean))),
-        "stage_ms_median": dict(zip(["encode", "plan", "rebuild", "pack", "unpack"], map(float, med))),
-        "stage_roofline": stage_roofline(med, S, nruns, ngroups, ndescs, wl.lanes, N, peak),
-        "memcpy_d2d_gbs": memcpy_gbs,
-        "e2e": e2e,
-        "gpu_launches": int(launches),
-        "clocks": clocks,
+        "config": {"workload": describe(args.workload, wl), "bytes_moved_per_step": 4 * N,
+                   "l2": l2_note(wl), "runs": m["nruns"], "groups": m["ngroups"],
+                   "descs": m["ndescs"]},
     }
-    if args.workload == "konly":
-        line["config"]["workload"] = ("konly: the default shape as a K-only cache (1000 blocks x 288 "
-                                      "slots, K 4 KiB, V 0 B), 1125 MiB per copy")
-    elif args.workload != "default":
-        line["config"]["workload"] = "%s: %d blocks x %d slots x 2 x %d B, %d segments (a parity configuration, not the headline)" % (
-            args.workload, wl.blocks, wl.slots, wl.seg, wl.segments)
-        line["config"]["bytes_moved_per_step"] = 4 * N
-    elif args.blocks != 1000:
-        line["config"]["workload"] = "reduced for profiling: %d of the default 1000 blocks" % args.blocks
-    if rank == 0 and world == 1 and oracle_leg:
+    line["roofline"] = fig.pop("roofline")
+    line.update(fig)
+    line["memcpy_d2d_gbs"] = memcpy_gbs
+    line["e2e"] = e2e
+    line["clocks"] = m["clocks"]
+    if reduced:
+        line["config"]["workload"] = "reduced for profiling: %s with %d blocks" % (args.workload,
+                                                                                   args.blocks)
+    if world == 1 and oracle_leg:
         cb, desc, n, per = oracle_baseline(target_s=args.cpu_seconds, workload=args.workload)
         line["cpu_baseline"] = {"value": cb, "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "host": host_info(),
                                 "sample": desc}
+    if world == 1 and aux and not args.headline_only:
+        # every other configuration and the calls beyond the main path, each
+        # checked against the oracle first, in the same run as the headline
+        for k in ("tr", "pool", "slab", "dst"):
+            m.pop(k)
+        del tr, pool, slab, dst
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        per = {}
+        for name in PER_WORKLOAD:
+            per[name] = workload_entry(name, args, dev, peak, peak_kind)
+        for name in PER_CALL:
+            per[name] = measure_next(name, args, dev, args.aux_cpu_seconds)
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+        line["per_workload"] = per
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -723,16 +818,24 @@ def _timed_cpu(fn, target_s):
 
 
 def run_next(args):
-    """--workload paged | seal | verify: the calls that widen the path, each
-    on a full-size input, checked against the oracle / the generator first,
-    then K launches timed with CUDA events on one stream."""
+    """--workload paged | seal | verify as a line of its own."""
     import torch
-    import oracle
-    from paged_kv_cache_kvx_gb300 import kvx, workloads as W, build
-
+    from paged_kv_cache_kvx_gb300 import build
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     build.build()
+    print(json.dumps(measure_next(args.workload, args, dev, args.cpu_seconds)), flush=True)
+    return 0
+
+
+def measure_next(name, args, dev, cpu_seconds):
+    """paged | seal | verify: the calls that widen the path, each on a
+    full-size input, checked against the oracle / the generator first, then
+    K launches timed with CUDA events on one stream.  Returns the line."""
+    import torch
+    import oracle
+    from paged_kv_cache_kvx_gb300 import kvx, workloads as W
+
     oracle.build()
     stream = torch.cuda.Stream(device=dev)
     K = args.steps
@@ -743,7 +846,7 @@ def run_next(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
             "data": "synthetic", "e2e": None}
 
-    if args.workload == "paged":
+    if name == "paged":
         wl = W.paged_default()
         src = torch.empty(wl.src_bytes, dtype=torch.uint8, device=dev)
         W.fill_pool_torch(src, wl.seed)
@@ -752,6 +855,7 @@ def run_next(args):
         di = torch.from_numpy(wl.dst_idx.view(np.int32)).to(dev)
 
         seg_ws = torch.zeros(kvx.kvx_segcopy_workspace_size(), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()  # the buffers were filled on torch's stream, the calls run on ours
 
         def call():
             kvx.kvx_paged_writes(wl.page_len, src, wl.src_bytes, si, wl.src_stride, wl.src_offset,
@@ -779,28 +883,29 @@ def run_next(args):
             d_np = np.zeros(small.dst_bytes, np.uint8)
             per, reps = _timed_cpu(lambda: oracle.paged_writes(
                 small.page_len, s_np, small.src_idx, small.src_stride, 0, d_np, small.dst_idx,
-                small.dst_stride, 0), args.cpu_seconds)
+                small.dst_stride, 0), cpu_seconds)
             return (2 * n * wl.page_len / per / 1e9,
                     "oracle paged_writes, %d pages of 4 KiB between two %d-page pools, %d passes"
                     % (n, n, reps))
 
         def status_ok():
             return int(status.item()) == 0
-    elif args.workload == "seal":
+    elif name == "seal":
         wl = W.default()
         tr = kvx.Transfer(wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes, device=dev)
         tr.set_addr(wl.addr)
         pool = torch.empty(wl.pool_bytes, dtype=torch.uint8, device=dev)
         W.fill_pool_torch(pool, wl.seed)
         slab = torch.empty(tr.slab_bytes, dtype=torch.uint8, device=dev)
-        tr.encode(stream=stream)
-        tr.plan(stream=stream)
-        tr.pack(pool, slab, stream=stream)
         B, L, seg = wl.blocks, wl.lanes, wl.seg
         b = torch.arange(B, dtype=torch.int64, device=dev)[:, None]
         l = torch.arange(L, dtype=torch.int64, device=dev)[None, :]
         dst_addr = ((l * B + b) * seg).reshape(-1).contiguous()   # receiver: lane-major
         dst = torch.full((B * L * seg,), W.CANARY, dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()  # the buffers were filled on torch's stream, the calls run on ours
+        tr.encode(stream=stream)
+        tr.plan(stream=stream)
+        tr.pack(pool, slab, stream=stream)
 
         def call():
             tr.seal(slab, dst_addr, dst, stream=stream)
@@ -829,7 +934,7 @@ def run_next(args):
                   * small.seg).astype(np.uint64)
             d_np = np.zeros(small.payload_bytes, np.uint8)
             per, reps = _timed_cpu(lambda: oracle.seal_blocks(
-                t, p, small.blocks, small.lanes, small.seg_len, sl, da, d_np), args.cpu_seconds)
+                t, p, small.blocks, small.lanes, small.seg_len, sl, da, d_np), cpu_seconds)
             return 2 * small.payload_bytes / per / 1e9, "oracle seal_blocks on the first 40 of 1000 blocks, %d passes" % reps
 
         def status_ok():
@@ -841,6 +946,7 @@ def run_next(args):
         size_np = np.tile(wl.seg_len, (wl.blocks, 1))
         size = torch.from_numpy(size_np.view(np.int32).reshape(-1).copy()).to(dev)
         prefix = torch.zeros(1, dtype=torch.int32, device=dev)
+        torch.cuda.synchronize()  # the buffers were filled on torch's stream, the calls run on ours
 
         def call():
             tr.verify_encode(size, prefix, stream=stream)
@@ -848,6 +954,7 @@ def run_next(args):
         bad = size_np.copy()
         bad[700, 301] = 1
         dbad = torch.from_numpy(bad.view(np.int32).reshape(-1).copy()).to(dev)
+        torch.cuda.synchronize()
         tr.verify_encode(dbad, prefix, stream=stream)
         torch.cuda.synchronize()
         pre_o, t_o = oracle.verify_encode(wl.addr, bad, wl.seg_len)
@@ -865,7 +972,7 @@ def run_next(args):
 
         def cpu_leg():
             per, reps = _timed_cpu(lambda: oracle.verify_encode(wl.addr, size_np, wl.seg_len),
-                                   args.cpu_seconds)
+                                   cpu_seconds)
             return wl.segments / per / 1e6, "oracle verify_encode on the whole default table, %d passes" % reps
 
         def status_ok():
@@ -887,7 +994,7 @@ def run_next(args):
         line.update({"value": value, "unit": "GB/s",
                      "roofline": {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s",
                                   "frac": value / peak, "traffic": profiled_traffic(
-                                      os.path.join(ROOT, "profiles", "%s_default.md" % args.workload),
+                                      os.path.join(ROOT, "profiles", "%s_default.md" % name),
                                       SEGCOPY_SRC), "kernel": kernel,
                                   "peak_source": "%s hbm_gbs" % peak_kind}})
     else:
@@ -901,8 +1008,7 @@ def run_next(args):
     line["cpu_baseline"] = {"value": cb, "unit": line["unit"], "cores": 1, "kind": "oracle",
                             "host": host_info(),
                             "sample": desc}
-    print(json.dumps(line), flush=True)
-    return 0
+    return line
 
 
 def measure_memcpy(pool, slab, N, stream):
@@ -941,7 +1047,11 @@ def main(argv=None):
                          "configurations (konly: the default shape as a K-only cache) and the "
                          "calls beyond the main path (paged, seal, verify)")
     ap.add_argument("--no-aux", action="store_true",
-                    help="skip the e2e, memcpy and CPU-baseline legs (profiler captures)")
+                    help="skip the e2e, memcpy, CPU-baseline and per-workload legs (profiler captures)")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="measure the default workload only (no per_workload entries)")
+    ap.add_argument("--aux-cpu-seconds", type=float, default=3.0,
+                    help="CPU work for the oracle leg of each per_workload entry")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -56,8 +56,32 @@ def test_stage_roofline_bytes_and_fractions():
     ms = [0.020, 0.020, 0.010, 0.700, 0.700]
     r = bench.stage_roofline(ms, S, R, G, D, L, N, 7000.0)
     assert r["encode"]["algorithmic_bytes"] == 8 * S + 20 * R + 4 * L
-    assert r["rebuild"]["algorithmic_bytes"] == 8 * S + 16 * R + 48 * G + 4 * (L + 1)
+    assert r["rebuild"]["algorithmic_bytes"] == 8 * S + 24 * R + 48 * G + 4 * (L + 1)
     assert r["pack"]["algorithmic_bytes"] == r["unpack"]["algorithmic_bytes"] == 2 * N
     assert r["pack"]["gbs"] == pytest.approx(2 * N / 0.7e-3 / 1e9)
     assert r["pack"]["frac"] == pytest.approx(r["pack"]["gbs"] / 7000.0)
     assert r["pack"]["bound"] == "hbm" and r["plan"]["bound"] == "latency"
+
+
+def test_per_workload_figures_reproduce_from_stage_times():
+    """path_figures: the value is the fastest launch mode's 4 N per step, and
+    pack / unpack rates and their roofline fraction come from the stages'
+    mean times (what a reader recomputes from the line)."""
+    import numpy as np
+    from paged_kv_cache_kvx_gb300 import workloads as W
+    wl = W.tiny()
+    N, K = wl.payload_bytes, 4
+    stage = np.array([[0.01, 0.02, 0.005, 0.5, 0.4]] * K)
+    m = dict(total_ms=4.0, stage=stage, launches=40, graph_ms=3.0, graph_launches=40, over_ms=3.5,
+             over_launches=44, nruns=8, ngroups=2, ndescs=2)
+    f = bench.path_figures(wl, m, K, 1, 7000.0, "measured")
+    assert f["launch_mode"] == "cuda_graph" and f["gpu_launches"] == 40
+    assert f["value"] == pytest.approx(4 * N * K / 3.0e-3 / 1e9)
+    assert f["ms_per_step"] == pytest.approx(0.75)
+    assert f["pack_gbs"] == pytest.approx(2 * N / 0.5e-3 / 1e9)
+    assert f["unpack_gbs"] == pytest.approx(2 * N / 0.4e-3 / 1e9)
+    assert f["roofline"]["kernel"] == "kvx_pack"
+    assert f["roofline"]["frac"] == pytest.approx(f["pack_gbs"] / 7000.0)
+    assert f["frac_of_measured_peak"] == pytest.approx(4 * N / 0.9e-3 / 1e9 / 7000.0)
+    assert f["encode_msegs_per_s"] == pytest.approx(wl.segments / 0.01e-3 / 1e6)
+    assert f["stage_ms_mean"]["rebuild"] == pytest.approx(0.005)
