@@ -28,7 +28,7 @@ namespace {
 
 constexpr int kRows = 8;
 constexpr int kThreads = 32 * kRows;
-constexpr int kCtasPerSm = 5;
+constexpr int kCtasPerSm = 4;  // 56 registers: the run entry's gathers and checks fit without spilling
 
 struct Geometry {
     uint32_t K, ntl, ntr;
@@ -98,20 +98,20 @@ k_rebuild(const uint32_t *__restrict__ lane_first, const uint32_t *__restrict__ 
     bool lane_ok = lo < hi && hi <= run_cap;
     uint64_t r = lane_ok ? find_run(run_block, lo, hi, b0, B) : lo;
     uint32_t bad = 0;
-    // Per run, everything that does not depend on the block is settled once.
-    // When the run's stride equals the remote step of the group's blocks (a
-    // dense group's chunk, a non-dense group's stride: true of every run of a
-    // planned group of more than one block) and its addresses do not wrap,
-    // local - slice is the same constant c for every block of the run, so
-    // local(b) = G.local + (b - G.block)*chunk + c on the window [vs, ve) of
-    // blocks in both the run and the group, and the loop only compares and
-    // adds while all lanes still store row b together.  Any other run (a
-    // one-block group, a corrupt record) is evaluated block by block with the
-    // exact formula (general).
-    uint64_t vs = 0, ve = 0, v = 0, g_chunk = 0;
-    bool general = false;
+    // Per run, everything that does not depend on the block is settled once
+    // (enter).  When the run starts at its group's first block, its stride
+    // equals the remote step of the group's blocks (a dense group's chunk, a
+    // non-dense group's stride: true of every run of a planned group) and
+    // its addresses do not wrap, local - slice is the same constant for
+    // every block, so local(b) = G.local + (b - G.block)*chunk + c on the
+    // window [vs, ve) of blocks in both the run and the group, and the loop
+    // only compares and adds while all lanes still store row b together.
+    // Any other run (a one-block group, a corrupt record) is evaluated one
+    // block at a time with the exact formula: enter then covers block b
+    // alone and asks to be called again at b + 1 (re).
+    uint64_t vs = 0, ve = 0, v = 0, g_chunk = 0, re = b0;
     // the run after r: its first block and group index, loaded together
-    uint64_t nb = ~0ull;
+    uint64_t nb = ~0ull, rb = lane_ok ? run_block[r] : 0;  // rb: run r's first block
     uint32_t ngi = 0, gi = lane_ok ? run_group[r] : 0;
     if (lane_ok && r + 1 < hi) {
         nb = run_block[r + 1];
@@ -119,74 +119,91 @@ k_rebuild(const uint32_t *__restrict__ lane_first, const uint32_t *__restrict__ 
     }
     auto enter = [&](uint64_t b) {  // run r from block b on
         vs = ve = 0;
-        general = false;
+        re = nb;
         if (!lane_ok || gi >= ngroups) return;
+        // all loads first, and no branch before every check has used them
+        // (a load sunk past an early return would cost a second round trip
+        // to L2); the run's first block is known from the walk, so each run
+        // costs three gathers besides the group record
         const kvx_group G = groups[gi];
-        const uint64_t rbase = run_base[r], rb = run_block[r];
+        const uint64_t rbase = run_base[r];
         const int64_t rstr = run_stride[r];
         g_chunk = G.chunk;
         // the carve of the group ends inside the slab
-        if ((__int128)G.local + (__int128)G.count * (__int128)G.chunk > (__int128)slab_bytes) return;
+        const bool carve_ok =
+            (__int128)G.local + (__int128)G.count * (__int128)G.chunk <= (__int128)slab_bytes;
         // the run's blocks from b on that lie in the group: [lo, we)
         uint64_t lo = b > G.block ? b : G.block;
-        if (lo < rb) lo = rb;
+        lo = lo < rb ? rb : lo;
         uint64_t we = (uint64_t)G.block + G.count;
-        if (nb < we) we = nb;
-        if (b1 < we) we = b1;
-        if (lo >= we) return;
-        // the run's stride equals the group's remote step e (a dense group's
-        // chunk, a non-dense group's stride) ...
+        we = nb < we ? nb : we;
+        we = b1 < we ? b1 : we;
+        // the fast case: the run starts at the group's first block, its
+        // stride is the group's remote step, and its addresses do not wrap
+        // over the window (moving monotonically, only the far end, block
+        // we - 1, can leave [0, 2^64)); then local - slice = run_base - G.base
         const bool step_ok = G.dense ? (rstr >= 0 && (uint64_t)rstr == G.chunk) : rstr == G.stride;
-        // ... and its addresses do not wrap over the window: they move
-        // monotonically, so only the far end (block we - 1) can leave [0, 2^64)
         const uint64_t n = we - 1 - rb, m = rstr < 0 ? 0ull - (uint64_t)rstr : (uint64_t)rstr;
         const uint64_t span = n * m;
         const bool no_wrap = __umul64hi(n, m) == 0 && (rstr < 0 ? span <= rbase : span <= ~rbase);
-        if (!step_ok || !no_wrap) {
-            general = true;
+        const uint64_t c = rbase - G.base;
+        const bool c_ok = rbase >= G.base && c <= G.chunk && len <= G.chunk - c;
+        if (!carve_ok || lo >= we) return;  // no block of the run is inside the group
+        if (rb == G.block && step_ok && no_wrap) {
+            if (c_ok) {  // otherwise every block overruns its slice
+                vs = lo;
+                ve = we;
+                v = G.local + (vs - G.block) * G.chunk + c;
+            }
             return;
         }
-        const __int128 e = G.dense ? (__int128)G.chunk : (__int128)G.stride;
-        const __int128 c = (__int128)rbase - (__int128)G.base + ((__int128)G.block - (__int128)rb) * e;
-        if (c < 0 || c + (__int128)len > (__int128)G.chunk) return;  // every block overruns its slice
-        vs = lo;
-        ve = we;
-        v = G.local + (vs - G.block) * G.chunk + (uint64_t)c;
+        // The exact formula for block b alone.  The carve ends inside the
+        // slab, so for a block inside the group every offset below G.count *
+        // G.chunk fits in 64 bits; only a non-dense group's G.base + i *
+        // G.stride needs 128.
+        re = b + 1;
+        const uint64_t i = b - G.block;
+        if (b < rb || b < G.block || i >= G.count) return;
+        const uint64_t remote = rbase + (b - rb) * (uint64_t)rstr;
+        const uint64_t slice = i * G.chunk;  // block i's part of the carve, from G.local
+        bool ok;
+        uint64_t off;  // the segment's offset inside its slice
+        if (G.dense) {  // local = G.local + (remote - G.base)
+            ok = remote >= G.base && remote - G.base >= slice;
+            off = remote - G.base - slice;
+        } else {        // local = G.local + slice + (remote - (G.base + i * G.stride))
+            const __int128 e = (__int128)remote - ((__int128)G.base + (__int128)i * (__int128)G.stride);
+            ok = e >= 0 && e <= (__int128)G.chunk;
+            off = (uint64_t)e;
+        }
+        if (ok && off <= G.chunk && len <= G.chunk - off) {
+            vs = b;
+            ve = b + 1;
+            v = G.local + slice + off;
+        }
     };
-    enter(b0);
     uint64_t *dst = local + b0 * L + l;
     for (uint64_t b = b0; b < b1; b++, dst += L) {
-        if (nb <= b) {  // the next run starts at or before b
-            do {
+        if (re <= b) {
+            while (nb <= b) {  // the next run starts at or before b
                 r++;
                 gi = ngi;
+                rb = nb;
                 nb = ~0ull;
                 if (r + 1 < hi) {
                     nb = run_block[r + 1];
                     ngi = run_group[r + 1];
                 }
-            } while (nb <= b);
+            }
             enter(b);
         }
         uint64_t out = ~0ull;
         if (b >= vs && b < ve) {
             out = v;
             v += g_chunk;
-        } else if (general) {
-            // the exact formula: remote(b) from the run, then the group's (a
-            // cold path: its inputs are loaded again rather than kept live)
-            const kvx_group G = groups[gi];
-            const uint64_t rb = run_block[r];
-            const uint64_t remote = run_base[r] + (b - rb) * (uint64_t)run_stride[r];
-            const __int128 gb = (__int128)b - (__int128)G.block;
-            const __int128 slice = (__int128)G.local + gb * (__int128)G.chunk;  // block gb's part of the carve
-            const __int128 loc = G.dense ? (__int128)G.local + ((__int128)remote - (__int128)G.base)
-                                         : slice + ((__int128)remote - ((__int128)G.base + gb * (__int128)G.stride));
-            if (b >= rb && gb >= 0 && gb < (__int128)G.count && loc >= slice &&
-                loc + (__int128)len <= slice + (__int128)G.chunk)
-                out = (uint64_t)loc;
+        } else {
+            bad = KVX_S_BOUNDS;
         }
-        if (out == ~0ull) bad = KVX_S_BOUNDS;
         *dst = out;
     }
     if (bad) atomicOr(status, bad);
