@@ -113,9 +113,13 @@ __device__ __forceinline__ uint64_t ld_addr(const uint64_t *addr, uint64_t b, ui
     return __ldg(addr + b * L + l);
 }
 
-// Slice [b0, b1) of lane l under both entry states.
-__device__ Xfer slice_xfer(const uint64_t *addr, uint32_t L, uint32_t l, uint64_t b0, uint64_t b1) {
+// Slice [b0, b1) of lane l under both entry states; m0 / m1 get a bit per
+// block of the slice (bit i - b0) where a run starts under entry state 0 /
+// 1 (slices are at most 64 blocks).
+__device__ Xfer slice_xfer(const uint64_t *addr, uint32_t L, uint32_t l, uint64_t b0, uint64_t b1,
+                           uint64_t &m0, uint64_t &m1) {
     Xfer x = xfer_identity();
+    m0 = m1 = 0;
     if (b0 >= b1) return x;
     uint64_t p2 = b0 >= 2 ? ld_addr(addr, b0 - 2, L, l) : 0;
     uint64_t p1 = b0 >= 1 ? ld_addr(addr, b0 - 1, L, l) : 0;
@@ -132,8 +136,9 @@ __device__ Xfer slice_xfer(const uint64_t *addr, uint32_t L, uint32_t l, uint64_
             n0 = s0 ^ 1u;
             n1 = s1 ^ 1u;
         }
-        if (n0 == 0) { x.cnt[0]++; x.last[0] = (uint32_t)i; }
-        if (n1 == 0) { x.cnt[1]++; x.last[1] = (uint32_t)i; }
+        const uint64_t bit = 1ull << (i - b0);
+        if (n0 == 0) { x.cnt[0]++; x.last[0] = (uint32_t)i; m0 |= bit; }
+        if (n1 == 0) { x.cnt[1]++; x.last[1] = (uint32_t)i; m1 |= bit; }
         s0 = n0;
         s1 = n1;
         p2 = p1;
@@ -160,10 +165,19 @@ Geometry geometry(uint32_t B, uint32_t L) {
     return g;
 }
 
+// Row tiles per lane above which the lane scan is spread over every warp of
+// the grid, one warp per (lane, chunk of 32 row tiles).
+constexpr uint32_t kTallRows = 64;
+
+__host__ __device__ __forceinline__ uint32_t lane_chunks(const Geometry &g) {
+    return g.ntr > kTallRows ? (g.ntr + 31) / 32 : 0;
+}
+
 struct Ws {
     EncodeCtl *ctl;
     TileRec *tiles;       // [ntr][L]
     uint64_t *tile_runs;  // [ntl]
+    TileRec *chunks;      // [L][lane_chunks]: each chunk's combined effect (tall tables)
 };
 
 Ws carve(void *base, uint32_t B, uint32_t L, size_t *bytes) {
@@ -173,6 +187,7 @@ Ws carve(void *base, uint32_t B, uint32_t L, size_t *bytes) {
     w.ctl = c.take<EncodeCtl>(1);
     w.tile_runs = c.take<uint64_t>(g.ntl);
     w.tiles = c.take<TileRec>((size_t)g.ntr * L);
+    w.chunks = c.take<TileRec>((size_t)L * lane_chunks(g));
     *bytes = c.off;
     return w;
 }
@@ -221,6 +236,7 @@ struct EncodeArgs {
     uint32_t B, L;
     Geometry g;
     TileRec *tiles;
+    TileRec *chunks;
     uint32_t *runs_per_lane;
     uint64_t *tile_runs;
     uint64_t *num_runs;
@@ -231,9 +247,6 @@ struct EncodeArgs {
     EncodeCtl *ctl;
     uint32_t *status;
 };
-
-// Row tiles per lane above which the lane scan takes a whole block per lane.
-constexpr uint32_t kTallRows = 64;
 
 // Scans the effects of row tiles [r_lo, r_hi) of lane l in chunks of 32 (one
 // per lane of the warp), from entry prefix carry: every tile's record is
@@ -263,27 +276,6 @@ __device__ Prefix scan_tile_range(TileRec *tiles, uint32_t L, uint32_t l, uint32
     return carry;
 }
 
-// The combined effect of row tiles [r_lo, r_hi) of lane l (nothing stored).
-__device__ Xfer range_xfer(const TileRec *tiles, uint32_t L, uint32_t l, uint32_t r_lo, uint32_t r_hi,
-                           uint32_t t) {
-    Xfer agg = xfer_identity();
-    for (uint32_t c0 = r_lo; c0 < r_hi; c0 += 32) {
-        const uint32_t r = c0 + t;
-        Xfer x = xfer_identity();
-        if (r < r_hi) {
-            const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(tiles + (uint64_t)r * L + l));
-            x = unpack_xfer(TileRec{v.x, v.y, v.z, v.w});
-        }
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const Xfer o = shfl_up_xfer(x, d);
-            if ((int)t >= d) x = xfer_then(o, x);
-        }
-        agg = xfer_then(agg, shfl_xfer(x, 31));
-    }
-    return agg;
-}
-
 // A lane's run count, and its share of its 32-lane tile's total (zeroed with
 // the control block).
 __device__ __forceinline__ void lane_done(const EncodeArgs &a, uint32_t l, uint32_t runs) {
@@ -294,7 +286,8 @@ __device__ __forceinline__ void lane_done(const EncodeArgs &a, uint32_t l, uint3
 // Six blocks per SM (40 registers): a grid of 912 resident blocks covers the
 // 782 tiles of a 100,000 x 64 table, one tile per block.
 __global__ void __launch_bounds__(kThreads, 6) k_encode(const __grid_constant__ EncodeArgs a) {
-    __shared__ Xfer sx[kRows][32];
+    __shared__ Xfer sx[kRows][32];     // slice effects; kept from phase 1 to 3 when one_tile
+    __shared__ uint64_t sm0[kRows][32], sm1[kRows][32];  // slice run starts (one_tile)
     __shared__ Prefix sp[kRows][32];
     __shared__ uint64_t s_lb[32];
     __shared__ uint64_t s_red[kRows];
@@ -335,14 +328,15 @@ __global__ void __launch_bounds__(kThreads, 6) k_encode(const __grid_constant__ 
 
     // ---- phase 1: each tile's effect on each of its lanes
     const bool one_tile = ntiles <= G;  // every block has at most one tile in phases 1 and 3
-    Xfer my_sx = xfer_identity();
     for (uint32_t tile = blockIdx.x; tile < ntiles; tile += G) {
         const uint32_t tl = tile % g.ntl, tr = tile / g.ntl;
         const uint32_t l = tl * 32 + t;
         const uint64_t b0 = (uint64_t)tr * kRows * g.K + (uint64_t)w * g.K;
         const uint64_t b1 = b0 + g.K < Bv ? b0 + g.K : Bv;
-        my_sx = (l < L && b0 < Bv) ? slice_xfer(a.addr, L, l, b0, b1) : xfer_identity();
-        sx[w][t] = my_sx;
+        uint64_t m0 = 0, m1 = 0;
+        sx[w][t] = (l < L && b0 < Bv) ? slice_xfer(a.addr, L, l, b0, b1, m0, m1) : xfer_identity();
+        sm0[w][t] = m0;
+        sm1[w][t] = m1;
         __syncthreads();
         if (w == 0 && l < L) {
             Xfer acc = sx[0][t];
@@ -357,27 +351,83 @@ __global__ void __launch_bounds__(kThreads, 6) k_encode(const __grid_constant__ 
     }
 
     // ---- phase 2: per lane, a warp-shuffle scan over its tiles' effects.  One
-    // warp per lane; for tall tables (many row tiles, few lanes) one block
-    // per lane, its warps scanning contiguous ranges of the lane's tiles and
-    // chaining through their ranges' totals.
+    // warp per lane; for tall tables (many row tiles, few lanes) one warp
+    // per (lane, chunk of 32 row tiles) over the whole grid: each chunk is
+    // scanned on its own and its total published, then, after a barrier,
+    // every chunk folds the totals of the lane's earlier chunks into its
+    // tiles' entry prefixes.
     if (g.ntr <= kTallRows) {
         for (uint32_t l = blockIdx.x * kRows + w; l < L; l += G * kRows) {
             const Prefix carry = scan_tile_range(a.tiles, L, l, 0, g.ntr, Prefix{0u, 0u, kNone}, t);
             if (t == 0) lane_done(a, l, carry.runs);
         }
     } else {
-        const uint32_t per = (g.ntr + kRows - 1) / kRows;
-        const uint32_t r_lo = w * per < g.ntr ? w * per : g.ntr;
-        const uint32_t r_hi = r_lo + per < g.ntr ? r_lo + per : g.ntr;
-        for (uint32_t l = blockIdx.x; l < L; l += G) {
-            const Xfer agg = range_xfer(a.tiles, L, l, r_lo, r_hi, t);
-            if (t == 0) sx[w][0] = agg;
-            __syncthreads();
-            Prefix carry{0u, 0u, kNone};
-            for (uint32_t i = 0; i < w; i++) carry = prefix_then(carry, sx[i][0]);
-            const Prefix end = scan_tile_range(a.tiles, L, l, r_lo, r_hi, carry, t);
-            if (w == kRows - 1 && t == 0) lane_done(a, l, end.runs);
-            __syncthreads();  // sx is rewritten for the next lane
+        const uint32_t C = lane_chunks(g);
+        const uint64_t tasks = (uint64_t)L * C;
+        const uint64_t gw = (uint64_t)blockIdx.x * kRows + w, nw = (uint64_t)G * kRows;
+        for (uint64_t q = gw; q < tasks; q += nw) {  // each chunk's own scan
+            const uint32_t l = (uint32_t)(q / C), c = (uint32_t)(q % C);
+            const uint32_t r = c * 32 + t;
+            TileRec *slot = a.tiles + (uint64_t)r * L + l;
+            Xfer x = xfer_identity();
+            if (r < g.ntr) {
+                const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(slot));
+                x = unpack_xfer(TileRec{v.x, v.y, v.z, v.w});
+            }
+            Xfer incl = x;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const Xfer o = shfl_up_xfer(incl, d);
+                if ((int)t >= d) incl = xfer_then(o, incl);
+            }
+            Xfer excl = shfl_up_xfer(incl, 1);
+            if (t == 0) excl = xfer_identity();
+            if (r < g.ntr) *slot = pack_xfer(excl);  // the tile's effect-before within its chunk
+            if (t == 31) a.chunks[(uint64_t)l * C + c] = pack_xfer(incl);
+        }
+        if (!grid_barrier(&a.ctl->gs, G)) {
+            if (threadIdx.x == 0) atomicOr(a.status, KVX_S_TIMEOUT);
+            return;
+        }
+        for (uint64_t q = gw; q < tasks; q += nw) {  // fold the earlier chunks in
+            const uint32_t l = (uint32_t)(q / C), c = (uint32_t)(q % C);
+            const uint32_t r = c * 32 + t;
+            TileRec *slot = a.tiles + (uint64_t)r * L + l;
+            const TileRec *tot = a.chunks + (uint64_t)l * C;
+            Xfer e = xfer_identity();
+            if (r < g.ntr) {
+                const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(slot));
+                e = unpack_xfer(TileRec{v.x, v.y, v.z, v.w});
+            }
+            // carry = the lane's prefix before chunk c; end = after chunk c
+            Prefix carry{0u, 0u, kNone}, end{0u, 0u, kNone};
+            for (uint32_t c0 = 0; c0 <= c; c0 += 32) {
+                Xfer x = xfer_identity();
+                if (c0 + t <= c) {
+                    const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(tot + c0 + t));
+                    x = unpack_xfer(TileRec{v.x, v.y, v.z, v.w});
+                }
+                Xfer incl = x;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const Xfer o = shfl_up_xfer(incl, d);
+                    if ((int)t >= d) incl = xfer_then(o, incl);
+                }
+                const uint32_t last = c - c0 < 32 ? c - c0 : 31;  // chunk c, or this group's last
+                end = prefix_then(carry, shfl_xfer(incl, (int)last));
+                if (c - c0 < 32) {
+                    // chunk c is in this group: the prefix before it
+                    const Xfer before = shfl_xfer(incl, last ? (int)last - 1 : 0);
+                    if (last) carry = prefix_then(carry, before);
+                } else {
+                    carry = end;
+                }
+            }
+            if (r < g.ntr) {
+                const Prefix mine = prefix_then(carry, e);
+                *slot = TileRec{mine.state, mine.runs, mine.prev, 0u};
+            }
+            if (c == C - 1 && t == 0) lane_done(a, l, end.runs);
         }
     }
     if (!grid_barrier(&a.ctl->gs, G)) {
@@ -410,7 +460,10 @@ __global__ void __launch_bounds__(kThreads, 6) k_encode(const __grid_constant__ 
         const uint64_t b1 = b0 + g.K < Bv ? b0 + g.K : Bv;
         const bool active = l < L && b0 < Bv;
         // a block with one tile kept its slice's effect from phase 1
-        sx[w][t] = !active ? xfer_identity() : one_tile ? my_sx : slice_xfer(a.addr, L, l, b0, b1);
+        if (!one_tile) {  // a block with one tile kept its slices' effects and starts from phase 1
+            uint64_t m0, m1;
+            sx[w][t] = active ? slice_xfer(a.addr, L, l, b0, b1, m0, m1) : xfer_identity();
+        }
         __syncthreads();
         if (w == 0 && l < L) {
             const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(a.tiles + (uint64_t)tr * L + l));
@@ -424,35 +477,52 @@ __global__ void __launch_bounds__(kThreads, 6) k_encode(const __grid_constant__ 
         if (active) {
             const Prefix p = sp[w][t];
             const uint64_t lb = s_lb[t];
-            uint64_t p2 = b0 >= 2 ? ld_addr(a.addr, b0 - 2, L, l) : 0;
-            uint64_t p1 = b0 >= 1 ? ld_addr(a.addr, b0 - 1, L, l) : 0;
-            uint64_t av = ld_addr(a.addr, b0, L, l);
-            uint32_t s = p.state;
             uint32_t runs = p.runs;
             uint32_t prev = p.prev;
-            for (uint64_t i = b0; i < b1; i++) {
-                const uint64_t nx = i + 1 < Bv ? ld_addr(a.addr, i + 1, L, l) : 0;
-                uint32_t n;
-                if (i == 0)
-                    n = 0;
-                else if (i == 1 || av - p1 == p1 - p2)
-                    n = 1;
-                else
-                    n = s ^ 1u;
-                if (n == 0) {
-                    const uint64_t idx = lb + runs;
-                    if (idx < a.run_cap) {  // always true: runs per lane <= ceil(B/2)
-                        a.run_base[idx] = av;
-                        a.run_stride[idx] = i + 1 < Bv ? (int64_t)(nx - av) : 0;
-                    }
-                    if (prev != kNone && idx - 1 < a.run_cap) a.run_count[idx - 1] = (uint32_t)(i - prev);
-                    prev = (uint32_t)i;
-                    runs++;
+            // a run starting at block i: its base and stride, and the block
+            // count of the run before it
+            auto emit = [&](uint64_t i, uint64_t av, uint64_t nx) {
+                const uint64_t idx = lb + runs;
+                if (idx < a.run_cap) {  // always true: runs per lane <= ceil(B/2)
+                    a.run_base[idx] = av;
+                    a.run_stride[idx] = i + 1 < Bv ? (int64_t)(nx - av) : 0;
                 }
-                s = n;
-                p2 = p1;
-                p1 = av;
-                av = nx;
+                if (prev != kNone && idx - 1 < a.run_cap) a.run_count[idx - 1] = (uint32_t)(i - prev);
+                prev = (uint32_t)i;
+                runs++;
+            };
+            if (one_tile) {
+                // the starts phase 1 found under this slice's entry state:
+                // only their addresses (and the next ones, for the stride)
+                // are read again
+                uint64_t m = p.state ? sm1[w][t] : sm0[w][t];
+                while (m) {
+                    const uint64_t i = b0 + (uint64_t)(__ffsll((long long)m) - 1);
+                    m &= m - 1;
+                    const uint64_t av = ld_addr(a.addr, i, L, l);
+                    const uint64_t nx = i + 1 < Bv ? ld_addr(a.addr, i + 1, L, l) : 0;
+                    emit(i, av, nx);
+                }
+            } else {
+                uint64_t p2 = b0 >= 2 ? ld_addr(a.addr, b0 - 2, L, l) : 0;
+                uint64_t p1 = b0 >= 1 ? ld_addr(a.addr, b0 - 1, L, l) : 0;
+                uint64_t av = ld_addr(a.addr, b0, L, l);
+                uint32_t s = p.state;
+                for (uint64_t i = b0; i < b1; i++) {
+                    const uint64_t nx = i + 1 < Bv ? ld_addr(a.addr, i + 1, L, l) : 0;
+                    uint32_t n;
+                    if (i == 0)
+                        n = 0;
+                    else if (i == 1 || av - p1 == p1 - p2)
+                        n = 1;
+                    else
+                        n = s ^ 1u;
+                    if (n == 0) emit(i, av, nx);
+                    s = n;
+                    p2 = p1;
+                    p1 = av;
+                    av = nx;
+                }
             }
             if (b1 == Bv && lb + runs - 1 < a.run_cap) a.run_count[lb + runs - 1] = (uint32_t)(Bv - prev);
         }
@@ -519,6 +589,7 @@ kvx_status launch_encode(const uint64_t *addr, const uint32_t *seg_size, const u
     a.L = L;
     a.g = g;
     a.tiles = w.tiles;
+    a.chunks = w.chunks;
     a.runs_per_lane = runs_per_lane;
     a.tile_runs = w.tile_runs;
     a.num_runs = num_runs;
