@@ -13,10 +13,11 @@
 //            digits, one barrier each; equal keys keep run order = (lane,
 //            first block) order
 //   adjacent step 3: sorted records; compat(p) = same node, first block,
-//            count and stride as p-1 and base-adjacent to it
-//   cut      step 3: group starts, with the "grown chunk still fits the
-//            stride" cut inside a compatible stretch
-//   count    group numbering
+//   + cut    count and stride as p-1 and base-adjacent to it; group starts,
+//            with the "grown chunk still fits the stride" cut inside a
+//            compatible stretch; per tile the number of group starts
+//   cut,     only when some stretch outgrows its stride: the cut again with
+//   count    walks along such stretches in order, then the counts again
 //   groups   group records, run_group / run_off, bytes and read pieces
 //   emit     step 4: slab carve (groups back to back) and descriptors (one
 //            per dense group / per block, split at 32 MiB)
@@ -45,11 +46,16 @@ constexpr int kIPT = 8;
 constexpr uint32_t kTile = kT * kIPT;
 constexpr uint64_t kSmallTiles = 256;
 constexpr uint32_t kDigits = 256;
+// Radix histograms are also kept summed over groups of this many tiles, so a
+// tile's digit offsets take the groups before its own plus at most
+// kHistGroup - 1 tiles of its own group, instead of every earlier tile.
+constexpr uint32_t kHistGroup = 16;
 
 struct PlanCtl {
     GridSync gs;
     uint32_t fail;
     uint32_t st;
+    uint32_t walked;  // a stretch walker of the cut phase set flags beyond its own position
     unsigned long long or_base, and_base;
     uint32_t or_node, and_node;
     uint32_t or_empty, and_empty;  // some / every run has a zero-size segment
@@ -138,7 +144,8 @@ struct PlanArgs {
     uint32_t *run_lane;
     Seg *seg;
     SortItem *items0, *items1;
-    uint32_t *hist[3];
+    uint32_t *hist[3];   // [tile][digit]
+    uint32_t *ghist[3];  // [tile group][digit]: the same counts summed over groups of kHistGroup tiles
     Rec *rec;
     uint8_t *compat;
     uint8_t *gflag;
@@ -242,6 +249,34 @@ __device__ __forceinline__ uint32_t digit_of(uint64_t base, uint32_t node, uint3
     if (dig < 8) return (uint32_t)(base >> (8 * dig)) & 0xFFu;
     if (dig == kEmptyDigit) return empty;
     return (node >> (8 * (dig - 8))) & 0xFFu;
+}
+
+// Lanes of the warp whose digit equals this lane's (digits below kDigits;
+// a lane holding kDigits or more matches nobody and gets no meaningful
+// mask): one ballot per digit bit, so the cost does not grow with the number
+// of distinct digits in the warp (random keys have nearly 32).
+__device__ __forceinline__ uint32_t digit_peers(uint32_t d) {
+    uint32_t m = __ballot_sync(0xFFFFFFFFu, d < kDigits);
+#pragma unroll
+    for (int b = 0; b < 8; b++) {
+        const uint32_t bit = (d >> b) & 1u;
+        const uint32_t bb = __ballot_sync(0xFFFFFFFFu, bit);
+        m &= bit ? bb : ~bb;
+    }
+    return m;
+}
+
+// H[key] += 1 for every lane whose key is not ~0u, with one atomic per run of
+// equal keys in consecutive lanes (sorted or structured keys come in runs;
+// random ones cost one atomic each, without a matching step).
+__device__ __forceinline__ void add_key_runs(uint32_t *H, uint32_t key, uint32_t lane) {
+    const uint32_t prev = __shfl_up_sync(0xFFFFFFFFu, key, 1);
+    const uint32_t bnd = __ballot_sync(0xFFFFFFFFu, lane == 0 || prev != key);
+    if (key != ~0u && (bnd >> lane & 1u)) {
+        const uint32_t after = bnd & ~((2u << lane) - 1u);  // run boundaries after this lane
+        const uint32_t next = after ? (uint32_t)__ffs((int)after) - 1u : 32u;
+        atomicAdd(&H[key], next - lane);
+    }
 }
 
 // The radix passes for keys whose bits differ as in db (base), de (empty), dn
@@ -431,6 +466,12 @@ __device__ void phase_decode(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
         s_andn = ~0u;
     }
     __syncthreads();
+    {   // the keys phase sums its first histogram into ghist[0]
+        const uint64_t n = (uint64_t)kDigits * ceil_div((uint64_t)nt, (uint64_t)kHistGroup);
+        for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+             i += (uint64_t)P * blockDim.x)
+            a.ghist[0][i] = 0;
+    }
     uint32_t bits = 0;
     unsigned long long o = 0, an = ~0ull;
     uint32_t on = 0, ann = ~0u, oe = 0, ae = 1;
@@ -589,22 +630,26 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
 #pragma unroll
             for (int j = 0; j < IPT; j++) {
                 const uint64_t r = r0 + j;
-                const uint32_t d = r < R ? digit_of(bases[j], nodes[j], empty[j], dig0) : kDigits;
-                const uint32_t peers = __match_any_sync(0xFFFFFFFFu, d);
-                if (d < kDigits && (threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1))
-                    atomicAdd(&s_hist[d], __popc(peers));
+                const uint32_t d = r < R ? digit_of(bases[j], nodes[j], empty[j], dig0) : ~0u;
+                add_key_runs(s_hist, d, threadIdx.x & 31);
             }
             __syncthreads();
-            for (uint32_t d = threadIdx.x; d < kDigits; d += blockDim.x)
-                a.hist[0][(uint64_t)tile * kDigits + d] = s_hist[d];
+            for (uint32_t d = threadIdx.x; d < kDigits; d += blockDim.x) {
+                const uint32_t c = s_hist[d];
+                a.hist[0][(uint64_t)tile * kDigits + d] = c;
+                if (c) atomicAdd(&a.ghist[0][(uint64_t)(tile / kHistGroup) * kDigits + d], c);
+            }
         }
         __syncthreads();
     }
-    if (nact > 1) {  // pass 0 accumulates the next digit's histogram here
+    if (nact > 1) {  // pass 0 accumulates the next digit's histograms here
         const uint64_t n = (uint64_t)kDigits * nt;
+        const uint64_t ng = (uint64_t)kDigits * ceil_div((uint64_t)nt, (uint64_t)kHistGroup);
         for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-             i += (uint64_t)P * blockDim.x)
+             i += (uint64_t)P * blockDim.x) {
             a.hist[1][i] = 0;
+            if (i < ng) a.ghist[1][i] = 0;
+        }
     }
     bits = __reduce_or_sync(0xFFFFFFFFu, bits);
     if ((threadIdx.x & 31) == 0 && bits) atomicOr(&s_bits, bits);
@@ -632,42 +677,60 @@ constexpr int kSweep = 32;         // histogram rows loaded at once in the offse
 template <int IPT>
 __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P,
                                 const SortItem *in, SortItem *out, const uint32_t *H,
-                                uint32_t *Hn, uint32_t *Hz, uint32_t dig, bool has_next,
-                                uint32_t ndig, bool clear_z, SortCounters &sc) {
+                                uint32_t *Hn, uint32_t *Hz, const uint32_t *G, uint32_t *Gn,
+                                uint32_t *Gz, uint32_t dig, bool has_next, uint32_t ndig,
+                                bool clear_z, SortCounters &sc) {
     uint32_t (*wcnt)[kDigits] = sc.wcnt;
     uint32_t (*s_off)[kDigits] = sc.s_off;
     uint32_t *s_base = sc.s_base;
     __shared__ uint64_t sh[33];
     static_assert(kT == kDigits, "one thread per digit");
+    const uint32_t ng = (nt + kHistGroup - 1) / kHistGroup;
     if (clear_z) {
         const uint64_t n = (uint64_t)kDigits * nt;
         for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-             i += (uint64_t)P * blockDim.x)
+             i += (uint64_t)P * blockDim.x) {
             Hz[i] = 0;
+            if (i < (uint64_t)kDigits * ng) Gz[i] = 0;
+        }
     }
     const uint32_t d_me = threadIdx.x;
     const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const uint32_t lt_mask = (1u << lane) - 1u;
     const uint32_t own = nt > blockIdx.x ? (nt - blockIdx.x + P - 1) / P : 0;
     for (uint32_t c0 = 0; c0 < own; c0 += kOwnChunk) {
-        // sweep: running count of digit d_me before each own tile of this chunk
+        const uint32_t nslot = own - c0 < kOwnChunk ? own - c0 : kOwnChunk;
+        // the count of digit d_me in the tile groups before each own tile's
+        // group (and, after the sweep, its total): kSweep group rows in
+        // flight per thread
         uint64_t run = 0;
         uint32_t next_slot = 0;
-        uint32_t next_tile = blockIdx.x + c0 * P;
-        for (uint32_t t = 0; t < nt; t += kSweep) {  // kSweep rows in flight per thread
+        for (uint32_t g0 = 0; g0 < ng; g0 += kSweep) {
             uint32_t v[kSweep];
 #pragma unroll
             for (int u = 0; u < kSweep; u++)
-                v[u] = t + u < nt ? __ldcg(H + (uint64_t)(t + u) * kDigits + d_me) : 0;
+                v[u] = g0 + u < ng ? __ldcg(G + (uint64_t)(g0 + u) * kDigits + d_me) : 0;
 #pragma unroll
             for (int u = 0; u < kSweep; u++) {
-                if (t + u == next_tile && next_slot < kOwnChunk && c0 + next_slot < own) {
+                while (next_slot < nslot && (blockIdx.x + (c0 + next_slot) * P) / kHistGroup == g0 + u) {
                     s_off[next_slot][d_me] = (uint32_t)run;
                     next_slot++;
-                    next_tile += P;
                 }
                 run += v[u];
             }
+        }
+        // plus the tiles of each own tile's group that come before it
+        for (uint32_t slot = 0; slot < nslot; slot++) {
+            const uint32_t tile = blockIdx.x + (c0 + slot) * P;
+            const uint32_t t0 = tile - tile % kHistGroup;
+            uint32_t v[kHistGroup - 1];
+#pragma unroll
+            for (int u = 0; u < (int)kHistGroup - 1; u++)
+                v[u] = t0 + u < tile ? __ldcg(H + (uint64_t)(t0 + u) * kDigits + d_me) : 0;
+            uint32_t sum = 0;
+#pragma unroll
+            for (int u = 0; u < (int)kHistGroup - 1; u++) sum += v[u];
+            s_off[slot][d_me] += sum;
         }
         {   // digit bases = exclusive scan of the digit totals
             uint64_t tot;
@@ -694,7 +757,7 @@ __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint
             }
 #pragma unroll
             for (int j = 0; j < IPT; j++) {
-                const uint32_t peers = __match_any_sync(0xFFFFFFFFu, d[j]);
+                const uint32_t peers = digit_peers(d[j]);
                 const uint32_t rank = __popc(peers & lt_mask);
                 const uint32_t before = d[j] < kDigits ? wcnt[w][d[j]] : 0;
                 __syncwarp();
@@ -714,18 +777,20 @@ __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint
             __syncthreads();
 #pragma unroll
             for (int j = 0; j < IPT; j++) {
-                uint64_t key = ~0ull;  // next-histogram bin of this item
+                uint32_t key = ~0u;  // next-histogram bin of this item (output tile, next digit)
                 if (d[j] < kDigits) {
                     const uint64_t dst = (uint64_t)s_base[d[j]] + s_off[slot][d[j]] + wcnt[w][d[j]] + pos[j];
                     if (dst < R) {  // always: the offsets are a permutation of [0, R)
                         out[dst] = it[j];
                         if (has_next)
-                            key = (dst / (kT * IPT)) * kDigits + digit_of(it[j].base, it[j].node, it[j].r >> 31, ndig);
+                            key = (uint32_t)(dst / (kT * IPT)) * kDigits +
+                                  digit_of(it[j].base, it[j].node, it[j].r >> 31, ndig);
                     }
                 }
-                if (has_next) {  // one atomic per distinct bin in the warp
-                    const uint32_t peers = __match_any_sync(0xFFFFFFFFu, key);
-                    if (key != ~0ull && lane == (uint32_t)(__ffs(peers) - 1)) atomicAdd(&Hn[key], __popc(peers));
+                if (has_next) {  // per tile, and per group of kHistGroup tiles
+                    add_key_runs(Hn, key, lane);
+                    add_key_runs(Gn, key == ~0u ? ~0u : (key / kDigits / kHistGroup) * kDigits + key % kDigits,
+                                 lane);
                 }
             }
             __syncthreads();
@@ -748,13 +813,56 @@ __device__ __forceinline__ Rec make_rec(const PlanArgs &a, SortItem it, uint64_t
     return x;
 }
 
-// Step 3: sorted records and compat flags; per tile, its last stretch start.
+// The base of the run that starts the compatible stretch holding sorted
+// position p (known to be compatible with p - 1), by the whole block: it
+// walks back over the sorted order kT positions at a time, each thread
+// testing one position against its predecessor, to the last position that
+// is not compatible with its predecessor.  A stretch joins runs of one block
+// range and stride at adjacent bases, so it is a few rounds long at most.
+__device__ uint64_t stretch_base(const PlanArgs &a, uint64_t R, const SortItem *sorted, uint64_t p,
+                                 int64_t *s_max, uint64_t *s_found) {
+    for (uint64_t hi = p; hi > 0; hi = hi > kT ? hi - kT : 0) {
+        const int64_t q = (int64_t)hi - (int64_t)kT + (int64_t)threadIdx.x;
+        bool start = false;
+        uint64_t base = 0;
+        if (q >= 0) {
+            const Rec x = make_rec(a, ld_cg(sorted + q), R);
+            base = x.base;
+            start = q == 0 || !compatible(make_rec(a, ld_cg(sorted + q - 1), R), x);
+        }
+        if (threadIdx.x == 0) *s_max = -1;
+        __syncthreads();
+        if (start) atomicMax(reinterpret_cast<long long *>(s_max), (long long)q);
+        __syncthreads();
+        const int64_t last = *s_max;
+        if (last >= 0) {
+            if (q == last) *s_found = base;
+            __syncthreads();
+            return *s_found;
+        }
+    }
+    return 0;  // never reached: position 0 starts a stretch
+}
+
+// Step 3, adjacency and group starts in one phase: the sorted records and
+// compat flags (as the groups phase and a stretch walk need them), then the
+// "grown chunk still fits the stride" cut from the bases of each stretch's
+// first run, taken from shared memory inside the tile and by a look-back for
+// the stretch open at the tile's start.  Runs whose stretch outgrows its
+// stride need a walk in order across positions other blocks are still
+// writing; they are left to the separate cut phase (ctl->walked), which then
+// runs after the barrier.  Per tile: the last stretch start and the group
+// starts (for the groups phase).
 template <int IPT>
-__device__ void phase_adjacent(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P,
-                               const SortItem *sorted, ScanSmem &sm) {
+__device__ void phase_adjacent_cut(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P,
+                                   const SortItem *sorted, ScanSmem &sm, uint64_t *s_tbase) {
+    __shared__ uint64_t s_open;  // base of the first run of the stretch open at the tile's start
+    __shared__ uint32_t s_need;
+    __shared__ int64_t s_lmax;
+    __shared__ uint64_t s_lbase;
+    const uint64_t T = (uint64_t)kT * IPT;
     for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
-        int64_t mx = -1;
-        const uint64_t p0 = (uint64_t)tile * (kT * IPT) + (uint64_t)threadIdx.x * IPT;
+        const uint64_t p0 = (uint64_t)tile * T + (uint64_t)threadIdx.x * IPT;
         Rec prev;
         bool have_prev = false;
         if (p0 > 0 && p0 < R) {
@@ -771,20 +879,22 @@ __device__ void phase_adjacent(const PlanArgs &a, uint64_t R, uint32_t nt, uint3
                 if (its[j].r >= R) its[j].r = 0;  // never taken: a permutation of the runs
             }
         }
-        int64_t strides[IPT];
-        uint32_t counts[IPT], blocks[IPT], lanes[IPT], lens[IPT];
+        int64_t xs[IPT];
+        uint32_t xc[IPT], blocks[IPT], lanes[IPT], xl[IPT];
 #pragma unroll
         for (int j = 0; j < IPT; j++) {
             if (p0 + j >= R) continue;
             const uint32_t r = its[j].r;
-            strides[j] = a.run_stride[r];
-            counts[j] = a.run_count[r];
+            xs[j] = a.run_stride[r];
+            xc[j] = a.run_count[r];
             blocks[j] = __ldcg(a.run_block + r);
             lanes[j] = __ldcg(a.run_lane + r);
         }
 #pragma unroll
         for (int j = 0; j < IPT; j++)
-            if (p0 + j < R) lens[j] = __ldg(a.seg_len + lanes[j]);
+            if (p0 + j < R) xl[j] = __ldg(a.seg_len + lanes[j]);
+        int64_t mx = -1;
+        uint32_t cm = 0;  // bit j: position p0 + j is compatible with its predecessor
 #pragma unroll
         for (int j = 0; j < IPT; j++) {
             const uint64_t p = p0 + j;
@@ -793,21 +903,89 @@ __device__ void phase_adjacent(const PlanArgs &a, uint64_t R, uint32_t nt, uint3
             x.base = its[j].base;
             x.node = its[j].node;
             x.r = its[j].r;
-            x.stride = strides[j];
-            x.count = counts[j];
+            x.stride = xs[j];
+            x.count = xc[j];
             x.block = blocks[j];
-            x.len = lens[j];
+            x.len = xl[j];
             x.pad = 0;
             a.rec[p] = x;
+            s_tbase[p - (uint64_t)tile * T] = x.base;
             const bool c = have_prev && compatible(prev, x);
             a.compat[p] = c ? 1 : 0;
-            if (!c) mx = (int64_t)p;
+            if (c) cm |= 1u << j;
+            else mx = (int64_t)p;
             prev = x;
             have_prev = true;
         }
         int64_t ex, tot;
         block_scan(mx, MaxOp(), (int64_t)-1, sm.i64, &ex, &tot);
         if (threadIdx.x == 0) a.segmax[tile] = tot;
+        // The stretch open at the tile's first position, if it began in an
+        // earlier tile: its first run's base is needed only when its runs
+        // could share a group (more than one block and a positive stride;
+        // every run of a stretch has the same count and stride).
+        if (threadIdx.x == 0)
+            s_need = p0 < R && (cm & 1u) && xc[0] > 1 && xs[0] > 0 ? 1u : 0u;
+        __syncthreads();  // s_tbase complete, s_need set
+        if (s_need) {
+            const uint64_t b = stretch_base(a, R, sorted, (uint64_t)tile * T, &s_lmax, &s_lbase);
+            if (threadIdx.x == 0) s_open = b;
+            __syncthreads();
+        }
+        uint64_t s_base = 0;  // base of the current stretch's first run
+        if (p0 < R && (cm & 1u)) s_base = ex >= 0 ? s_tbase[(uint64_t)ex - (uint64_t)tile * T] : s_open;
+        GAgg g{0, -1};
+        bool walker = false;
+#pragma unroll
+        for (int j = 0; j < IPT; j++) {
+            const uint64_t p = p0 + j;
+            if (p >= R) break;
+            const bool c = cm >> j & 1u;
+            const uint64_t xb = its[j].base;
+            if (!c) s_base = xb;
+            bool start;
+            if (xc[j] == 1) {
+                start = !c;
+            } else if (xs[j] <= 0) {
+                start = true;  // a non-positive stride never fits: one run per group
+            } else {
+                const uint64_t E = xb - s_base + xl[j];  // end of the run in its stretch
+                if (E > (uint64_t)xs[j]) {  // the stretch outgrows its stride: the cut phase walks it
+                    walker = true;
+                    continue;
+                }
+                start = !c;
+            }
+            a.gflag[p] = start ? 1 : 0;
+            if (start) {
+                g.n++;
+                g.last = (int64_t)p;
+            }
+        }
+        GAgg gex, gtot;
+        block_scan(g, GOp(), GAgg{0, -1}, sm.g, &gex, &gtot);
+        if (threadIdx.x == 0) a.gagg[tile] = gtot;
+        if (__any_sync(0xFFFFFFFFu, walker) && (threadIdx.x & 31) == 0) atomicOr(&a.ctl->walked, 1u);
+        __syncthreads();  // s_tbase is rewritten by the next tile
+    }
+}
+
+// The run at position p outgrows the first group of its compatible stretch
+// (its chunk exceeds the stride): it starts a group, and the rest of the
+// stretch is cut in order, a new group wherever the chunk would outgrow the
+// stride again (only tables whose block chunks exceed their stride get here).
+__device__ __noinline__ void walk_stretch(const PlanArgs &a, uint64_t R, uint64_t p, uint64_t base,
+                                          uint64_t stride) {
+    a.gflag[p] = 1;
+    uint64_t cur = base;
+    for (uint64_t q = p + 1; q < R && __ldcg(a.compat + q); q++) {
+        const Rec y = ld_cg(a.rec + q);
+        if (y.base + y.len - cur > stride) {
+            a.gflag[q] = 1;
+            cur = y.base;
+        } else {
+            a.gflag[q] = 0;
+        }
     }
 }
 
@@ -843,43 +1021,46 @@ __device__ void phase_cut(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P
         const int64_t s0 = carry > ex ? carry : ex;  // stretch start before this thread's first run
         uint64_t s_base = 0;                          // base of the current stretch's first run
         if (p0 < R && (cm & 1u)) s_base = __ldcg(&a.rec[s0 > 0 ? s0 : 0].base);
+        // the tile's group starts, for the groups phase (valid when no
+        // walker ran anywhere: then every flag was set by its own position)
+        GAgg g{0, -1};
+        bool walker = false;
 #pragma unroll
         for (int j = 0; j < IPT; j++) {
             const uint64_t p = p0 + j;
             if (p >= R) break;
             const bool c = cm >> j & 1u;
             if (!c) s_base = xb[j];
+            bool start;
             if (xc[j] == 1) {
-                a.gflag[p] = c ? 0 : 1;
-                continue;
-            }
-            if (xs[j] <= 0) {
-                a.gflag[p] = 1;  // a non-positive stride never fits: one run per group
-                continue;
-            }
-            const uint64_t stride = (uint64_t)xs[j];
-            const uint64_t O = xb[j] - s_base;  // offset in the stretch
-            const uint64_t E = O + xl[j];
-            if (E <= stride) {
-                a.gflag[p] = c ? 0 : 1;
-            } else if (O <= stride) {
-                // First run that outgrows the stretch's first group: walk the
-                // rest of the stretch in order (only tables whose block chunks
-                // exceed their stride get here).
-                a.gflag[p] = 1;
-                uint64_t cur = xb[j];
-                for (uint64_t q = p + 1; q < R && __ldcg(a.compat + q); q++) {
-                    const Rec y = ld_cg(a.rec + q);
-                    if (y.base + y.len - cur > stride) {
-                        a.gflag[q] = 1;
-                        cur = y.base;
-                    } else {
-                        a.gflag[q] = 0;
-                    }
+                start = !c;
+            } else if (xs[j] <= 0) {
+                start = true;  // a non-positive stride never fits: one run per group
+            } else {
+                const uint64_t stride = (uint64_t)xs[j];
+                const uint64_t O = xb[j] - s_base;  // offset in the stretch
+                const uint64_t E = O + xl[j];
+                if (E <= stride) {
+                    start = !c;
+                } else {
+                    // O <= stride: the first run that outgrows the stretch's
+                    // first group walks the rest of the stretch; O > stride:
+                    // a later run of such a stretch, flagged by that walker
+                    walker = true;
+                    if (O <= stride) walk_stretch(a, R, p, xb[j], stride);
+                    continue;
                 }
             }
-            // else: written by the walker of this stretch
+            a.gflag[p] = start ? 1 : 0;
+            if (start) {
+                g.n++;
+                g.last = (int64_t)p;
+            }
         }
+        GAgg gex, gtot;
+        block_scan(g, GOp(), GAgg{0, -1}, sm.g, &gex, &gtot);
+        if (threadIdx.x == 0) a.gagg[tile] = gtot;
+        if (__any_sync(0xFFFFFFFFu, walker) && (threadIdx.x & 31) == 0) atomicOr(&a.ctl->walked, 1u);
     }
 }
 
@@ -1163,6 +1344,12 @@ __global__ void __launch_bounds__(kST, 1) k_plan_small(const __grid_constant__ P
     __shared__ uint32_t s_bits;
     __shared__ unsigned long long s_or, s_and;
     __shared__ uint32_t s_orn, s_andn, s_ore, s_ande;
+    // This kernel always runs just before k_plan on the same stream, so it
+    // clears k_plan's control block (barrier counter, flags) for it: one
+    // operation fewer per plan than a separate memset.
+    static_assert(sizeof(PlanCtl) % 4 == 0, "cleared in 4-byte words");
+    for (uint32_t i = threadIdx.x; i < sizeof(PlanCtl) / 4; i += blockDim.x)
+        reinterpret_cast<uint32_t *>(a.ctl)[i] = 0;
     const uint64_t R = *a.num_runs;
     if (!plan_is_small(a, R)) return;
     const uint32_t tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -1350,7 +1537,7 @@ __global__ void __launch_bounds__(kST, 1) k_plan_small(const __grid_constant__ P
         }
 #pragma unroll
         for (int j = 0; j < 2; j++) {
-            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, d[j]);
+            const uint32_t peers = digit_peers(d[j]);
             const uint32_t rank = __popc(peers & lt_mask);
             const uint32_t before = d[j] < kDigits ? S.wcnt[w][d[j]] : 0;
             __syncwarp();
@@ -1548,6 +1735,7 @@ struct KeyStage {
 union PlanStages {
     KeyStage keys;
     SortCounters sort;
+    uint64_t tile_base[kTile];  // the adjacent-cut phase: bases of the tile's sorted runs
 };
 
 // Every phase over tiles of kT * IPT runs.  The shared memory is the
@@ -1578,18 +1766,23 @@ __device__ void plan_tiles(const PlanArgs &a, uint64_t R_in, uint64_t R, ScanSme
         SortItem *out = (k & 1) ? a.items0 : a.items1;
         const bool has_next = k + 1 < nact;
         phase_sort_pass<IPT>(a, R, nt, P, in, out, a.hist[k % 3], a.hist[(k + 1) % 3],
-                        a.hist[(k + 2) % 3], s_act[k], has_next, has_next ? s_act[k + 1] : 0,
-                        k + 2 < nact, st.sort);
+                             a.hist[(k + 2) % 3], a.ghist[k % 3], a.ghist[(k + 1) % 3],
+                             a.ghist[(k + 2) % 3], s_act[k], has_next, has_next ? s_act[k + 1] : 0,
+                             k + 2 < nact, st.sort);
         PLAN_BARRIER();
     }
     const SortItem *sorted = (nact & 1) ? a.items1 : a.items0;
 
-    phase_adjacent<IPT>(a, R, nt, P, sorted, sm);
+    phase_adjacent_cut<IPT>(a, R, nt, P, sorted, sm, st.tile_base);
     PLAN_BARRIER();
-    phase_cut<IPT>(a, R, nt, P, sm);
-    PLAN_BARRIER();
-    phase_count<IPT>(a, R, nt, P, sm);
-    PLAN_BARRIER();
+    if (__ldcg(&a.ctl->walked)) {
+        // some stretch outgrows its stride: cut again with the walks (in
+        // order along the stretch), then count every tile
+        phase_cut<IPT>(a, R, nt, P, sm);
+        PLAN_BARRIER();
+        phase_count<IPT>(a, R, nt, P, sm);
+        PLAN_BARRIER();
+    }
     const GAgg gall = reduce_prefix(a.gagg, nt, GOp(), GAgg{0, -1}, sm.g);
     if (gall.n > a.group_cap) {
         if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -1661,6 +1854,7 @@ struct Ws {
     Seg *seg;
     SortItem *items[2];
     uint32_t *hist[3];
+    uint32_t *ghist[3];
     Rec *rec;
     uint8_t *compat;
     uint8_t *gflag;
@@ -1688,6 +1882,7 @@ Ws carve(void *base, uint64_t run_cap, size_t *bytes) {
     w.items[0] = c.take<SortItem>(run_cap);
     w.items[1] = c.take<SortItem>(run_cap);
     for (int i = 0; i < 3; i++) w.hist[i] = c.take<uint32_t>(kDigits * ntc);
+    for (int i = 0; i < 3; i++) w.ghist[i] = c.take<uint32_t>(kDigits * ceil_div(ntc, (uint64_t)kHistGroup));
     w.rec = c.take<Rec>(run_cap);
     w.compat = c.take<uint8_t>(run_cap);
     w.gflag = c.take<uint8_t>(run_cap + 1);
@@ -1791,7 +1986,10 @@ extern "C" kvx_status kvx_plan_groups(const uint32_t *runs_per_lane, uint32_t ta
     a.seg = w.seg;
     a.items0 = w.items[0];
     a.items1 = w.items[1];
-    for (int i = 0; i < 3; i++) a.hist[i] = w.hist[i];
+    for (int i = 0; i < 3; i++) {
+        a.hist[i] = w.hist[i];
+        a.ghist[i] = w.ghist[i];
+    }
     a.rec = w.rec;
     a.compat = w.compat;
     a.gflag = w.gflag;
@@ -1810,9 +2008,8 @@ extern "C" kvx_status kvx_plan_groups(const uint32_t *runs_per_lane, uint32_t ta
             return KVX_ECUDA;
         small_ready[dev] = true;
     }
-    k_plan_small<<<1, kST, sizeof(SmallSmem), s>>>(a);
+    k_plan_small<<<1, kST, sizeof(SmallSmem), s>>>(a);  // also clears k_plan's control block
     KVX_LAUNCHED();
-    if (cudaMemsetAsync(w.ctl, 0, sizeof(PlanCtl), s) != cudaSuccess) return KVX_ECUDA;
     const uint64_t ntc = tile_cap(run_capacity);
     const int maxb = plan_max_blocks();
     const unsigned grid = (unsigned)(ntc < (uint64_t)maxb ? ntc : (uint64_t)maxb);
