@@ -49,7 +49,7 @@ constexpr uint32_t kDigits = 256;
 // Radix histograms are also kept summed over groups of this many tiles, so a
 // tile's digit offsets take the groups before its own plus at most
 // kHistGroup - 1 tiles of its own group, instead of every earlier tile.
-constexpr uint32_t kHistGroup = 16;
+constexpr uint32_t kHistGroup = 8;
 
 struct PlanCtl {
     GridSync gs;
