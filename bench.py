@@ -846,8 +846,12 @@ def measure_next(name, args, dev, cpu_seconds):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
             "data": "synthetic", "e2e": None}
 
+    # a reduced case for profiler captures (seal and paged only)
+    reduced = args.blocks != 1000 and args.workload == name and name in ("seal", "paged")
     if name == "paged":
-        wl = W.paged_default()
+        # full size: 576,000 pages; reduced: 576 pages per block of --blocks
+        wl = W.paged("paged", 576 * args.blocks, 4096, 720 * args.blocks, 640 * args.blocks,
+                     seed=6) if reduced else W.paged_default()
         src = torch.empty(wl.src_bytes, dtype=torch.uint8, device=dev)
         W.fill_pool_torch(src, wl.seed)
         dst = torch.full((wl.dst_bytes,), W.CANARY, dtype=torch.uint8, device=dev)
@@ -891,7 +895,7 @@ def measure_next(name, args, dev, cpu_seconds):
         def status_ok():
             return int(status.item()) == 0
     elif name == "seal":
-        wl = W.default()
+        wl = make_workload("default", args.blocks if reduced else 1000)
         tr = kvx.Transfer(wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes, device=dev)
         tr.set_addr(wl.addr)
         pool = torch.empty(wl.pool_bytes, dtype=torch.uint8, device=dev)
@@ -1000,6 +1004,8 @@ def measure_next(name, args, dev, cpu_seconds):
     else:
         value = N * K / (ms / 1e3) / 1e6
         line.update({"value": value, "unit": "Msegments/s", "roofline": None})
+    if reduced:
+        cfg = "reduced for profiling: %s with %d blocks (%s)" % (name, args.blocks, cfg)
     line.update({"ms_per_step": per_ms, "gpu_launches": int(launches), "clocks": clocks,
                  "launch_mode": "stream",
                  "config": {"workload": cfg, "l2": "inputs larger than L2, no flush"
