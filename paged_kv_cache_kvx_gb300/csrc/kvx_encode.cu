@@ -30,7 +30,6 @@ namespace {
 
 constexpr int kRows = 8;           // warps per CTA = row slices per tile
 constexpr int kThreads = 32 * kRows;
-constexpr uint32_t kTargetCtas = 1024;
 
 // Effect of a slice on the greedy state, for entry state 0 (START) or 1 (IN).
 struct Xfer {
@@ -155,13 +154,31 @@ struct Geometry {
     uint32_t ntr;   // row tiles (kRows * K blocks each)
 };
 
-Geometry geometry(uint32_t B, uint32_t L) {
+// The launch geometry: slices of K blocks, K chosen so that the tiles fill at
+// most kTilesPerSm blocks on every SM (phases 1 and 3 then end together on
+// every SM; an SM with one block more than the others sets the pace), K at
+// least kMinK and at most 64 (a slice's run starts fit one 64-bit mask).
+constexpr uint32_t kMinK = 8;
+constexpr uint32_t kTilesPerSm = 5;
+
+Geometry geometry(uint32_t B, uint32_t L, uint32_t sms, uint32_t k_min = kMinK) {
     Geometry g;
     g.ntl = (uint32_t)ceil_div(L ? L : 1, 32);
-    g.K = 8;
-    while (g.K < 64 && (uint64_t)g.ntl * ceil_div(B ? B : 1, (uint64_t)kRows * g.K) > kTargetCtas)
-        g.K *= 2;
+    const uint64_t target = (uint64_t)kTilesPerSm * (sms ? sms : 1);
+    const uint64_t rows = target / g.ntl ? target / g.ntl : 1;  // row tiles that fit beside ntl lane tiles
+    const uint64_t K = ceil_div(B ? B : 1, (uint64_t)kRows * rows);
+    g.K = K < k_min ? k_min : (K > 64 ? 64 : (uint32_t)K);
     g.ntr = (uint32_t)ceil_div(B ? B : 1, (uint64_t)kRows * g.K);
+    return g;
+}
+
+// The workspace holds the tile records of the tallest geometry any device
+// can choose (K = kMinK), so its size does not depend on the device.
+Geometry ws_geometry(uint32_t B, uint32_t L) {
+    Geometry g;
+    g.ntl = (uint32_t)ceil_div(L ? L : 1, 32);
+    g.K = kMinK;
+    g.ntr = (uint32_t)ceil_div(B ? B : 1, (uint64_t)kRows * kMinK);
     return g;
 }
 
@@ -181,7 +198,7 @@ struct Ws {
 };
 
 Ws carve(void *base, uint32_t B, uint32_t L, size_t *bytes) {
-    Geometry g = geometry(B, L);
+    Geometry g = ws_geometry(B, L);
     Carver c(base);
     Ws w;
     w.ctl = c.take<EncodeCtl>(1);
@@ -575,7 +592,7 @@ kvx_status launch_encode(const uint64_t *addr, const uint32_t *seg_size, const u
     size_t need = 0;
     Ws w = carve(ws, B, L, &need);
     if (ws_bytes < need) return KVX_EINVAL;
-    const Geometry g = geometry(B, L);
+    const Geometry g = geometry(B, L, (uint32_t)sm_count());
     cudaStream_t s = as_stream(stream);
     // the control block and the lane-tile totals (carved right after it) start at zero
     const size_t zero_bytes = reinterpret_cast<char *>(w.tile_runs + g.ntl) - reinterpret_cast<char *>(w.ctl);
