@@ -154,6 +154,8 @@ struct PlanArgs {
     CAgg *cagg;
     GAgg *gthr;  // per tile and thread: groups before the thread's first run
     CAgg *cthr;  // per tile and thread: carve prefix inside the tile
+    uint32_t *ready_g;  // per tile: gagg (and the tile's first group flag) published, 2 = abandoned
+    uint32_t *ready_c;  // per tile: cagg published, 2 = abandoned
 };
 
 union ScanSmem {
@@ -466,11 +468,17 @@ __device__ void phase_decode(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
         s_andn = ~0u;
     }
     __syncthreads();
-    {   // the keys phase sums its first histogram into ghist[0]
+    {   // the keys phase sums its first histogram into ghist[0]; the post-sort
+        // phase publishes per-tile totals behind these flags
         const uint64_t n = (uint64_t)kDigits * ceil_div((uint64_t)nt, (uint64_t)kHistGroup);
         for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
              i += (uint64_t)P * blockDim.x)
             a.ghist[0][i] = 0;
+        for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nt;
+             i += (uint64_t)P * blockDim.x) {
+            a.ready_g[i] = 0;
+            a.ready_c[i] = 0;
+        }
     }
     uint32_t bits = 0;
     unsigned long long o = 0, an = ~0ull;
@@ -844,22 +852,62 @@ __device__ uint64_t stretch_base(const PlanArgs &a, uint64_t R, const SortItem *
     return 0;  // never reached: position 0 starts a stretch
 }
 
-// Step 3, adjacency and group starts in one phase: the sorted records and
-// compat flags (as the groups phase and a stretch walk need them), then the
-// "grown chunk still fits the stride" cut from the bases of each stretch's
-// first run, taken from shared memory inside the tile and by a look-back for
-// the stretch open at the tile's start.  Runs whose stretch outgrows its
-// stride need a walk in order across positions other blocks are still
-// writing; they are left to the separate cut phase (ctl->walked), which then
-// runs after the barrier.  Per tile: the last stretch start and the group
-// starts (for the groups phase).
+// Per-tile totals passed between blocks inside one phase: a tile publishes
+// its total behind a flag (after a fence), and a later tile waits for the
+// flags of the tiles before it.  Every tile publishes before it waits for
+// anything, waits go only to tiles that publish first (earlier tiles, and
+// the first flag of the next tile), and all blocks are resident, so the
+// waits end; each is bounded in time all the same.
+__device__ __forceinline__ void publish(uint32_t *flag, uint32_t v) {
+    __syncthreads();  // the block's writes of this tile are done
+    if (threadIdx.x == 0) {
+        __threadfence();
+        asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
+    }
+}
+// The flag's value once set (1 = published, 2 = the tile was abandoned), or 0
+// if the wait gave up after about a second.
+__device__ __forceinline__ uint32_t wait_ready(const uint32_t *flag) {
+    uint64_t t0 = 0;
+    for (uint32_t polls = 0;; polls++) {
+        const uint32_t v = ld_acquire_gpu(flag);
+        if (v) return v;
+        if (polls >= 64) {
+            if (polls == 64) t0 = global_ns();
+            if (polls >= kBarrierPolls || global_ns() - t0 > kWaitNs) return 0;
+            __nanosleep(64);
+        }
+    }
+}
+
+// Steps 3 and 4 after the sort, one phase per tile with no grid barrier:
+//   - adjacency: the sorted records and compat flags;
+//   - the group starts: the "grown chunk still fits the stride" cut from the
+//     bases of each stretch's first run (shared memory inside the tile, a
+//     look-back for the stretch open at the tile's start);
+//   - group numbering: the tile publishes its group count, then sums the
+//     counts of the tiles before it;
+//   - groups: run_group / run_off, and the tile's slab bytes and reads, which
+//     it publishes, then sums those of the tiles before it;
+//   - the carve and the reads: group records with their slab offsets and the
+//     read descriptors, replayed from registers;
+//   - the last tile writes the counts.
+// Runs whose stretch outgrows its stride need a walk in order across
+// positions other tiles own: such a tile is marked walked and abandoned, so
+// are the tiles after it, and the barrier-separated phases (cut with the
+// walks, count, groups, emit) redo everything after the grid barrier.  The
+// records, compat flags and per-tile stretch starts every tile writes here
+// are what those phases read.
 template <int IPT>
-__device__ void phase_adjacent_cut(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P,
-                                   const SortItem *sorted, ScanSmem &sm, uint64_t *s_tbase) {
+__device__ void phase_post_sort(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P,
+                                const SortItem *sorted, ScanSmem &sm, uint64_t *s_tbase) {
     __shared__ uint64_t s_open;  // base of the first run of the stretch open at the tile's start
     __shared__ uint32_t s_need;
     __shared__ int64_t s_lmax;
     __shared__ uint64_t s_lbase;
+    __shared__ uint8_t s_first[kT];  // each thread's first position starts a group
+    __shared__ uint32_t s_next;      // the position after the tile starts a group (or is the end)
+    __shared__ uint32_t s_bad;
     const uint64_t T = (uint64_t)kT * IPT;
     for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
         const uint64_t p0 = (uint64_t)tile * T + (uint64_t)threadIdx.x * IPT;
@@ -936,6 +984,7 @@ __device__ void phase_adjacent_cut(const PlanArgs &a, uint64_t R, uint32_t nt, u
         if (p0 < R && (cm & 1u)) s_base = ex >= 0 ? s_tbase[(uint64_t)ex - (uint64_t)tile * T] : s_open;
         GAgg g{0, -1};
         bool walker = false;
+        uint32_t sb = 0;  // bit j: position p0 + j starts a group
 #pragma unroll
         for (int j = 0; j < IPT; j++) {
             const uint64_t p = p0 + j;
@@ -958,15 +1007,192 @@ __device__ void phase_adjacent_cut(const PlanArgs &a, uint64_t R, uint32_t nt, u
             }
             a.gflag[p] = start ? 1 : 0;
             if (start) {
+                sb |= 1u << j;
                 g.n++;
                 g.last = (int64_t)p;
             }
         }
         GAgg gex, gtot;
         block_scan(g, GOp(), GAgg{0, -1}, sm.g, &gex, &gtot);
-        if (threadIdx.x == 0) a.gagg[tile] = gtot;
-        if (__any_sync(0xFFFFFFFFu, walker) && (threadIdx.x & 31) == 0) atomicOr(&a.ctl->walked, 1u);
-        __syncthreads();  // s_tbase is rewritten by the next tile
+        s_first[threadIdx.x] = (uint8_t)(sb & 1u);
+        const bool tile_walked = __syncthreads_or(walker) != 0;
+        if (threadIdx.x == 0) {
+            a.gagg[tile] = gtot;
+            if (tile_walked) atomicOr(&a.ctl->walked, 1u);
+        }
+        publish(a.ready_g + tile, tile_walked ? 2u : 1u);
+
+        // ---- group numbering: the group counts of the tiles before this one,
+        // and whether the position after the tile starts a group
+        uint32_t bad = tile_walked ? 1u : 0u;  // 1: abandoned (a walk), 2: a wait gave up
+        GAgg vg{0, -1};
+        for (uint32_t t = threadIdx.x; t < tile && !bad; t += kT) {
+            const uint32_t f = wait_ready(a.ready_g + t);
+            if (f != 1) bad = f ? 1u : 2u;
+            else vg = GOp()(vg, ld_cg(a.gagg + t));
+        }
+        if (threadIdx.x == kT - 1 && !bad) {
+            const uint64_t q = (uint64_t)(tile + 1) * T;
+            uint32_t nx = 1;  // the end of the table ends the last group
+            if (q < R) {
+                const uint32_t f = wait_ready(a.ready_g + tile + 1);
+                if (f != 1) bad = f ? 1u : 2u;
+                else nx = __ldcg(a.gflag + q) ? 1u : 0u;
+            }
+            s_next = nx;
+        }
+        {
+            GAgg ex2, all;
+            block_scan(vg, GOp(), GAgg{0, -1}, sm.g, &ex2, &all);
+            vg = all;
+        }
+        if (threadIdx.x == 0) s_bad = 0;
+        __syncthreads();
+        if (bad) atomicOr(&s_bad, bad);
+        __syncthreads();
+        bad = s_bad;
+        if (bad) {
+            if (threadIdx.x == 0 && (bad & 2u)) raise_plan(a, KVX_S_TIMEOUT);
+            publish(a.ready_c + tile, 2u);
+            continue;
+        }
+        const GAgg carry_g = vg;
+        // bit j: p0 + j starts a group or is the end; bit IPT: the position after the thread's
+        uint32_t fl = sb;
+#pragma unroll
+        for (int j = 0; j <= IPT; j++)
+            if (p0 + j == R) fl |= 1u << j;
+        if (p0 + IPT < R)
+            fl |= (threadIdx.x + 1 < kT ? (uint32_t)s_first[threadIdx.x + 1] : s_next) << IPT;
+
+        // ---- groups: run_group / run_off; the tile's slab bytes and reads
+        const GAgg run0 = GOp()(carry_g, gex);  // groups before this thread's first run
+        uint64_t o_base = 0, o_block = 0, o_count = 0, o_node = 0;  // the group open at the first run
+        int64_t o_stride = 0;
+        if (p0 < R && !(fl & 1u)) {
+            const Rec *q = a.rec + (run0.last >= 0 ? run0.last : 0);
+            o_base = __ldcg(&q->base);
+            o_stride = __ldcg(&q->stride);
+            o_block = __ldcg(&q->block);
+            o_count = __ldcg(&q->count);
+            o_node = __ldcg(&q->node);
+        }
+        CAgg c{0, 0};
+        {
+            uint64_t n = run0.n, g_base = o_base, g_count = o_count;
+            int64_t g_stride = o_stride;
+#pragma unroll
+            for (int j = 0; j < IPT; j++) {
+                const uint64_t p = p0 + j;
+                if (p >= R) break;
+                if (fl >> j & 1u) {
+                    n++;
+                    g_base = its[j].base;
+                    g_stride = xs[j];
+                    g_count = xc[j];
+                }
+                const uint64_t off = its[j].base - g_base;
+                a.run_group[its[j].r] = (uint32_t)(n - 1);
+                a.run_off[its[j].r] = off;
+                if (fl >> (j + 1) & 1u) {  // the group ends here
+                    kvx_group G;
+                    G.stride = g_stride;
+                    G.chunk = off + xl[j];
+                    G.count = (uint32_t)g_count;
+                    G.dense = group_dense(G.count, G.stride, G.chunk) ? 1u : 0u;
+                    c.bytes += (uint64_t)G.count * G.chunk;
+                    c.descs += group_pieces(G);
+                }
+            }
+        }
+        CAgg cex, ctot;
+        block_scan(c, COp(), CAgg{0, 0}, sm.c, &cex, &ctot);
+        if (threadIdx.x == 0) a.cagg[tile] = ctot;
+        publish(a.ready_c + tile, 1u);
+
+        // ---- the carve of the tiles before this one
+        CAgg vc{0, 0};
+        for (uint32_t t = threadIdx.x; t < tile && !bad; t += kT) {
+            const uint32_t f = wait_ready(a.ready_c + t);
+            if (f != 1) bad = f ? 1u : 2u;
+            else vc = COp()(vc, ld_cg(a.cagg + t));
+        }
+        {
+            CAgg ex2, all;
+            block_scan(vc, COp(), CAgg{0, 0}, sm.c, &ex2, &all);
+            vc = all;
+        }
+        if (threadIdx.x == 0) s_bad = 0;
+        __syncthreads();
+        if (bad) atomicOr(&s_bad, bad);
+        __syncthreads();
+        if (s_bad) {  // the barrier-separated phases redo it (after a walk), or the wait gave up
+            if (threadIdx.x == 0 && (s_bad & 2u)) raise_plan(a, KVX_S_TIMEOUT);
+            continue;
+        }
+
+        // ---- step 4: group records with their slab offsets, and the reads
+        {
+            CAgg cur = COp()(vc, cex);
+            const uint64_t M = KVX_MAX_READ_BYTES;
+            uint64_t n = run0.n, g_base = o_base, g_block = o_block, g_count = o_count, g_node = o_node;
+            int64_t g_stride = o_stride;
+#pragma unroll
+            for (int j = 0; j < IPT; j++) {
+                const uint64_t p = p0 + j;
+                if (p >= R) break;
+                if (fl >> j & 1u) {
+                    n++;
+                    g_base = its[j].base;
+                    g_stride = xs[j];
+                    g_block = blocks[j];
+                    g_count = xc[j];
+                    g_node = its[j].node;
+                }
+                if (!(fl >> (j + 1) & 1u)) continue;
+                kvx_group G;
+                G.base = g_base;
+                G.stride = g_stride;
+                G.chunk = its[j].base - g_base + xl[j];
+                G.local = cur.bytes;
+                G.block = (uint32_t)g_block;
+                G.count = (uint32_t)g_count;
+                G.node = (uint32_t)g_node;
+                G.dense = group_dense(G.count, G.stride, G.chunk) ? 1u : 0u;
+                const uint64_t gid = n - 1;
+                if (gid < a.group_cap) st_group(a, gid, G);
+                uint64_t d = cur.descs;
+                if (G.dense) {
+                    const uint64_t total = (uint64_t)G.count * G.chunk;
+                    for (uint64_t o = 0; o < total; o += M, d++)
+                        if (d < a.desc_cap)
+                            st_desc(a, d, G.base + o, G.local + o, total - o < M ? total - o : M, (uint32_t)gid);
+                } else if (G.chunk > 0) {  // a group of empty runs has no read
+                    for (uint64_t i = 0; i < G.count; i++) {
+                        const uint64_t rb = G.base + i * (uint64_t)G.stride;
+                        const uint64_t lb = G.local + i * G.chunk;
+                        for (uint64_t o = 0; o < G.chunk; o += M, d++)
+                            if (d < a.desc_cap)
+                                st_desc(a, d, rb + o, lb + o, G.chunk - o < M ? G.chunk - o : M, (uint32_t)gid);
+                    }
+                }
+                cur.bytes += (uint64_t)G.count * G.chunk;
+                cur.descs += group_pieces(G);
+            }
+        }
+        if (tile == nt - 1 && threadIdx.x == 0) {  // the counts, with the capacity checks
+            const GAgg gall = GOp()(carry_g, gtot);
+            const CAgg call = COp()(vc, ctot);
+            if (gall.n > a.group_cap || call.descs > a.desc_cap) {
+                raise_plan(a, KVX_S_CAPACITY);
+                a.counts[0] = a.counts[1] = a.counts[2] = 0;
+            } else {
+                a.counts[0] = gall.n;
+                a.counts[1] = call.descs;
+                a.counts[2] = call.bytes;
+            }
+        }
+        __syncthreads();  // s_tbase and s_first are rewritten by the next tile
     }
 }
 
@@ -1773,16 +1999,15 @@ __device__ void plan_tiles(const PlanArgs &a, uint64_t R_in, uint64_t R, ScanSme
     }
     const SortItem *sorted = (nact & 1) ? a.items1 : a.items0;
 
-    phase_adjacent_cut<IPT>(a, R, nt, P, sorted, sm, st.tile_base);
+    phase_post_sort<IPT>(a, R, nt, P, sorted, sm, st.tile_base);
     PLAN_BARRIER();
-    if (__ldcg(&a.ctl->walked)) {
-        // some stretch outgrows its stride: cut again with the walks (in
-        // order along the stretch), then count every tile
-        phase_cut<IPT>(a, R, nt, P, sm);
-        PLAN_BARRIER();
-        phase_count<IPT>(a, R, nt, P, sm);
-        PLAN_BARRIER();
-    }
+    if (!__ldcg(&a.ctl->walked)) return;  // every tile was grouped and carved in that phase
+    // Some stretch outgrows its stride: steps 3 and 4 again, phase by phase,
+    // with the walks along such stretches in order.
+    phase_cut<IPT>(a, R, nt, P, sm);
+    PLAN_BARRIER();
+    phase_count<IPT>(a, R, nt, P, sm);
+    PLAN_BARRIER();
     const GAgg gall = reduce_prefix(a.gagg, nt, GOp(), GAgg{0, -1}, sm.g);
     if (gall.n > a.group_cap) {
         if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -1863,6 +2088,8 @@ struct Ws {
     CAgg *cagg;
     GAgg *gthr;
     CAgg *cthr;
+    uint32_t *ready_g;
+    uint32_t *ready_c;
 };
 
 // Tiles a table of up to run_cap runs can be cut into (any tile size).
@@ -1891,6 +2118,8 @@ Ws carve(void *base, uint64_t run_cap, size_t *bytes) {
     w.cagg = c.take<CAgg>(ntc);
     w.gthr = c.take<GAgg>(ntc * kT);
     w.cthr = c.take<CAgg>(ntc * kT);
+    w.ready_g = c.take<uint32_t>(ntc);
+    w.ready_c = c.take<uint32_t>(ntc);
     *bytes = c.off;
     return w;
 }
@@ -1998,6 +2227,8 @@ extern "C" kvx_status kvx_plan_groups(const uint32_t *runs_per_lane, uint32_t ta
     a.cagg = w.cagg;
     a.gthr = w.gthr;
     a.cthr = w.cthr;
+    a.ready_g = w.ready_g;
+    a.ready_c = w.ready_c;
     static bool small_ready[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
