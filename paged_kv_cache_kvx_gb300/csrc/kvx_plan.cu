@@ -898,7 +898,7 @@ __device__ __forceinline__ uint32_t wait_ready(const uint32_t *flag) {
 // walks, count, groups, emit) redo everything after the grid barrier.  The
 // records, compat flags and per-tile stretch starts every tile writes here
 // are what those phases read.
-template <int IPT>
+template <int IPT, bool kFuse>
 __device__ void phase_post_sort(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P,
                                 const SortItem *sorted, ScanSmem &sm, uint64_t *s_tbase) {
     __shared__ uint64_t s_open;  // base of the first run of the stretch open at the tile's start
@@ -1019,6 +1019,11 @@ __device__ void phase_post_sort(const PlanArgs &a, uint64_t R, uint32_t nt, uint
         if (threadIdx.x == 0) {
             a.gagg[tile] = gtot;
             if (tile_walked) atomicOr(&a.ctl->walked, 1u);
+        }
+        if constexpr (!kFuse) {
+            // groups and the carve follow as their own phases, after a barrier
+            __syncthreads();  // s_tbase and s_first are rewritten by the next tile
+            continue;
         }
         publish(a.ready_g + tile, tile_walked ? 2u : 1u);
 
@@ -1999,15 +2004,23 @@ __device__ void plan_tiles(const PlanArgs &a, uint64_t R_in, uint64_t R, ScanSme
     }
     const SortItem *sorted = (nact & 1) ? a.items1 : a.items0;
 
-    phase_post_sort<IPT>(a, R, nt, P, sorted, sm, st.tile_base);
+    // The 2048-run tile body carries each tile through groups and the carve
+    // in the same phase; the smaller bodies (tables of a few dozen tiles,
+    // one short tile per block) measured faster with those steps as their
+    // own phases, after barriers.
+    constexpr bool kFuse = IPT == kIPT;
+    phase_post_sort<IPT, kFuse>(a, R, nt, P, sorted, sm, st.tile_base);
     PLAN_BARRIER();
-    if (!__ldcg(&a.ctl->walked)) return;  // every tile was grouped and carved in that phase
-    // Some stretch outgrows its stride: steps 3 and 4 again, phase by phase,
-    // with the walks along such stretches in order.
-    phase_cut<IPT>(a, R, nt, P, sm);
-    PLAN_BARRIER();
-    phase_count<IPT>(a, R, nt, P, sm);
-    PLAN_BARRIER();
+    if (__ldcg(&a.ctl->walked)) {
+        // Some stretch outgrows its stride: the cut again, phase by phase,
+        // with the walks along such stretches in order, then the counts.
+        phase_cut<IPT>(a, R, nt, P, sm);
+        PLAN_BARRIER();
+        phase_count<IPT>(a, R, nt, P, sm);
+        PLAN_BARRIER();
+    } else if (kFuse) {
+        return;  // every tile was grouped and carved in that phase
+    }
     const GAgg gall = reduce_prefix(a.gagg, nt, GOp(), GAgg{0, -1}, sm.g);
     if (gall.n > a.group_cap) {
         if (blockIdx.x == 0 && threadIdx.x == 0) {
