@@ -491,11 +491,12 @@ kvx_status kvx_pack_noalloc(const uint8_t *pool, uint64_t pool_bytes,
 
 /*
  * Diagnostic, no counterpart in the paper: shows that the library's bounded
- * waits give up instead of hanging.  Launches a grid barrier that waits for
- * one block more than is launched and an mbarrier wait for bytes no copy
- * will deliver; each polls to its limit (about one second), then ORs
- * KVX_S_TIMEOUT into *status (device word) and returns.  Nothing is copied
- * and nothing faults.
+ * waits give up instead of hanging.  Launches, in order on the stream, a grid
+ * barrier that waits for one block more than is launched, an mbarrier wait
+ * for bytes no copy will deliver, and the planner's cross-block flag wait on
+ * a flag nothing sets; each polls to its limit (about one second), then ORs
+ * KVX_S_TIMEOUT into its own word of status[3] (device words: barrier,
+ * mbarrier, flag) and returns.  Nothing is copied and nothing faults.
  */
 kvx_status kvx_selftest_timeouts(uint32_t *status, void *stream);
 

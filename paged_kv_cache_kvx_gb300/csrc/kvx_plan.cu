@@ -880,6 +880,14 @@ __device__ __forceinline__ uint32_t wait_ready(const uint32_t *flag) {
     }
 }
 
+// Diagnostic (kvx_selftest_timeouts): the flag wait gives up on a flag that
+// nothing ever sets.
+__device__ uint32_t g_selftest_flag;  // never written: stays 0
+
+__global__ void k_selftest_flag(uint32_t *status) {
+    if (threadIdx.x == 0 && wait_ready(&g_selftest_flag) == 0) atomicOr(status, KVX_S_TIMEOUT);
+}
+
 // Steps 3 and 4 after the sort, one phase per tile with no grid barrier:
 //   - adjacency: the sorted records and compat flags;
 //   - the group starts: the "grown chunk still fits the stride" cut from the
@@ -2146,6 +2154,15 @@ Ws carve(void *base, uint64_t run_cap, size_t *bytes) {
 int plan_max_blocks() { return sm_count(); }
 
 }  // namespace
+}  // namespace kvx
+
+namespace kvx {
+// Launches the flag-wait diagnostic for kvx_selftest_timeouts.
+kvx_status launch_selftest_flag_wait(uint32_t *status, cudaStream_t s) {
+    k_selftest_flag<<<1, 32, 0, s>>>(status);
+    KVX_LAUNCHED();
+    return KVX_OK;
+}
 }  // namespace kvx
 
 using namespace kvx;

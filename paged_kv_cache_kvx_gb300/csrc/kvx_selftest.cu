@@ -1,9 +1,10 @@
 // Diagnostic: the bounded waits of libkvx give up and report instead of
-// hanging.  Two tiny kernels wait on conditions that nothing will satisfy --
-// a grid barrier that expects one block more than is launched, and an
-// mbarrier that expects bytes no copy will deliver -- and raise KVX_S_TIMEOUT
-// when their poll limits run out.  Nothing faults: no copy is ever in
-// flight, and each wait ends by itself after at most a few seconds.
+// hanging.  Three tiny kernels wait on conditions that nothing will satisfy --
+// a grid barrier that expects one block more than is launched, an mbarrier
+// that expects bytes no copy will deliver, and the planner's cross-block flag
+// wait on a flag that nothing sets -- and each raises KVX_S_TIMEOUT in its own
+// status word when its limit runs out.  Nothing faults: no copy is ever in
+// flight, and each wait ends by itself after about a second.
 #include "kvx_common.cuh"
 
 namespace kvx {
@@ -29,6 +30,10 @@ __global__ void k_selftest_mbarrier(uint32_t *status) {
 }  // namespace
 }  // namespace kvx
 
+namespace kvx {
+kvx_status launch_selftest_flag_wait(uint32_t *status, cudaStream_t s);  // kvx_plan.cu
+}
+
 using namespace kvx;
 
 extern "C" kvx_status kvx_selftest_timeouts(uint32_t *status, void *stream) {
@@ -44,7 +49,7 @@ extern "C" kvx_status kvx_selftest_timeouts(uint32_t *status, void *stream) {
         return KVX_ECUDA;
     }
     note_launch();
-    k_selftest_mbarrier<<<1, 32, 0, s>>>(status);
+    k_selftest_mbarrier<<<1, 32, 0, s>>>(status + 1);
     KVX_LAUNCHED();
-    return KVX_OK;
+    return launch_selftest_flag_wait(status + 2, s);
 }

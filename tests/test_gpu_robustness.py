@@ -12,14 +12,15 @@ pytestmark = pytest.mark.gpu
 
 
 def test_bounded_waits_report_a_timeout():
-    """A grid barrier and an mbarrier that nothing will release give up
-    within seconds and say so; the context stays usable afterwards."""
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    """A grid barrier, an mbarrier and the planner's cross-block flag wait that
+    nothing will release each give up within seconds and say so in their own
+    status word; the context stays usable afterwards."""
+    status = torch.zeros(3, dtype=torch.int32, device="cuda")
     t0 = time.time()
     kvx.kvx_selftest_timeouts(status)
     torch.cuda.synchronize()
     assert time.time() - t0 < 30
-    assert int(status.item()) == kvx.S_TIMEOUT
+    assert status.cpu().tolist() == [kvx.S_TIMEOUT] * 3
     x = torch.arange(10, device="cuda")
     assert int(x.sum().item()) == 45
 
