@@ -373,15 +373,18 @@ __global__ void __launch_bounds__(kThreads, 6) k_encode(const __grid_constant__ 
     // scanned on its own and its total published, then, after a barrier,
     // every chunk folds the totals of the lane's earlier chunks into its
     // tiles' entry prefixes.
+    // Work items are numbered warp-major over the blocks (item i to warp i / G
+    // of block i % G): numbered block-major, the few hundred items landed on
+    // the first blocks, eight warps each, and ran several times slower.
     if (g.ntr <= kTallRows) {
-        for (uint32_t l = blockIdx.x * kRows + w; l < L; l += G * kRows) {
+        for (uint32_t l = w * G + blockIdx.x; l < L; l += G * kRows) {
             const Prefix carry = scan_tile_range(a.tiles, L, l, 0, g.ntr, Prefix{0u, 0u, kNone}, t);
             if (t == 0) lane_done(a, l, carry.runs);
         }
     } else {
         const uint32_t C = lane_chunks(g);
         const uint64_t tasks = (uint64_t)L * C;
-        const uint64_t gw = (uint64_t)blockIdx.x * kRows + w, nw = (uint64_t)G * kRows;
+        const uint64_t gw = (uint64_t)w * G + blockIdx.x, nw = (uint64_t)G * kRows;
         for (uint64_t q = gw; q < tasks; q += nw) {  // each chunk's own scan
             const uint32_t l = (uint32_t)(q / C), c = (uint32_t)(q % C);
             const uint32_t r = c * 32 + t;
