@@ -146,7 +146,7 @@ struct PlanArgs {
     SortItem *items0, *items1;
     uint32_t *hist[3];   // [tile][digit]
     uint32_t *ghist[3];  // [tile group][digit]: the same counts summed over groups of kHistGroup tiles
-    Rec *rec;
+    uint64_t *run_bl;  // per run: its first block (low word), its lane's segment length (high word)
     uint8_t *compat;
     uint8_t *gflag;
     int64_t *segmax;
@@ -593,7 +593,7 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
         const Seg carry = reduce_prefix(a.seg, tile, SegOp(), Seg{0, 0, 0}, sm.seg);
         const uint64_t r0 = (uint64_t)tile * (kT * IPT) + (uint64_t)threadIdx.x * IPT;
         Seg agg{0, 0, 0};
-        uint32_t cnts[IPT], lanes[IPT], nodes[IPT], empty[IPT];
+        uint32_t cnts[IPT], lanes[IPT], nodes[IPT], lens[IPT];
         uint64_t bases[IPT];
         uint32_t heads = 0;
 #pragma unroll
@@ -612,7 +612,7 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
             const uint64_t r = r0 + j;
             if (r >= R) continue;
             nodes[j] = __ldg(a.numa + lanes[j]);
-            empty[j] = __ldg(a.seg_len + lanes[j]) == 0 ? 1u : 0u;
+            lens[j] = __ldg(a.seg_len + lanes[j]);
             const bool head = r == (lf_smem ? s_lf[lanes[j]] : __ldcg(a.lane_first + lanes[j]));
             if (head) heads |= 1u << j;
             agg = SegOp()(agg, Seg{cnts[j], head ? 1u : 0u, 0});
@@ -627,10 +627,11 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
             if (heads >> j & 1u) blk = 0;
             const uint32_t l = lanes[j];
             a.run_block[r] = (uint32_t)blk;
+            a.run_bl[r] = blk | (uint64_t)lens[j] << 32;
             blk += cnts[j];
             const uint32_t next_first = lf_smem ? s_lf[l + 1] : __ldcg(a.lane_first + l + 1);
             if (r + 1 == (uint64_t)next_first && blk != a.B) bits |= KVX_S_COVERAGE;
-            a.items0[r] = SortItem{bases[j], nodes[j], (uint32_t)r | (empty[j] ? kEmptyBit : 0u)};
+            a.items0[r] = SortItem{bases[j], nodes[j], (uint32_t)r | (lens[j] == 0 ? kEmptyBit : 0u)};
         }
         if (nact) {
             // histogram of the first active digit; one shared atomic per distinct
@@ -638,7 +639,7 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
 #pragma unroll
             for (int j = 0; j < IPT; j++) {
                 const uint64_t r = r0 + j;
-                const uint32_t d = r < R ? digit_of(bases[j], nodes[j], empty[j], dig0) : ~0u;
+                const uint32_t d = r < R ? digit_of(bases[j], nodes[j], lens[j] == 0 ? 1u : 0u, dig0) : ~0u;
                 add_key_runs(s_hist, d, threadIdx.x & 31);
             }
             __syncthreads();
@@ -813,12 +814,18 @@ __device__ __forceinline__ Rec make_rec(const PlanArgs &a, SortItem it, uint64_t
     x.base = it.base;
     x.node = it.node;
     x.r = it.r;
-    x.stride = a.run_stride[it.r];
-    x.count = a.run_count[it.r];
-    x.block = __ldcg(a.run_block + it.r);
-    x.len = a.seg_len[__ldcg(a.run_lane + it.r)];
+    x.stride = __ldg(a.run_stride + it.r);
+    x.count = __ldg(a.run_count + it.r);
+    const uint64_t bl = __ldcg(a.run_bl + it.r);
+    x.block = (uint32_t)bl;
+    x.len = (uint32_t)(bl >> 32);
     x.pad = 0;
     return x;
+}
+
+// The record of the run at sorted position p.
+__device__ __forceinline__ Rec rec_at(const PlanArgs &a, const SortItem *sorted, uint64_t p, uint64_t R) {
+    return make_rec(a, ld_cg(sorted + p), R);
 }
 
 // The base of the run that starts the compatible stretch holding sorted
@@ -936,19 +943,17 @@ __device__ void phase_post_sort(const PlanArgs &a, uint64_t R, uint32_t nt, uint
             }
         }
         int64_t xs[IPT];
-        uint32_t xc[IPT], blocks[IPT], lanes[IPT], xl[IPT];
+        uint32_t xc[IPT], blocks[IPT], xl[IPT];
 #pragma unroll
         for (int j = 0; j < IPT; j++) {
             if (p0 + j >= R) continue;
             const uint32_t r = its[j].r;
-            xs[j] = a.run_stride[r];
-            xc[j] = a.run_count[r];
-            blocks[j] = __ldcg(a.run_block + r);
-            lanes[j] = __ldcg(a.run_lane + r);
+            xs[j] = __ldg(a.run_stride + r);
+            xc[j] = __ldg(a.run_count + r);
+            const uint64_t bl = __ldcg(a.run_bl + r);
+            blocks[j] = (uint32_t)bl;
+            xl[j] = (uint32_t)(bl >> 32);
         }
-#pragma unroll
-        for (int j = 0; j < IPT; j++)
-            if (p0 + j < R) xl[j] = __ldg(a.seg_len + lanes[j]);
         int64_t mx = -1;
         uint32_t cm = 0;  // bit j: position p0 + j is compatible with its predecessor
 #pragma unroll
@@ -964,7 +969,6 @@ __device__ void phase_post_sort(const PlanArgs &a, uint64_t R, uint32_t nt, uint
             x.block = blocks[j];
             x.len = xl[j];
             x.pad = 0;
-            a.rec[p] = x;
             s_tbase[p - (uint64_t)tile * T] = x.base;
             const bool c = have_prev && compatible(prev, x);
             a.compat[p] = c ? 1 : 0;
@@ -1083,12 +1087,12 @@ __device__ void phase_post_sort(const PlanArgs &a, uint64_t R, uint32_t nt, uint
         uint64_t o_base = 0, o_block = 0, o_count = 0, o_node = 0;  // the group open at the first run
         int64_t o_stride = 0;
         if (p0 < R && !(fl & 1u)) {
-            const Rec *q = a.rec + (run0.last >= 0 ? run0.last : 0);
-            o_base = __ldcg(&q->base);
-            o_stride = __ldcg(&q->stride);
-            o_block = __ldcg(&q->block);
-            o_count = __ldcg(&q->count);
-            o_node = __ldcg(&q->node);
+            const Rec q = rec_at(a, sorted, run0.last >= 0 ? (uint64_t)run0.last : 0, R);
+            o_base = q.base;
+            o_stride = q.stride;
+            o_block = q.block;
+            o_count = q.count;
+            o_node = q.node;
         }
         CAgg c{0, 0};
         {
@@ -1213,12 +1217,12 @@ __device__ void phase_post_sort(const PlanArgs &a, uint64_t R, uint32_t nt, uint
 // (its chunk exceeds the stride): it starts a group, and the rest of the
 // stretch is cut in order, a new group wherever the chunk would outgrow the
 // stride again (only tables whose block chunks exceed their stride get here).
-__device__ __noinline__ void walk_stretch(const PlanArgs &a, uint64_t R, uint64_t p, uint64_t base,
-                                          uint64_t stride) {
+__device__ __noinline__ void walk_stretch(const PlanArgs &a, const SortItem *sorted, uint64_t R, uint64_t p,
+                                          uint64_t base, uint64_t stride) {
     a.gflag[p] = 1;
     uint64_t cur = base;
     for (uint64_t q = p + 1; q < R && __ldcg(a.compat + q); q++) {
-        const Rec y = ld_cg(a.rec + q);
+        const Rec y = rec_at(a, sorted, q, R);
         if (y.base + y.len - cur > stride) {
             a.gflag[q] = 1;
             cur = y.base;
@@ -1230,7 +1234,8 @@ __device__ __noinline__ void walk_stretch(const PlanArgs &a, uint64_t R, uint64_
 
 // Step 3: group starts.
 template <int IPT>
-__device__ void phase_cut(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, ScanSmem &sm) {
+__device__ void phase_cut(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, const SortItem *sorted,
+                          ScanSmem &sm) {
     for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
         const int64_t carry = reduce_prefix(a.segmax, tile, MaxOp(), (int64_t)-1, sm.i64);
         const uint64_t p0 = (uint64_t)tile * (kT * IPT) + (uint64_t)threadIdx.x * IPT;
@@ -1243,12 +1248,12 @@ __device__ void phase_cut(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P
         for (int j = 0; j < IPT; j++) {
             const uint64_t p = p0 + j;
             if (p < R) {
-                const Rec *q = a.rec + p;
+                const Rec q = rec_at(a, sorted, p, R);
                 if (__ldcg(a.compat + p)) cm |= 1u << j;
-                xb[j] = __ldcg(&q->base);
-                xs[j] = __ldcg(&q->stride);
-                xc[j] = __ldcg(&q->count);
-                xl[j] = __ldcg(&q->len);
+                xb[j] = q.base;
+                xs[j] = q.stride;
+                xc[j] = q.count;
+                xl[j] = q.len;
             }
         }
         int64_t mx = -1;
@@ -1259,7 +1264,7 @@ __device__ void phase_cut(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P
         block_scan(mx, MaxOp(), (int64_t)-1, sm.i64, &ex, &tot);
         const int64_t s0 = carry > ex ? carry : ex;  // stretch start before this thread's first run
         uint64_t s_base = 0;                          // base of the current stretch's first run
-        if (p0 < R && (cm & 1u)) s_base = __ldcg(&a.rec[s0 > 0 ? s0 : 0].base);
+        if (p0 < R && (cm & 1u)) s_base = ld_cg(sorted + (s0 > 0 ? s0 : 0)).base;
         // the tile's group starts, for the groups phase (valid when no
         // walker ran anywhere: then every flag was set by its own position)
         GAgg g{0, -1};
@@ -1286,7 +1291,7 @@ __device__ void phase_cut(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P
                     // first group walks the rest of the stretch; O > stride:
                     // a later run of such a stretch, flagged by that walker
                     walker = true;
-                    if (O <= stride) walk_stretch(a, R, p, xb[j], stride);
+                    if (O <= stride) walk_stretch(a, sorted, R, p, xb[j], stride);
                     continue;
                 }
             }
@@ -1327,7 +1332,8 @@ __device__ void phase_count(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t
 // round trip per dependency level rather than one per run.  The thread's
 // group count and carve prefix inside the tile are kept for the emit phase.
 template <int IPT>
-__device__ void phase_groups(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, ScanSmem &sm) {
+__device__ void phase_groups(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, const SortItem *sorted,
+                             ScanSmem &sm) {
     for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
         const GAgg carry = reduce_prefix(a.gagg, tile, GOp(), GAgg{0, -1}, sm.g);
         const uint64_t p0 = (uint64_t)tile * (kT * IPT) + (uint64_t)threadIdx.x * IPT;
@@ -1346,15 +1352,18 @@ __device__ void phase_groups(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
         for (int j = 0; j < IPT; j++) {
             const uint64_t p = p0 + j;
             if (p < R) {
-                const Rec *q = a.rec + p;
-                xb[j] = __ldcg(&q->base);
-                xl[j] = __ldcg(&q->len);
-                xr[j] = __ldcg(&q->r);
+                SortItem it = ld_cg(sorted + p);
+                it.r = item_run(it);
+                if (it.r >= R) it.r = 0;  // never taken: sorted items are a permutation of the runs
+                const uint64_t bl = __ldcg(a.run_bl + it.r);
+                xb[j] = it.base;
+                xl[j] = (uint32_t)(bl >> 32);
+                xr[j] = it.r;
                 if (fl >> j & 1u) {
-                    gs[j] = __ldcg(&q->stride);
-                    gb[j] = __ldcg(&q->block);
-                    gc[j] = __ldcg(&q->count);
-                    gn[j] = __ldcg(&q->node);
+                    gs[j] = __ldg(a.run_stride + it.r);
+                    gb[j] = (uint32_t)bl;
+                    gc[j] = __ldg(a.run_count + it.r);
+                    gn[j] = it.node;
                 }
             }
         }
@@ -1373,12 +1382,12 @@ __device__ void phase_groups(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
         uint64_t g_base = 0, g_block = 0, g_count = 0, g_node = 0;
         int64_t g_stride = 0;
         if (p0 < R && !(fl & 1u)) {
-            const Rec *q = a.rec + (run.last >= 0 ? run.last : 0);
-            g_base = __ldcg(&q->base);
-            g_stride = __ldcg(&q->stride);
-            g_block = __ldcg(&q->block);
-            g_count = __ldcg(&q->count);
-            g_node = __ldcg(&q->node);
+            const Rec q = rec_at(a, sorted, run.last >= 0 ? (uint64_t)run.last : 0, R);
+            g_base = q.base;
+            g_stride = q.stride;
+            g_block = q.block;
+            g_count = q.count;
+            g_node = q.node;
         }
         CAgg c{0, 0};
 #pragma unroll
@@ -2022,7 +2031,7 @@ __device__ void plan_tiles(const PlanArgs &a, uint64_t R_in, uint64_t R, ScanSme
     if (__ldcg(&a.ctl->walked)) {
         // Some stretch outgrows its stride: the cut again, phase by phase,
         // with the walks along such stretches in order, then the counts.
-        phase_cut<IPT>(a, R, nt, P, sm);
+        phase_cut<IPT>(a, R, nt, P, sorted, sm);
         PLAN_BARRIER();
         phase_count<IPT>(a, R, nt, P, sm);
         PLAN_BARRIER();
@@ -2037,7 +2046,7 @@ __device__ void plan_tiles(const PlanArgs &a, uint64_t R_in, uint64_t R, ScanSme
         }
         return;
     }
-    phase_groups<IPT>(a, R, nt, P, sm);
+    phase_groups<IPT>(a, R, nt, P, sorted, sm);
     PLAN_BARRIER();
     const CAgg call = reduce_prefix(a.cagg, nt, COp(), CAgg{0, 0}, sm.c);
     if (call.descs > a.desc_cap) {
@@ -2101,7 +2110,7 @@ struct Ws {
     SortItem *items[2];
     uint32_t *hist[3];
     uint32_t *ghist[3];
-    Rec *rec;
+    uint64_t *run_bl;
     uint8_t *compat;
     uint8_t *gflag;
     int64_t *segmax;
@@ -2131,7 +2140,7 @@ Ws carve(void *base, uint64_t run_cap, size_t *bytes) {
     w.items[1] = c.take<SortItem>(run_cap);
     for (int i = 0; i < 3; i++) w.hist[i] = c.take<uint32_t>(kDigits * ntc);
     for (int i = 0; i < 3; i++) w.ghist[i] = c.take<uint32_t>(kDigits * ceil_div(ntc, (uint64_t)kHistGroup));
-    w.rec = c.take<Rec>(run_cap);
+    w.run_bl = c.take<uint64_t>(run_cap);
     w.compat = c.take<uint8_t>(run_cap);
     w.gflag = c.take<uint8_t>(run_cap + 1);
     w.segmax = c.take<int64_t>(ntc);
@@ -2249,7 +2258,7 @@ extern "C" kvx_status kvx_plan_groups(const uint32_t *runs_per_lane, uint32_t ta
         a.hist[i] = w.hist[i];
         a.ghist[i] = w.ghist[i];
     }
-    a.rec = w.rec;
+    a.run_bl = w.run_bl;
     a.compat = w.compat;
     a.gflag = w.gflag;
     a.segmax = w.segmax;
