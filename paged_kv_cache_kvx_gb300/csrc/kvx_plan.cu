@@ -211,6 +211,37 @@ __device__ T block_scan(T v, Op op, T identity, T *sh, T *excl, T *total) {
     return op(before, x);
 }
 
+// Seg over a warp in lane order: the fold of all 32 values (every lane gets
+// it), and each lane's inclusive prefix.
+__device__ __forceinline__ Seg shfl_seg(const Seg &v, int src, bool down, int d) {
+    Seg o;
+    const uint32_t lo = (uint32_t)v.sum, hi = (uint32_t)(v.sum >> 32);
+    const uint32_t l2 = down ? __shfl_down_sync(0xFFFFFFFFu, lo, d) : __shfl_sync(0xFFFFFFFFu, lo, src);
+    const uint32_t h2 = down ? __shfl_down_sync(0xFFFFFFFFu, hi, d) : __shfl_sync(0xFFFFFFFFu, hi, src);
+    o.head = down ? __shfl_down_sync(0xFFFFFFFFu, v.head, d) : __shfl_sync(0xFFFFFFFFu, v.head, src);
+    o.sum = (uint64_t)h2 << 32 | l2;
+    o.pad = 0;
+    return o;
+}
+__device__ __forceinline__ Seg warp_fold_seg(Seg v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const Seg o = shfl_seg(v, 0, true, d);
+        if (lane + d < 32) v = SegOp()(v, o);
+    }
+    return shfl_seg(v, 0, false, 0);
+}
+__device__ __forceinline__ Seg warp_scan_seg(Seg v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const Seg o = shfl_up_words(v, d);
+        if (lane >= d) v = SegOp()(o, v);
+    }
+    return v;
+}
+
 // Ordered reduction of agg[0, t) by the whole block (the carry into tile t).
 template <class T, class Op>
 __device__ T reduce_prefix(const T *agg, uint64_t t, Op op, T identity, T *sh) {
@@ -483,16 +514,19 @@ __device__ void phase_decode(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
     uint32_t bits = 0;
     unsigned long long o = 0, an = ~0ull;
     uint32_t on = 0, ann = ~0u, oe = 0, ae = 1;
+    // Each warp takes 32 * IPT consecutive runs of the tile, run j * 32 + lane
+    // for its lane (coalesced loads and stores); the tile's segmented count
+    // total is folded in run order, warp by warp.
+    const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
-        Seg agg{0, 0, 0};
-        const uint64_t r0 = (uint64_t)tile * (kT * IPT) + (uint64_t)threadIdx.x * IPT;
+        const uint64_t r0 = (uint64_t)tile * (kT * IPT) + (uint64_t)w * (32 * IPT) + lane;
         // all loads of this thread's runs first, then the checks
         uint32_t lanes[IPT], cnts[IPT], lens[IPT], nodes[IPT];
         uint64_t bases[IPT];
         int64_t strides[IPT];
 #pragma unroll
         for (int j = 0; j < IPT; j++) {
-            const uint64_t r = r0 + j;
+            const uint64_t r = r0 + (uint64_t)j * 32;
             lanes[j] = 0;
             if (r < R) {
                 lanes[j] = lf_smem ? lane_of([&](uint32_t i) { return s_lf[i]; }, L, r)
@@ -504,42 +538,51 @@ __device__ void phase_decode(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
         }
 #pragma unroll
         for (int j = 0; j < IPT; j++) {
-            if (r0 + j < R) {
+            if (r0 + (uint64_t)j * 32 < R) {
                 lens[j] = __ldg(a.seg_len + lanes[j]);
                 nodes[j] = __ldg(a.numa + lanes[j]);
             }
         }
+        Seg wagg{0, 0, 0};  // this warp's runs so far, in order
 #pragma unroll
         for (int j = 0; j < IPT; j++) {
-            const uint64_t r = r0 + j;
-            if (r >= R) continue;
-            const uint32_t l = lanes[j];
-            a.run_lane[r] = l;
-            const uint64_t base = bases[j];
-            const int64_t stride = strides[j];
-            const uint32_t cnt = cnts[j];
-            const uint32_t len = lens[j];
-            const uint32_t node = nodes[j];
-            if (cnt == 0) bits |= KVX_S_ZERO_COUNT;
-            if (cnt == 1 && stride != 0) bits |= KVX_S_STRIDE1;
-            if (cnt >= 1) {
-                const __int128 first = (__int128)base;
-                const __int128 last = first + (__int128)(cnt - 1) * (__int128)stride;
-                const __int128 hi = last > first ? last : first;
-                if (last < 0 || hi + (__int128)len > (__int128)a.pool_bytes) bits |= KVX_S_SPAN;
+            const uint64_t r = r0 + (uint64_t)j * 32;
+            Seg s{0, 0, 0};
+            if (r < R) {
+                const uint32_t l = lanes[j];
+                a.run_lane[r] = l;
+                const uint64_t base = bases[j];
+                const int64_t stride = strides[j];
+                const uint32_t cnt = cnts[j];
+                const uint32_t len = lens[j];
+                const uint32_t node = nodes[j];
+                if (cnt == 0) bits |= KVX_S_ZERO_COUNT;
+                if (cnt == 1 && stride != 0) bits |= KVX_S_STRIDE1;
+                if (cnt >= 1) {
+                    const __int128 first = (__int128)base;
+                    const __int128 last = first + (__int128)(cnt - 1) * (__int128)stride;
+                    const __int128 hi = last > first ? last : first;
+                    if (last < 0 || hi + (__int128)len > (__int128)a.pool_bytes) bits |= KVX_S_SPAN;
+                }
+                const bool head = r == (lf_smem ? s_lf[l] : __ldcg(a.lane_first + l));
+                s = Seg{cnt, head ? 1u : 0u, 0};
+                o |= base;
+                an &= base;
+                on |= node;
+                ann &= node;
+                oe |= len == 0;
+                ae &= len == 0;
             }
-            const bool head = r == (lf_smem ? s_lf[l] : __ldcg(a.lane_first + l));
-            agg = SegOp()(agg, Seg{cnt, head ? 1u : 0u, 0});
-            o |= base;
-            an &= base;
-            on |= node;
-            ann &= node;
-            oe |= len == 0;
-            ae &= len == 0;
+            wagg = SegOp()(wagg, warp_fold_seg(s));
         }
-        Seg ex, tot;
-        block_scan(agg, SegOp(), Seg{0, 0, 0}, sm.seg, &ex, &tot);
-        if (threadIdx.x == 0) a.seg[tile] = tot;
+        __syncthreads();  // sm.seg may still be read from the previous tile
+        if (lane == 0) sm.seg[w] = wagg;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            Seg tot{0, 0, 0};
+            for (uint32_t i = 0; i < kT / 32; i++) tot = SegOp()(tot, sm.seg[i]);
+            a.seg[tile] = tot;
+        }
     }
     // one shared atomic per warp, one global atomic per block
     bits = __reduce_or_sync(0xFFFFFFFFu, bits);
@@ -588,17 +631,22 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
     if (threadIdx.x == 0) s_bits = 0;
     __syncthreads();
     uint32_t bits = 0;
+    // Runs as in the decode phase: each warp takes 32 * IPT consecutive runs,
+    // run j * 32 + lane for its lane.  A run's first block is the segmented
+    // count sum before it: warp scans per j in run order, the warps' totals
+    // through shared memory (the scans run twice rather than hold IPT
+    // prefixes in registers).
+    const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
         for (uint32_t d = threadIdx.x; d < kDigits; d += blockDim.x) s_hist[d] = 0;
         const Seg carry = reduce_prefix(a.seg, tile, SegOp(), Seg{0, 0, 0}, sm.seg);
-        const uint64_t r0 = (uint64_t)tile * (kT * IPT) + (uint64_t)threadIdx.x * IPT;
-        Seg agg{0, 0, 0};
+        const uint64_t r0 = (uint64_t)tile * (kT * IPT) + (uint64_t)w * (32 * IPT) + lane;
         uint32_t cnts[IPT], lanes[IPT], nodes[IPT], lens[IPT];
         uint64_t bases[IPT];
         uint32_t heads = 0;
 #pragma unroll
         for (int j = 0; j < IPT; j++) {
-            const uint64_t r = r0 + j;
+            const uint64_t r = r0 + (uint64_t)j * 32;
             cnts[j] = 0;
             lanes[j] = 0;
             if (r < R) {
@@ -607,40 +655,49 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
                 bases[j] = a.run_base[r];
             }
         }
+        Seg wagg{0, 0, 0};
 #pragma unroll
         for (int j = 0; j < IPT; j++) {
-            const uint64_t r = r0 + j;
-            if (r >= R) continue;
-            nodes[j] = __ldg(a.numa + lanes[j]);
-            lens[j] = __ldg(a.seg_len + lanes[j]);
-            const bool head = r == (lf_smem ? s_lf[lanes[j]] : __ldcg(a.lane_first + lanes[j]));
-            if (head) heads |= 1u << j;
-            agg = SegOp()(agg, Seg{cnts[j], head ? 1u : 0u, 0});
+            const uint64_t r = r0 + (uint64_t)j * 32;
+            if (r < R) {
+                nodes[j] = __ldg(a.numa + lanes[j]);
+                lens[j] = __ldg(a.seg_len + lanes[j]);
+                const bool head = r == (lf_smem ? s_lf[lanes[j]] : __ldcg(a.lane_first + lanes[j]));
+                if (head) heads |= 1u << j;
+            }
+            const Seg incl = warp_scan_seg(Seg{cnts[j], heads >> j & 1u, 0});
+            wagg = SegOp()(wagg, shfl_seg(incl, 31, false, 0));
         }
-        Seg ex, tot;
-        block_scan(agg, SegOp(), Seg{0, 0, 0}, sm.seg, &ex, &tot);
-        uint64_t blk = SegOp()(carry, ex).sum;  // blocks before this thread's first run
+        __syncthreads();  // reduce_prefix's scan has read sm.seg
+        if (lane == 0) sm.seg[w] = wagg;
+        __syncthreads();
+        Seg run = carry;  // every run before this warp's j-th group of 32
+        for (uint32_t i = 0; i < w; i++) run = SegOp()(run, sm.seg[i]);
 #pragma unroll
         for (int j = 0; j < IPT; j++) {
-            const uint64_t r = r0 + j;
+            const uint64_t r = r0 + (uint64_t)j * 32;
+            const Seg incl = warp_scan_seg(Seg{cnts[j], heads >> j & 1u, 0});
+            Seg ex = shfl_up_words(incl, 1);
+            if (lane == 0) ex = Seg{0, 0, 0};
+            const Seg before = SegOp()(run, ex);
+            run = SegOp()(run, shfl_seg(incl, 31, false, 0));
             if (r >= R) continue;
-            if (heads >> j & 1u) blk = 0;
+            const uint64_t blk = (heads >> j & 1u) ? 0 : before.sum;  // blocks of the lane before this run
             const uint32_t l = lanes[j];
             a.run_block[r] = (uint32_t)blk;
             a.run_bl[r] = blk | (uint64_t)lens[j] << 32;
-            blk += cnts[j];
             const uint32_t next_first = lf_smem ? s_lf[l + 1] : __ldcg(a.lane_first + l + 1);
-            if (r + 1 == (uint64_t)next_first && blk != a.B) bits |= KVX_S_COVERAGE;
+            if (r + 1 == (uint64_t)next_first && blk + cnts[j] != a.B) bits |= KVX_S_COVERAGE;
             a.items0[r] = SortItem{bases[j], nodes[j], (uint32_t)r | (lens[j] == 0 ? kEmptyBit : 0u)};
         }
         if (nact) {
-            // histogram of the first active digit; one shared atomic per distinct
-            // digit in each warp round
+            // histogram of the first active digit; one shared atomic per run of
+            // equal digits in consecutive lanes
 #pragma unroll
             for (int j = 0; j < IPT; j++) {
-                const uint64_t r = r0 + j;
+                const uint64_t r = r0 + (uint64_t)j * 32;
                 const uint32_t d = r < R ? digit_of(bases[j], nodes[j], lens[j] == 0 ? 1u : 0u, dig0) : ~0u;
-                add_key_runs(s_hist, d, threadIdx.x & 31);
+                add_key_runs(s_hist, d, lane);
             }
             __syncthreads();
             for (uint32_t d = threadIdx.x; d < kDigits; d += blockDim.x) {
