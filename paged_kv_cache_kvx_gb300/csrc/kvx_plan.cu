@@ -44,6 +44,16 @@ constexpr int kT = 256;
 // per-tile workspace.
 constexpr int kIPT = 8;
 constexpr uint32_t kTile = kT * kIPT;
+
+// Where a radix pass after the first gets its histograms.  2048-run tiles:
+// from a phase of their own before the pass (each block counts its own tiles
+// in shared memory, a grid barrier, then the pass), where the previous pass's
+// scatter would pay two global atomics per run (tile and tile-group rows).
+// Smaller tiles (tables of a few dozen): from those atomics during the
+// previous pass's scatter, which cost less there than the extra barrier.
+template <int IPT>
+constexpr bool kLocalHist = IPT == kIPT;
+
 constexpr uint64_t kSmallTiles = 256;
 constexpr uint32_t kDigits = 256;
 // Radix histograms are also kept summed over groups of this many tiles, so a
@@ -708,12 +718,12 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
         }
         __syncthreads();
     }
-    if (nact > 1) {  // pass 0 accumulates the next digit's histograms here
-        const uint64_t n = (uint64_t)kDigits * nt;
+    if (nact > 1) {  // pass 1's histograms sum into hist[1] (small tiles) and ghist[1]
         const uint64_t ng = (uint64_t)kDigits * ceil_div((uint64_t)nt, (uint64_t)kHistGroup);
+        const uint64_t n = kLocalHist<IPT> ? ng : (uint64_t)kDigits * nt;
         for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
              i += (uint64_t)P * blockDim.x) {
-            a.hist[1][i] = 0;
+            if (!kLocalHist<IPT>) a.hist[1][i] = 0;
             if (i < ng) a.ghist[1][i] = 0;
         }
     }
@@ -740,23 +750,23 @@ struct SortCounters {
 };
 constexpr int kSweep = 32;         // histogram rows loaded at once in the offset sweep
 
+
 template <int IPT>
 __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P,
-                                const SortItem *in, SortItem *out, const uint32_t *H,
-                                uint32_t *Hn, uint32_t *Hz, const uint32_t *G, uint32_t *Gn,
-                                uint32_t *Gz, uint32_t dig, bool has_next, uint32_t ndig,
-                                bool clear_z, SortCounters &sc) {
+                                const SortItem *in, SortItem *out, const uint32_t *H, uint32_t *Hn,
+                                uint32_t *Hz, const uint32_t *G, uint32_t *Gn, uint32_t *Gz, uint32_t dig,
+                                bool has_next, uint32_t ndig, bool clear_z, SortCounters &sc) {
     uint32_t (*wcnt)[kDigits] = sc.wcnt;
     uint32_t (*s_off)[kDigits] = sc.s_off;
     uint32_t *s_base = sc.s_base;
     __shared__ uint64_t sh[33];
     static_assert(kT == kDigits, "one thread per digit");
     const uint32_t ng = (nt + kHistGroup - 1) / kHistGroup;
-    if (clear_z) {
-        const uint64_t n = (uint64_t)kDigits * nt;
+    if (clear_z) {  // the histograms of the pass after next sum into Hz and Gz
+        const uint64_t n = (uint64_t)kDigits * (kLocalHist<IPT> ? ng : nt);
         for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
              i += (uint64_t)P * blockDim.x) {
-            Hz[i] = 0;
+            if (!kLocalHist<IPT>) Hz[i] = 0;
             if (i < (uint64_t)kDigits * ng) Gz[i] = 0;
         }
     }
@@ -848,12 +858,12 @@ __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint
                     const uint64_t dst = (uint64_t)s_base[d[j]] + s_off[slot][d[j]] + wcnt[w][d[j]] + pos[j];
                     if (dst < R) {  // always: the offsets are a permutation of [0, R)
                         out[dst] = it[j];
-                        if (has_next)
+                        if (!kLocalHist<IPT> && has_next)
                             key = (uint32_t)(dst / (kT * IPT)) * kDigits +
                                   digit_of(it[j].base, it[j].node, it[j].r >> 31, ndig);
                     }
                 }
-                if (has_next) {  // per tile, and per group of kHistGroup tiles
+                if (!kLocalHist<IPT> && has_next) {  // per tile, and per group of kHistGroup tiles
                     add_key_runs(Hn, key, lane);
                     add_key_runs(Gn, key == ~0u ? ~0u : (key / kDigits / kHistGroup) * kDigits + key % kDigits,
                                  lane);
@@ -861,6 +871,40 @@ __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint
             }
             __syncthreads();
         }
+    }
+}
+
+// The histograms of a radix pass after the first, from the previous pass's
+// output: each block counts its own tiles' digits in shared memory (one
+// atomic per run of equal digits in consecutive lanes), writes the tile rows
+// of H and adds them into the group rows of G (cleared two phases earlier).
+// A grid barrier follows, then the pass.  Out of line: inlined, it made the
+// whole kernel spill.
+template <int IPT>
+__device__ __noinline__ void phase_hist(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P,
+                                        const SortItem *in, uint32_t *H, uint32_t *G, uint32_t dig,
+                                        uint32_t *s_hist) {
+    const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
+        for (uint32_t d = threadIdx.x; d < kDigits; d += blockDim.x) s_hist[d] = 0;
+        __syncthreads();
+        const uint64_t t0 = (uint64_t)tile * (kT * IPT) + (uint64_t)w * (32 * IPT) + lane;
+        SortItem it[IPT];
+#pragma unroll
+        for (int j = 0; j < IPT; j++)
+            if (t0 + (uint64_t)j * 32 < R) it[j] = ld_cg(in + t0 + (uint64_t)j * 32);
+#pragma unroll
+        for (int j = 0; j < IPT; j++) {
+            const bool in_range = t0 + (uint64_t)j * 32 < R;
+            add_key_runs(s_hist, in_range ? digit_of(it[j].base, it[j].node, it[j].r >> 31, dig) : ~0u, lane);
+        }
+        __syncthreads();
+        for (uint32_t d = threadIdx.x; d < kDigits; d += blockDim.x) {
+            const uint32_t c = s_hist[d];
+            H[(uint64_t)tile * kDigits + d] = c;
+            if (c) atomicAdd(&G[(uint64_t)(tile / kHistGroup) * kDigits + d], c);
+        }
+        __syncthreads();
     }
 }
 
@@ -2069,6 +2113,10 @@ __device__ void plan_tiles(const PlanArgs &a, uint64_t R_in, uint64_t R, ScanSme
     for (uint32_t k = 0; k < nact; k++) {
         const SortItem *in = (k & 1) ? a.items1 : a.items0;
         SortItem *out = (k & 1) ? a.items0 : a.items1;
+        if (kLocalHist<IPT> && k > 0) {  // pass 0's histograms came with the keys
+            phase_hist<IPT>(a, R, nt, P, in, a.hist[k % 3], a.ghist[k % 3], s_act[k], st.keys.hist);
+            PLAN_BARRIER();
+        }
         const bool has_next = k + 1 < nact;
         phase_sort_pass<IPT>(a, R, nt, P, in, out, a.hist[k % 3], a.hist[(k + 1) % 3],
                              a.hist[(k + 2) % 3], a.ghist[k % 3], a.ghist[(k + 1) % 3],
