@@ -112,6 +112,33 @@ __device__ __forceinline__ uint64_t ld_addr(const uint64_t *addr, uint64_t b, ui
     return __ldg(addr + b * L + l);
 }
 
+// Position of the j-th set bit (from 0) of m; m has more than j set bits.
+__device__ __forceinline__ uint32_t nth_bit(uint64_t m, uint32_t j) {
+    uint32_t x = (uint32_t)m, pos = 0;
+    const uint32_t c = __popc(x);
+    if (j >= c) {
+        x = (uint32_t)(m >> 32);
+        j -= c;
+        pos = 32;
+    }
+#pragma unroll
+    for (uint32_t s = 16; s > 0; s >>= 1) {
+        const uint32_t below = __popc(x & ((1u << s) - 1u));
+        if (j >= below) {
+            x >>= s;
+            j -= below;
+            pos += s;
+        }
+    }
+    return pos;
+}
+
+__device__ __forceinline__ uint64_t shfl_u64(uint64_t v, uint32_t src) {
+    const uint32_t lo = __shfl_sync(0xFFFFFFFFu, (uint32_t)v, src);
+    const uint32_t hi = __shfl_sync(0xFFFFFFFFu, (uint32_t)(v >> 32), src);
+    return (uint64_t)hi << 32 | lo;
+}
+
 // Slice [b0, b1) of lane l under both entry states; m0 / m1 get a bit per
 // block of the slice (bit i - b0) where a run starts under entry state 0 /
 // 1 (slices are at most 64 blocks).
@@ -494,7 +521,59 @@ __global__ void __launch_bounds__(kThreads, 6) k_encode(const __grid_constant__ 
             }
         }
         __syncthreads();
-        if (active) {
+        if (one_tile) {
+            // Runs in table order: warp w writes those of lanes 4w .. 4w+3 of the
+            // tile, 32 consecutive runs at a time, so that its stores are
+            // contiguous.  Its 32 (lane, slice) pairs are its lanes' slices,
+            // one per thread; a run's pair is found by a search over the
+            // pairs' run offsets, its block from the pair's start mask.
+            static_assert(kRows * 4 == 32, "four lanes of eight slices per warp");
+            const uint32_t tt = w * 4 + (t >> 3), r = t & 7;  // this thread's pair
+            const uint64_t rb0 = (uint64_t)tr * kRows * g.K + (uint64_t)r * g.K;
+            const bool act = l0 + tt < L && rb0 < Bv;
+            const Prefix pr = sp[r][tt];
+            const uint64_t m = act ? (pr.state ? sm1[r][tt] : sm0[r][tt]) : 0;
+            const uint32_t c = (uint32_t)__popcll(m);
+            uint32_t incl = c;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                if ((int)t >= d) incl += o;
+            }
+            const uint32_t off = incl - c;  // the warp's runs before this pair's
+            const uint32_t T = __shfl_sync(0xFFFFFFFFu, incl, 31);
+            for (uint32_t q0 = 0; q0 < T; q0 += 32) {
+                const uint32_t q = q0 + t;
+                uint32_t v = 0;  // the last pair whose runs start at or before run q
+#pragma unroll
+                for (uint32_t s = 16; s > 0; s >>= 1)
+                    if (__shfl_sync(0xFFFFFFFFu, off, v + s) <= q) v += s;
+                const uint32_t j = q - __shfl_sync(0xFFFFFFFFu, off, v);
+                const uint32_t lane_run0 = __shfl_sync(0xFFFFFFFFu, off, v & ~7u);  // offset of its lane's first pair
+                const uint64_t mv = shfl_u64(m, v);
+                if (q < T) {
+                    const uint32_t tv = w * 4 + (v >> 3), rv = v & 7, lv = l0 + tv;
+                    const uint64_t b0v = (uint64_t)tr * kRows * g.K + (uint64_t)rv * g.K;
+                    const uint64_t i = b0v + nth_bit(mv, j);
+                    const uint64_t av = ld_addr(a.addr, i, L, lv);
+                    const uint64_t nx = i + 1 < Bv ? ld_addr(a.addr, i + 1, L, lv) : 0;
+                    const uint64_t idx = s_lb[tv] + sp[0][tv].runs + (q - lane_run0);
+                    if (idx < a.run_cap) {  // always true: runs per lane <= ceil(B/2)
+                        a.run_base[idx] = av;
+                        a.run_stride[idx] = i + 1 < Bv ? (int64_t)(nx - av) : 0;
+                    }
+                    // the run before it in its lane ends here
+                    const uint32_t pv = j ? (uint32_t)(b0v + nth_bit(mv, j - 1)) : sp[rv][tv].prev;
+                    if (pv != kNone && idx - 1 < a.run_cap) a.run_count[idx - 1] = (uint32_t)(i - pv);
+                }
+            }
+            // the lane's last run, in the slice where the table ends
+            if (act && rb0 + g.K >= Bv) {
+                const uint32_t last = c ? (uint32_t)(rb0 + 63 - __clzll((long long)m)) : pr.prev;
+                const uint64_t li = s_lb[tt] + pr.runs + c - 1;
+                if (li < a.run_cap) a.run_count[li] = (uint32_t)(Bv - last);
+            }
+        } else if (active) {
             const Prefix p = sp[w][t];
             const uint64_t lb = s_lb[t];
             uint32_t runs = p.runs;
@@ -511,19 +590,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_encode(const __grid_constant__ 
                 prev = (uint32_t)i;
                 runs++;
             };
-            if (one_tile) {
-                // the starts phase 1 found under this slice's entry state:
-                // only their addresses (and the next ones, for the stride)
-                // are read again
-                uint64_t m = p.state ? sm1[w][t] : sm0[w][t];
-                while (m) {
-                    const uint64_t i = b0 + (uint64_t)(__ffsll((long long)m) - 1);
-                    m &= m - 1;
-                    const uint64_t av = ld_addr(a.addr, i, L, l);
-                    const uint64_t nx = i + 1 < Bv ? ld_addr(a.addr, i + 1, L, l) : 0;
-                    emit(i, av, nx);
-                }
-            } else {
+            {
                 uint64_t p2 = b0 >= 2 ? ld_addr(a.addr, b0 - 2, L, l) : 0;
                 uint64_t p1 = b0 >= 1 ? ld_addr(a.addr, b0 - 1, L, l) : 0;
                 uint64_t av = ld_addr(a.addr, b0, L, l);
