@@ -3,8 +3,8 @@ is integer or byte data).
 
 Small inputs: every output array and every slab / pool byte.  Full sizes of
 the five configurations (and the 64 KiB shape): every run-table, plan and
-rebuild array in full; the payload bytes by sampled segments against the
-seeded generator and by the pack-then-unpack identity over the whole pool.
+rebuild array in full, and every byte of the packed slab and of the unpacked
+pool against the oracle's pack and unpack of the same holder bytes.
 """
 import numpy as np
 import pytest
@@ -128,6 +128,39 @@ def test_tall_tables_block_per_lane_scan(B, L, kind):
     torch.cuda.synchronize()
     assert tr.read_status() == 0
     assert_table_equal(tr, t)
+
+
+@pytest.mark.parametrize("kind", ["bump", "random"])
+def test_encoder_blocks_with_several_tiles(kind):
+    """A table of more tiles than the encoder's grid has blocks: 40,000 x 512
+    is 16 lane tiles x 79 row tiles of 8 slices x 64 blocks, 1264 tiles,
+    against at most six blocks per SM.  Blocks then loop over tiles, and the
+    emit walks each slice again instead of writing from the start masks.
+    Bit-exact against the oracle (relocated bump layout: long runs broken;
+    random: pair runs)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, L = 40000, 512
+    assert 16 * ((B + 511) // 512) > 6 * sms  # more tiles than resident blocks
+    rng = np.random.default_rng(40512 + len(kind))
+    if kind == "random":
+        addr, seg_len, numa, pool = random_lanes(rng, B, L)
+    else:
+        seg = 64
+        pos = np.arange(B, dtype=np.int64)
+        rel = np.sort(rng.choice(B, size=B // 50, replace=False))
+        pos[rel] = B + np.arange(rel.size)
+        addr = (pos[:, None] * (L * seg) + np.arange(L)[None, :] * seg).astype(np.uint64)
+        seg_len, numa = np.full(L, seg, np.uint32), np.zeros(L, np.uint32)
+        pool = int(addr.max()) + seg
+    t = oracle.encode_runs(addr)
+    tr = kvx.Transfer(B, seg_len, numa, pool)
+    tr.set_addr(addr)
+    tr.encode()
+    torch.cuda.synchronize()
+    assert tr.read_status() == 0
+    assert_table_equal(tr, t)
+    del tr
+    torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("B,L", [(0, 4), (1, 2), (1, 7 * 2), (2, 2), (3, 50), (65, 34), (513, 2)])
