@@ -104,6 +104,27 @@ def test_planner_tile_size_boundary(per_sm, extra):
     assert np.array_equal(tr.read_local(), local)
 
 
+def test_planner_more_tiles_than_one_sweep():
+    """2,560,000 pair runs (10,000 x 512 random lanes): 1250 tiles of 2048
+    runs, more than eight per planner block, so every radix pass sweeps its
+    offsets for a block's tiles in two chunks and the histogram phase counts
+    more than eight tiles per block.  Plan and rebuilt pointers equal the
+    oracle's."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, L = 10000, 512
+    assert (L * B // 2 + 2047) // 2048 > 8 * sms
+    addr, seg_len, numa, pool = random_lanes(np.random.default_rng(10512), B, L)
+    t, p, st, local = oracle_all(addr, B, seg_len, numa, pool)
+    assert t.num_runs == L * B // 2 and p.status == 0
+    tr = gpu_plan(addr, B, seg_len, numa, pool)
+    assert tr.read_status() == 0
+    assert_table_equal(tr, t)
+    assert_plan_equal(tr, p)
+    assert np.array_equal(tr.read_local(), local)
+    del tr
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("B,L,kind", [(20011, 6, "random"), (30013, 9, "random"), (40960, 4, "bump"),
                                       (9001, 2, "bump")])
 def test_tall_tables_block_per_lane_scan(B, L, kind):
