@@ -327,8 +327,9 @@ __device__ __forceinline__ void lane_done(const EncodeArgs &a, uint32_t l, uint3
     atomicAdd(reinterpret_cast<unsigned long long *>(a.tile_runs + l / 32), (unsigned long long)runs);
 }
 
-// Six blocks per SM (40 registers): a grid of 912 resident blocks covers the
-// 782 tiles of a 100,000 x 64 table, one tile per block.
+// Six blocks per SM fit (40 registers); the geometry fills at most five per
+// SM with tiles (758 tiles of a 100,000 x 64 table on 152 SMs), so tables
+// up to that height run one tile per block, and taller ones loop.
 __global__ void __launch_bounds__(kThreads, 6) k_encode(const __grid_constant__ EncodeArgs a) {
     __shared__ Xfer sx[kRows][32];     // slice effects; kept from phase 1 to 3 when one_tile
     __shared__ uint64_t sm0[kRows][32], sm1[kRows][32];  // slice run starts (one_tile)
