@@ -418,6 +418,12 @@ k_copy_tma(const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r, uint8_
         if (!s_go && blockIdx.x == 0) atomicOr(status, KVX_S_DESC);
     }
     __syncthreads();
+    // The register-path kernel launched after this one may start as soon as
+    // every block has claimed its place here (users counted) when it has at
+    // most a tile per bulk block to move; with more, beside the bulk copy it
+    // measured slower, so it starts as the bulk blocks exit (still without
+    // the gap between two ordinary launches).
+    if (__ldcg(&ctl->n_vec) <= gridDim.x) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (!s_go) return;
     const uint32_t wid = threadIdx.x >> 5;
     if (wid == 0) tile_ring<PACK>(pool_r, pool_w, slab_r, slab_w, jobs, ctl, status, ring, bars);
@@ -449,7 +455,7 @@ k_copy_vec(const uint8_t *pool_r, uint8_t *pool_w, const uint8_t *slab_r, uint8_
     __shared__ uint64_t s_delta[kThreads];
     __shared__ uint8_t s_ok[kThreads];
     __shared__ uint16_t s_first[kBuckets];  // per 64-byte bucket: the last span starting at or before it
-    if (ctl->bad || ctl->key != key || ctl->users != bulk_blocks) return;
+    if (ctl->bad || ctl->key != key || __ldcg(&ctl->users) != bulk_blocks) return;
     const uint64_t n = *num_descs < desc_cap ? *num_descs : desc_cap;
     const uint64_t used = ctl->used < slab_bytes ? ctl->used : slab_bytes;
     const uint32_t nlist = ctl->n_vec;
@@ -635,15 +641,29 @@ kvx_status launch_copy(bool pack, const CopySetup &cs, const uint8_t *pool_r, ui
         k_copy_tma<false><<<bulk, 32 * kBulkWarps, smem, s>>>(pool_r, pool_w, slab_r, slab_w, w.jobs, w.pieces,
                                                               w.ctl, status, cs.key);
     KVX_LAUNCHED();
+    // The register path starts as soon as every bulk block has begun (a
+    // programmatic dependency), so its tiles move beside the bulk kernel's
+    // instead of after them; the two write disjoint tiles.
     const uint32_t grid = (uint32_t)(sms * kCtasPerSm);
-    if (pack)
-        k_copy_vec<true><<<grid, kThreads, 0, s>>>(pool_r, pool_w, slab_r, slab_w, pool_bytes, slab_bytes,
-                                                   cs.aligned, descs, num_descs, desc_cap, w.tile_desc,
-                                                   w.vec_tiles, w.ctl, cs.key, bulk);
-    else
-        k_copy_vec<false><<<grid, kThreads, 0, s>>>(pool_r, pool_w, slab_r, slab_w, pool_bytes, slab_bytes,
-                                                    cs.aligned, descs, num_descs, desc_cap, w.tile_desc,
-                                                    w.vec_tiles, w.ctl, cs.key, bulk);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const CopyCtl *cctl = w.ctl;
+    const cudaError_t e =
+        pack ? cudaLaunchKernelEx(&cfg, k_copy_vec<true>, pool_r, pool_w, slab_r, slab_w, pool_bytes, slab_bytes,
+                                  cs.aligned, descs, num_descs, desc_cap, (const uint32_t *)w.tile_desc,
+                                  (const uint32_t *)w.vec_tiles, cctl, cs.key, bulk)
+             : cudaLaunchKernelEx(&cfg, k_copy_vec<false>, pool_r, pool_w, slab_r, slab_w, pool_bytes, slab_bytes,
+                                  cs.aligned, descs, num_descs, desc_cap, (const uint32_t *)w.tile_desc,
+                                  (const uint32_t *)w.vec_tiles, cctl, cs.key, bulk);
+    if (e != cudaSuccess) return KVX_ECUDA;
     KVX_LAUNCHED();
     return KVX_OK;
 }
