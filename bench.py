@@ -463,7 +463,8 @@ def measure_path(wl, K, warmup, dev, world, sample_clocks):
 def path_figures(wl, m, K, world, peak, peak_kind):
     """Every figure of one measured workload: the fastest of the three launch
     modes as the value, each stage's mean and median time, pack and unpack
-    against the HBM roofline (2 N bytes over the call's mean time), encode
+    against the HBM roofline (2 N bytes over the call's mean time) and as
+    payload rates (N over the call's mean time), encode and rebuild
     Msegments/s and every stage against its algorithmic bytes."""
     N, S = wl.payload_bytes, wl.segments
     total_ms, launch_mode, launches = m["total_ms"], "stream", m["launches"]
@@ -494,6 +495,9 @@ def path_figures(wl, m, K, world, peak, peak_kind):
         "frac_of_%s_peak" % peak_kind: both / peak,
         "frac_of_nominal_8tbs": both / NOMINAL_HBM_GBS,
         "encode_msegs_per_s": S / (mean[0] / 1e3) / 1e6,
+        "rebuild_msegs_per_s": S / (mean[2] / 1e3) / 1e6,
+        "pack_payload_gbs": N / (mean[3] / 1e3) / 1e9,
+        "unpack_payload_gbs": N / (mean[4] / 1e3) / 1e9,
         "stage_ms_mean": dict(zip(names, map(float, mean))),
         "stage_ms_median": dict(zip(names, map(float, med))),
         "stage_roofline": stage_roofline(med, S, m["nruns"], m["ngroups"], m["ndescs"], wl.lanes, N,

@@ -84,4 +84,7 @@ def test_per_workload_figures_reproduce_from_stage_times():
     assert f["roofline"]["frac"] == pytest.approx(f["pack_gbs"] / 7000.0)
     assert f["frac_of_measured_peak"] == pytest.approx(4 * N / 0.9e-3 / 1e9 / 7000.0)
     assert f["encode_msegs_per_s"] == pytest.approx(wl.segments / 0.01e-3 / 1e6)
+    assert f["rebuild_msegs_per_s"] == pytest.approx(wl.segments / 0.005e-3 / 1e6)
+    assert f["pack_payload_gbs"] == pytest.approx(f["pack_gbs"] / 2)
+    assert f["unpack_payload_gbs"] == pytest.approx(N / 0.4e-3 / 1e9)
     assert f["stage_ms_mean"]["rebuild"] == pytest.approx(0.005)
