@@ -377,6 +377,13 @@ def l2_note(wl) -> str:
             "not the headline)" % (wl.pool_bytes / 2**20, N / 2**20))
 
 
+# Blocks per SM of the planner's grid (kvx_plan_set_sm_share) in each launch
+# mode: two where a pass runs alone on the device (stream-launched steps, one
+# transfer at a time), one where each pass is planned beside the previous
+# pass's copies (the overlapped graph: its grid must be resident beside them).
+PLAN_SHARE = {"stream": 2, "graph": 2, "overlapped": 1}
+
+
 def measure_path(wl, K, warmup, dev, world, sample_clocks):
     """The whole path on one workload: one step checked against the oracle
     first, then K steps launched call by call with an event between calls, K
@@ -384,6 +391,7 @@ def measure_path(wl, K, warmup, dev, world, sample_clocks):
     (overlapped graph).  Returns the buffers and every raw figure."""
     import torch
     from paged_kv_cache_kvx_gb300 import kvx, workloads as W
+    kvx.kvx_plan_set_sm_share(PLAN_SHARE["stream"])
     tr = kvx.Transfer(wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes, device=dev)
     tr.set_addr(wl.addr)
     pool = torch.empty(wl.pool_bytes, dtype=torch.uint8, device=dev)
@@ -441,6 +449,7 @@ def measure_path(wl, K, warmup, dev, world, sample_clocks):
 
     # The same step captured once as a CUDA graph and replayed K times (the
     # path keeps its counts on the device, so one capture replays every step).
+    kvx.kvx_plan_set_sm_share(PLAN_SHARE["graph"])
     graph_ms, graph_launches = measure_graph(tr, wl, pool, slab, dst, K, world, dev)
     if graph_ms is not None:
         graph_ms = max_over_ranks(graph_ms, device=dev)
@@ -449,7 +458,9 @@ def measure_path(wl, K, warmup, dev, world, sample_clocks):
     # pass copies (every pass still does all five calls).
     tr2 = kvx.Transfer(wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes, device=dev)
     tr2.set_addr(wl.addr)
+    kvx.kvx_plan_set_sm_share(PLAN_SHARE["overlapped"])
     over_ms, over_launches = measure_graph_overlapped([tr, tr2], wl, pool, slab, dst, K, world, dev)
+    kvx.kvx_plan_set_sm_share(PLAN_SHARE["stream"])  # e2e and later calls run one transfer at a time
     if over_ms is not None:
         over_ms = max_over_ranks(over_ms, device=dev)
     clocks = sampler.stop() if sampler else None  # sampled over all three timed regions
@@ -485,7 +496,7 @@ def path_figures(wl, m, K, world, peak, peak_kind):
     names = ["encode", "plan", "rebuild", "pack", "unpack"]
     return {
         "value": step_value(N, K, world, total_ms), "ms_per_step": total_ms / K,
-        "launch_mode": launch_mode, "gpu_launches": int(launches),
+        "launch_mode": launch_mode, "gpu_launches": int(launches), "plan_sm_share": dict(PLAN_SHARE),
         "value_stream_launched": stream_value, "value_graph_one_transfer_at_a_time": graph_value,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None,

@@ -282,6 +282,24 @@ kvx_status kvx_plan_groups(const uint32_t *runs_per_lane, uint32_t table_lanes,
                            uint64_t *counts, uint32_t *status,
                            void *ws, size_t ws_bytes, void *stream);
 
+/*
+ * The share of the device kvx_plan_groups may use for its cooperative grid,
+ * in blocks per SM, for the calling thread's current device and every later
+ * call on it (default 1).
+ *   1  one block per SM: the whole grid can be resident beside a running
+ *      kvx_pack / kvx_unpack bulk copy (one planner block fits next to a
+ *      copy block), so a transfer is planned while another one copies.
+ *   2  two blocks per SM, for a device that runs nothing else meanwhile:
+ *      tables of more than one 2048-run tile per SM then give each block
+ *      one tile instead of two (the many_small table plans ~18 % faster);
+ *      smaller tables still work one block per SM (one per distinct SM).
+ *      Beside a bulk copy half the grid would wait for the copy to end.
+ * Any other value: KVX_EINVAL, setting unchanged.  The grid size is fixed
+ * when a call is made (a captured graph keeps the share it was captured
+ * with).
+ */
+kvx_status kvx_plan_set_sm_share(uint32_t blocks_per_sm);
+
 /* ---------------------------------------------------------------- rebuild */
 
 /*

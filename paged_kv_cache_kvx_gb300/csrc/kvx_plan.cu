@@ -31,6 +31,8 @@
 // another block wrote in this kernel bypasses L1.  Tables of up to 2048 runs
 // (every bump-allocated holder of up to 1024 slots) go to k_plan_small, one
 // block with the table in shared memory, and this kernel returns at once.
+#include <atomic>
+
 #include "kvx_common.cuh"
 
 namespace kvx {
@@ -69,6 +71,8 @@ struct PlanCtl {
     unsigned long long or_base, and_base;
     uint32_t or_node, and_node;
     uint32_t or_empty, and_empty;  // some / every run has a zero-size segment
+    uint32_t primaries;            // blocks that came first on their SM (two blocks per SM, small tables)
+    uint32_t sm_rank[256];         // per SM id: planner blocks that have started there
 };
 
 // Sort record; r holds the run index in its low 31 bits and, in the top bit,
@@ -149,6 +153,7 @@ struct PlanArgs {
     uint64_t *counts;
     uint32_t *status;
     uint32_t out16;  // groups and descs start on 16-byte boundaries: records move in 16-byte pieces
+    uint32_t sms;    // the device's SMs
     // workspace
     PlanCtl *ctl;
     uint32_t *run_lane;
@@ -167,6 +172,12 @@ struct PlanArgs {
     uint32_t *ready_g;  // per tile: gagg (and the tile's first group flag) published, 2 = abandoned
     uint32_t *ready_c;  // per tile: cagg published, 2 = abandoned
 };
+
+// The block's index among the planner's working blocks, which every phase
+// takes as vb: blockIdx.x, except that with two blocks per SM a table of at
+// most one tile per SM takes one block per distinct SM (the first to start
+// there, numbered in arrival order).
+__shared__ uint32_t g_vb;
 
 union ScanSmem {
     Seg seg[kT];
@@ -492,7 +503,7 @@ __device__ void phase_init(const PlanArgs &a, uint64_t R) {
 
 // Step 1 per run; lanes; per-tile segmented count sums; key bits.
 template <int IPT>
-__device__ void phase_decode(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, ScanSmem &sm,
+__device__ void phase_decode(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, uint32_t vb, ScanSmem &sm,
                              uint32_t *s_lf) {
     __shared__ uint32_t s_bits;
     __shared__ unsigned long long s_or, s_and;
@@ -512,10 +523,10 @@ __device__ void phase_decode(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
     {   // the keys phase sums its first histogram into ghist[0]; the post-sort
         // phase publishes per-tile totals behind these flags
         const uint64_t n = (uint64_t)kDigits * ceil_div((uint64_t)nt, (uint64_t)kHistGroup);
-        for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+        for (uint64_t i = (uint64_t)vb * blockDim.x + threadIdx.x; i < n;
              i += (uint64_t)P * blockDim.x)
             a.ghist[0][i] = 0;
-        for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nt;
+        for (uint64_t i = (uint64_t)vb * blockDim.x + threadIdx.x; i < nt;
              i += (uint64_t)P * blockDim.x) {
             a.ready_g[i] = 0;
             a.ready_c[i] = 0;
@@ -528,7 +539,7 @@ __device__ void phase_decode(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
     // for its lane (coalesced loads and stores); the tile's segmented count
     // total is folded in run order, warp by warp.
     const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
+    for (uint32_t tile = vb; tile < nt; tile += P) {
         const uint64_t r0 = (uint64_t)tile * (kT * IPT) + (uint64_t)w * (32 * IPT) + lane;
         // all loads of this thread's runs first, then the checks
         uint32_t lanes[IPT], cnts[IPT], lens[IPT], nodes[IPT];
@@ -634,7 +645,7 @@ __device__ uint32_t active_digits(const PlanArgs &a, uint64_t R, uint32_t *act) 
 
 // Step 2: first block of each run, coverage, sort items, first histogram.
 template <int IPT>
-__device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, uint32_t nact,
+__device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, uint32_t vb, uint32_t nact,
                            uint32_t dig0, ScanSmem &sm, const uint32_t *s_lf, uint32_t *s_hist) {
     const bool lf_smem = a.table_lanes + 1 <= kLaneSmem;
     __shared__ uint32_t s_bits;
@@ -647,7 +658,7 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
     // through shared memory (the scans run twice rather than hold IPT
     // prefixes in registers).
     const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
+    for (uint32_t tile = vb; tile < nt; tile += P) {
         for (uint32_t d = threadIdx.x; d < kDigits; d += blockDim.x) s_hist[d] = 0;
         const Seg carry = reduce_prefix(a.seg, tile, SegOp(), Seg{0, 0, 0}, sm.seg);
         const uint64_t r0 = (uint64_t)tile * (kT * IPT) + (uint64_t)w * (32 * IPT) + lane;
@@ -721,7 +732,7 @@ __device__ void phase_keys(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t 
     if (nact > 1) {  // pass 1's histograms sum into hist[1] (small tiles) and ghist[1]
         const uint64_t ng = (uint64_t)kDigits * ceil_div((uint64_t)nt, (uint64_t)kHistGroup);
         const uint64_t n = kLocalHist<IPT> ? ng : (uint64_t)kDigits * nt;
-        for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+        for (uint64_t i = (uint64_t)vb * blockDim.x + threadIdx.x; i < n;
              i += (uint64_t)P * blockDim.x) {
             if (!kLocalHist<IPT>) a.hist[1][i] = 0;
             if (i < ng) a.ghist[1][i] = 0;
@@ -752,7 +763,7 @@ constexpr int kSweep = 32;         // histogram rows loaded at once in the offse
 
 
 template <int IPT>
-__device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P,
+__device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, uint32_t vb,
                                 const SortItem *in, SortItem *out, const uint32_t *H, uint32_t *Hn,
                                 uint32_t *Hz, const uint32_t *G, uint32_t *Gn, uint32_t *Gz, uint32_t dig,
                                 bool has_next, uint32_t ndig, bool clear_z, SortCounters &sc) {
@@ -764,7 +775,7 @@ __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint
     const uint32_t ng = (nt + kHistGroup - 1) / kHistGroup;
     if (clear_z) {  // the histograms of the pass after next sum into Hz and Gz
         const uint64_t n = (uint64_t)kDigits * (kLocalHist<IPT> ? ng : nt);
-        for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+        for (uint64_t i = (uint64_t)vb * blockDim.x + threadIdx.x; i < n;
              i += (uint64_t)P * blockDim.x) {
             if (!kLocalHist<IPT>) Hz[i] = 0;
             if (i < (uint64_t)kDigits * ng) Gz[i] = 0;
@@ -773,7 +784,7 @@ __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint
     const uint32_t d_me = threadIdx.x;
     const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const uint32_t lt_mask = (1u << lane) - 1u;
-    const uint32_t own = nt > blockIdx.x ? (nt - blockIdx.x + P - 1) / P : 0;
+    const uint32_t own = nt > vb ? (nt - vb + P - 1) / P : 0;
     for (uint32_t c0 = 0; c0 < own; c0 += kOwnChunk) {
         const uint32_t nslot = own - c0 < kOwnChunk ? own - c0 : kOwnChunk;
         // the count of digit d_me in the tile groups before each own tile's
@@ -788,7 +799,7 @@ __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint
                 v[u] = g0 + u < ng ? __ldcg(G + (uint64_t)(g0 + u) * kDigits + d_me) : 0;
 #pragma unroll
             for (int u = 0; u < kSweep; u++) {
-                while (next_slot < nslot && (blockIdx.x + (c0 + next_slot) * P) / kHistGroup == g0 + u) {
+                while (next_slot < nslot && (vb + (c0 + next_slot) * P) / kHistGroup == g0 + u) {
                     s_off[next_slot][d_me] = (uint32_t)run;
                     next_slot++;
                 }
@@ -797,7 +808,7 @@ __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint
         }
         // plus the tiles of each own tile's group that come before it
         for (uint32_t slot = 0; slot < nslot; slot++) {
-            const uint32_t tile = blockIdx.x + (c0 + slot) * P;
+            const uint32_t tile = vb + (c0 + slot) * P;
             const uint32_t t0 = tile - tile % kHistGroup;
             uint32_t v[kHistGroup - 1];
 #pragma unroll
@@ -815,7 +826,7 @@ __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint
         }
         __syncthreads();
         for (uint32_t slot = 0; slot < kOwnChunk && c0 + slot < own; slot++) {
-            const uint32_t tile = blockIdx.x + (c0 + slot) * P;
+            const uint32_t tile = vb + (c0 + slot) * P;
             for (uint32_t i = threadIdx.x; i < (kT / 32) * kDigits; i += blockDim.x) (&wcnt[0][0])[i] = 0;
             __syncthreads();
             SortItem it[IPT];
@@ -881,11 +892,11 @@ __device__ void phase_sort_pass(const PlanArgs &a, uint64_t R, uint32_t nt, uint
 // A grid barrier follows, then the pass.  Out of line: inlined, it made the
 // whole kernel spill.
 template <int IPT>
-__device__ __noinline__ void phase_hist(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P,
+__device__ __noinline__ void phase_hist(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, uint32_t vb,
                                         const SortItem *in, uint32_t *H, uint32_t *G, uint32_t dig,
                                         uint32_t *s_hist) {
     const uint32_t lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
+    for (uint32_t tile = vb; tile < nt; tile += P) {
         for (uint32_t d = threadIdx.x; d < kDigits; d += blockDim.x) s_hist[d] = 0;
         __syncthreads();
         const uint64_t t0 = (uint64_t)tile * (kT * IPT) + (uint64_t)w * (32 * IPT) + lane;
@@ -1015,7 +1026,7 @@ __global__ void k_selftest_flag(uint32_t *status) {
 // records, compat flags and per-tile stretch starts every tile writes here
 // are what those phases read.
 template <int IPT, bool kFuse>
-__device__ void phase_post_sort(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P,
+__device__ void phase_post_sort(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, uint32_t vb,
                                 const SortItem *sorted, ScanSmem &sm, uint64_t *s_tbase) {
     __shared__ uint64_t s_open;  // base of the first run of the stretch open at the tile's start
     __shared__ uint32_t s_need;
@@ -1025,7 +1036,7 @@ __device__ void phase_post_sort(const PlanArgs &a, uint64_t R, uint32_t nt, uint
     __shared__ uint32_t s_next;      // the position after the tile starts a group (or is the end)
     __shared__ uint32_t s_bad;
     const uint64_t T = (uint64_t)kT * IPT;
-    for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
+    for (uint32_t tile = vb; tile < nt; tile += P) {
         const uint64_t p0 = (uint64_t)tile * T + (uint64_t)threadIdx.x * IPT;
         Rec prev;
         bool have_prev = false;
@@ -1335,9 +1346,9 @@ __device__ __noinline__ void walk_stretch(const PlanArgs &a, const SortItem *sor
 
 // Step 3: group starts.
 template <int IPT>
-__device__ void phase_cut(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, const SortItem *sorted,
-                          ScanSmem &sm) {
-    for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
+__device__ void phase_cut(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, uint32_t vb,
+                          const SortItem *sorted, ScanSmem &sm) {
+    for (uint32_t tile = vb; tile < nt; tile += P) {
         const int64_t carry = reduce_prefix(a.segmax, tile, MaxOp(), (int64_t)-1, sm.i64);
         const uint64_t p0 = (uint64_t)tile * (kT * IPT) + (uint64_t)threadIdx.x * IPT;
         // every load of this thread's runs first
@@ -1410,8 +1421,8 @@ __device__ void phase_cut(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P
 }
 
 template <int IPT>
-__device__ void phase_count(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, ScanSmem &sm) {
-    for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
+__device__ void phase_count(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, uint32_t vb, ScanSmem &sm) {
+    for (uint32_t tile = vb; tile < nt; tile += P) {
         GAgg g{0, -1};
         const uint64_t p0 = (uint64_t)tile * (kT * IPT) + (uint64_t)threadIdx.x * IPT;
         for (int j = 0; j < IPT; j++) {
@@ -1433,9 +1444,9 @@ __device__ void phase_count(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t
 // round trip per dependency level rather than one per run.  The thread's
 // group count and carve prefix inside the tile are kept for the emit phase.
 template <int IPT>
-__device__ void phase_groups(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, const SortItem *sorted,
-                             ScanSmem &sm) {
-    for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
+__device__ void phase_groups(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, uint32_t vb,
+                             const SortItem *sorted, ScanSmem &sm) {
+    for (uint32_t tile = vb; tile < nt; tile += P) {
         const GAgg carry = reduce_prefix(a.gagg, tile, GOp(), GAgg{0, -1}, sm.g);
         const uint64_t p0 = (uint64_t)tile * (kT * IPT) + (uint64_t)threadIdx.x * IPT;
         uint32_t fl = 0;  // bit j: position p0 + j starts a group (bit IPT: the next one, or R)
@@ -1533,8 +1544,8 @@ __device__ void phase_groups(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_
 // prefix from the groups phase, so each group end costs one load of its
 // record (all of them issued at once).
 template <int IPT>
-__device__ void phase_emit(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, ScanSmem &sm) {
-    for (uint32_t tile = blockIdx.x; tile < nt; tile += P) {
+__device__ void phase_emit(const PlanArgs &a, uint64_t R, uint32_t nt, uint32_t P, uint32_t vb, ScanSmem &sm) {
+    for (uint32_t tile = vb; tile < nt; tile += P) {
         const CAgg carry = reduce_prefix(a.cagg, tile, COp(), CAgg{0, 0}, sm.c);
         const uint64_t p0 = (uint64_t)tile * (kT * IPT) + (uint64_t)threadIdx.x * IPT;
         if (p0 >= R) continue;
@@ -2095,18 +2106,33 @@ __device__ void plan_tiles(const PlanArgs &a, uint64_t R_in, uint64_t R, ScanSme
     uint32_t *s_lf = st.keys.lf;
     const uint32_t nt = (uint32_t)ceil_div(R, kT * IPT);
     const uint32_t P = nt < gridDim.x ? (nt ? nt : 1) : gridDim.x;
-    if (blockIdx.x >= P) return;
+    if (threadIdx.x == 0) {
+        uint32_t vb = blockIdx.x;
+        if (gridDim.x > a.sms && nt <= a.sms) {
+            // two blocks per SM and at most a tile per SM: the first block to
+            // start on each SM works (numbered in arrival order), so no two
+            // working blocks share an SM; every SM runs one, all of them resident
+            uint32_t smid;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+            const uint32_t rank = smid < 256 ? atomicAdd(&a.ctl->sm_rank[smid], 1u) : 1u;
+            vb = rank == 0 ? atomicAdd(&a.ctl->primaries, 1u) : ~0u;
+        }
+        g_vb = vb;
+    }
+    __syncthreads();
+    const uint32_t vb = g_vb;
+    if (vb >= P) return;
 
-    if (blockIdx.x == 0) phase_init(a, R_in);
+    if (vb == 0) phase_init(a, R_in);
     PLAN_BARRIER();
     if (__ldcg(&a.ctl->fail)) return;
 
-    phase_decode<IPT>(a, R, nt, P, sm, s_lf);
+    phase_decode<IPT>(a, R, nt, P, vb, sm, s_lf);
     PLAN_BARRIER();
     if (threadIdx.x == 0) s_nact = active_digits(a, R, s_act);
     __syncthreads();
     const uint32_t nact = s_nact;
-    phase_keys<IPT>(a, R, nt, P, nact, nact ? s_act[0] : 0, sm, s_lf, st.keys.hist);
+    phase_keys<IPT>(a, R, nt, P, vb, nact, nact ? s_act[0] : 0, sm, s_lf, st.keys.hist);
     PLAN_BARRIER();
     if (__ldcg(&a.ctl->st) != 0) return;  // counts stay 0
 
@@ -2114,11 +2140,11 @@ __device__ void plan_tiles(const PlanArgs &a, uint64_t R_in, uint64_t R, ScanSme
         const SortItem *in = (k & 1) ? a.items1 : a.items0;
         SortItem *out = (k & 1) ? a.items0 : a.items1;
         if (kLocalHist<IPT> && k > 0) {  // pass 0's histograms came with the keys
-            phase_hist<IPT>(a, R, nt, P, in, a.hist[k % 3], a.ghist[k % 3], s_act[k], st.keys.hist);
+            phase_hist<IPT>(a, R, nt, P, vb, in, a.hist[k % 3], a.ghist[k % 3], s_act[k], st.keys.hist);
             PLAN_BARRIER();
         }
         const bool has_next = k + 1 < nact;
-        phase_sort_pass<IPT>(a, R, nt, P, in, out, a.hist[k % 3], a.hist[(k + 1) % 3],
+        phase_sort_pass<IPT>(a, R, nt, P, vb, in, out, a.hist[k % 3], a.hist[(k + 1) % 3],
                              a.hist[(k + 2) % 3], a.ghist[k % 3], a.ghist[(k + 1) % 3],
                              a.ghist[(k + 2) % 3], s_act[k], has_next, has_next ? s_act[k + 1] : 0,
                              k + 2 < nact, st.sort);
@@ -2131,42 +2157,42 @@ __device__ void plan_tiles(const PlanArgs &a, uint64_t R_in, uint64_t R, ScanSme
     // one short tile per block) measured faster with those steps as their
     // own phases, after barriers.
     constexpr bool kFuse = IPT == kIPT;
-    phase_post_sort<IPT, kFuse>(a, R, nt, P, sorted, sm, st.tile_base);
+    phase_post_sort<IPT, kFuse>(a, R, nt, P, vb, sorted, sm, st.tile_base);
     PLAN_BARRIER();
     if (__ldcg(&a.ctl->walked)) {
         // Some stretch outgrows its stride: the cut again, phase by phase,
         // with the walks along such stretches in order, then the counts.
-        phase_cut<IPT>(a, R, nt, P, sorted, sm);
+        phase_cut<IPT>(a, R, nt, P, vb, sorted, sm);
         PLAN_BARRIER();
-        phase_count<IPT>(a, R, nt, P, sm);
+        phase_count<IPT>(a, R, nt, P, vb, sm);
         PLAN_BARRIER();
     } else if (kFuse) {
         return;  // every tile was grouped and carved in that phase
     }
     const GAgg gall = reduce_prefix(a.gagg, nt, GOp(), GAgg{0, -1}, sm.g);
     if (gall.n > a.group_cap) {
-        if (blockIdx.x == 0 && threadIdx.x == 0) {
+        if (vb == 0 && threadIdx.x == 0) {
             raise_plan(a, KVX_S_CAPACITY);
             a.counts[0] = a.counts[1] = a.counts[2] = 0;
         }
         return;
     }
-    phase_groups<IPT>(a, R, nt, P, sorted, sm);
+    phase_groups<IPT>(a, R, nt, P, vb, sorted, sm);
     PLAN_BARRIER();
     const CAgg call = reduce_prefix(a.cagg, nt, COp(), CAgg{0, 0}, sm.c);
     if (call.descs > a.desc_cap) {
-        if (blockIdx.x == 0 && threadIdx.x == 0) {
+        if (vb == 0 && threadIdx.x == 0) {
             raise_plan(a, KVX_S_CAPACITY);
             a.counts[0] = a.counts[1] = a.counts[2] = 0;
         }
         return;
     }
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (vb == 0 && threadIdx.x == 0) {
         a.counts[0] = gall.n;
         a.counts[1] = call.descs;
         a.counts[2] = call.bytes;
     }
-    phase_emit<IPT>(a, R, nt, P, sm);
+    phase_emit<IPT>(a, R, nt, P, vb, sm);
 }
 
 // The tile size follows the run count, which only the device knows: the
@@ -2259,13 +2285,22 @@ Ws carve(void *base, uint64_t run_cap, size_t *bytes) {
     return w;
 }
 
-// Blocks of k_plan that can be resident at once (cooperative launch limit),
-// at most one per SM: then the whole grid also fits beside a bulk copy (one
+// Blocks per SM the planner's grid may take, per device (0: the default, 1).
+std::atomic<uint32_t> g_plan_share[64];
+uint32_t plan_share() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    const uint32_t s = g_plan_share[dev].load(std::memory_order_relaxed);
+    return s ? s : 1;
+}
+
+// Blocks of k_plan's grid: the share (blocks per SM) times the SMs.  One per
+// SM, the default, lets the whole grid be resident beside a bulk copy (one
 // planner block fits next to a copy block), so a transfer is planned while
-// another copies.  Tables of more than one 2048-run tile per SM give a block
-// several tiles (many_small: 284 tiles, 2 per block; planned alone 236 -> 269
-// us, but overlapped passes 2.257 -> 2.175 ms).
-int plan_max_blocks() { return sm_count(); }
+// another copies; tables of more than one 2048-run tile per SM then give a
+// block several tiles (many_small: 284 tiles, 2 per block).  Two per SM (the
+// kernel's register budget allows two) serve an otherwise idle device.
+int plan_max_blocks() { return (int)plan_share() * sm_count(); }
 
 }  // namespace
 }  // namespace kvx
@@ -2295,6 +2330,17 @@ extern "C" kvx_status kvx_plan_bounds(uint32_t B, uint32_t L, uint64_t num_runs,
     // every group holds at least one run
     *group_cap = num_runs ? num_runs : runs_max;
     *desc_cap = kvx_desc_capacity(B, L, max_seg_bytes_total);
+    return KVX_OK;
+}
+
+extern "C" kvx_status kvx_plan_set_sm_share(uint32_t blocks_per_sm) {
+    if (blocks_per_sm != 1 && blocks_per_sm != 2) return KVX_EINVAL;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        (void)cudaGetLastError();
+        return KVX_ECUDA;
+    }
+    kvx::g_plan_share[dev].store(blocks_per_sm, std::memory_order_relaxed);
     return KVX_OK;
 }
 
@@ -2354,6 +2400,7 @@ extern "C" kvx_status kvx_plan_groups(const uint32_t *runs_per_lane, uint32_t ta
     a.counts = counts;
     a.status = status;
     a.out16 = ((reinterpret_cast<uintptr_t>(groups) | reinterpret_cast<uintptr_t>(descs)) & 15) == 0;
+    a.sms = (uint32_t)sm_count();
     a.ctl = w.ctl;
     a.run_lane = w.run_lane;
     a.seg = w.seg;

@@ -46,6 +46,7 @@ _SIGS = {
     "kvx_desc_capacity": (_U64, [_U32, _U32, _U64]),
     "kvx_plan_bounds": (ctypes.c_int, [_U32, _U32, _U64, _U64, _P, _P]),
     "kvx_plan_workspace_size": (_SZ, [_U32, _U64, _U64]),
+    "kvx_plan_set_sm_share": (ctypes.c_int, [_U32]),
     "kvx_plan_groups": (ctypes.c_int, [_P, _U32, _P, _P, _P, _P, _U64, _U32, _P, _P, _U32, _U64,
                                        _P, _U64, _P, _U64, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "kvx_rebuild": (ctypes.c_int, [_P, _P, _P, _P, _P, _U64, _P, _U64, _P, _U32, _U32, _P, _U64,
@@ -143,6 +144,13 @@ def kvx_plan_bounds(B: int, L: int, num_runs: int, max_seg_bytes_total: int):
     _check(lib().kvx_plan_bounds(B, L, num_runs, max_seg_bytes_total, ctypes.addressof(g),
                                  ctypes.addressof(d)), "kvx_plan_bounds")
     return int(g.value), int(d.value)
+
+
+def kvx_plan_set_sm_share(blocks_per_sm: int) -> None:
+    """Blocks per SM the planner's grid may take on the current device: 1 (the
+    default; it fits beside a running bulk copy) or 2 (an otherwise idle
+    device)."""
+    _check(lib().kvx_plan_set_sm_share(blocks_per_sm), "kvx_plan_set_sm_share")
 
 
 def kvx_plan_workspace_size(L: int, run_capacity: int, pool_bytes: int) -> int:

@@ -61,6 +61,15 @@ def test_plan_bounds_through_the_c_abi():
     assert L.kvx_plan_bounds(1000, 576, 576, 4096, ctypes.addressof(g), None) == EINVAL
 
 
+def test_plan_sm_share_rejects_other_values():
+    """kvx_plan_set_sm_share takes 1 or 2 blocks per SM; anything else is
+    KVX_EINVAL before the device is looked at."""
+    from paged_kv_cache_kvx_gb300 import kvx
+    L = kvx.lib()
+    for bad in (0, 3, 4, 2**32 - 1):
+        assert L.kvx_plan_set_sm_share(bad) == EINVAL
+
+
 def test_binding_has_no_cpu_fallback():
     """The product path refuses to run without its CUDA library."""
     from paged_kv_cache_kvx_gb300 import kvx

@@ -125,6 +125,33 @@ def test_planner_more_tiles_than_one_sweep():
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("case", ["one_per_sm", "two_per_sm", "sweep_chunks"])
+def test_planner_two_blocks_per_sm(case):
+    """kvx_plan_set_sm_share(2): a table of at most one 2048-run tile per SM is
+    planned by one block per distinct SM (the first to start on each), a
+    larger one by up to two blocks per SM, and the plan equals the oracle's
+    either way (and the one-block-per-SM plan)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    L = 512
+    B = {"one_per_sm": 2 * 2048 * (sms - 10) // L,       # ~sms - 10 tiles
+         "two_per_sm": 2 * 2048 * (2 * sms - 10) // L,   # ~2 sms - 10 tiles
+         "sweep_chunks": 10000}[case]                   # 1250 tiles
+    addr, seg_len, numa, pool = random_lanes(np.random.default_rng(7000 + B), B, L)
+    t, p, st, local = oracle_all(addr, B, seg_len, numa, pool)
+    assert p.status == 0
+    try:
+        kvx.kvx_plan_set_sm_share(2)
+        tr = gpu_plan(addr, B, seg_len, numa, pool)
+    finally:
+        kvx.kvx_plan_set_sm_share(1)
+    assert tr.read_status() == 0
+    assert_table_equal(tr, t)
+    assert_plan_equal(tr, p)
+    assert np.array_equal(tr.read_local(), local)
+    del tr
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("B,L,kind", [(20011, 6, "random"), (30013, 9, "random"), (40960, 4, "bump"),
                                       (9001, 2, "bump")])
 def test_tall_tables_block_per_lane_scan(B, L, kind):
