@@ -292,8 +292,12 @@ kvx_status kvx_plan_groups(const uint32_t *runs_per_lane, uint32_t table_lanes,
  *   2  two blocks per SM, for a device that runs nothing else meanwhile:
  *      tables of more than one 2048-run tile per SM then give each block
  *      one tile instead of two (the many_small table plans ~18 % faster);
- *      smaller tables still work one block per SM (one per distinct SM).
- *      Beside a bulk copy half the grid would wait for the copy to end.
+ *      smaller tables still work one block per SM (the first block to
+ *      start on each distinct SM).  Beside a bulk copy half the grid would
+ *      wait for the copy to end; if other work keeps whole SMs from hosting
+ *      any planner block while fewer such SMs remain than the table has
+ *      tiles, the call ends in KVX_S_TIMEOUT after about a second, like any
+ *      cooperative call whose grid cannot become resident.
  * Any other value: KVX_EINVAL, setting unchanged.  The grid size is fixed
  * when a call is made (a captured graph keeps the share it was captured
  * with).
