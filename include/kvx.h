@@ -284,8 +284,9 @@ kvx_status kvx_plan_groups(const uint32_t *runs_per_lane, uint32_t table_lanes,
 
 /*
  * The share of the device kvx_plan_groups may use for its cooperative grid,
- * in blocks per SM, for the calling thread's current device and every later
- * call on it (default 1).
+ * in blocks per SM (default 1).  One setting per device for the whole
+ * process: set for the calling thread's current device, it applies to every
+ * later call on that device, from any thread.
  *   1  one block per SM: the whole grid can be resident beside a running
  *      kvx_pack / kvx_unpack bulk copy (one planner block fits next to a
  *      copy block), so a transfer is planned while another one copies.
