@@ -2108,13 +2108,15 @@ __device__ void plan_tiles(const PlanArgs &a, uint64_t R_in, uint64_t R, ScanSme
     const uint32_t P = nt < gridDim.x ? (nt ? nt : 1) : gridDim.x;
     if (threadIdx.x == 0) {
         uint32_t vb = blockIdx.x;
-        if (gridDim.x > a.sms && nt <= a.sms) {
+        uint32_t nsmid;  // SM ids are below this
+        asm volatile("mov.u32 %0, %%nsmid;" : "=r"(nsmid));
+        if (gridDim.x > a.sms && nt <= a.sms && nsmid <= 256) {
             // two blocks per SM and at most a tile per SM: the first block to
             // start on each SM works (numbered in arrival order), so no two
             // working blocks share an SM; every SM runs one, all of them resident
             uint32_t smid;
             asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-            const uint32_t rank = smid < 256 ? atomicAdd(&a.ctl->sm_rank[smid], 1u) : 1u;
+            const uint32_t rank = atomicAdd(&a.ctl->sm_rank[smid < 256 ? smid : 255], 1u);
             vb = rank == 0 ? atomicAdd(&a.ctl->primaries, 1u) : ~0u;
         }
         g_vb = vb;
