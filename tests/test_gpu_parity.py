@@ -761,6 +761,28 @@ def _used_positions(wl):
 
 
 @pytest.mark.parametrize("name", ["worst", "many_small", "mixed"])
+def test_full_size_plan_two_blocks_per_sm(name):
+    """The full worst (141 tiles: one block per distinct SM), many_small (284
+    tiles: up to two blocks per SM) and mixed (66 short tiles) tables planned
+    at kvx_plan_set_sm_share(2): run table, plan and rebuilt pointers equal to
+    the oracle's, as at the default share."""
+    wl = W.CONFIGS[name]()
+    t, p, st, local = oracle_all(wl.addr, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
+    assert p.status == 0 and st == 0
+    try:
+        kvx.kvx_plan_set_sm_share(2)
+        tr = gpu_plan(wl.addr, wl.blocks, wl.seg_len, wl.numa, wl.pool_bytes)
+    finally:
+        kvx.kvx_plan_set_sm_share(1)
+    assert tr.read_status() == 0
+    assert_table_equal(tr, t)
+    assert_plan_equal(tr, p)
+    assert np.array_equal(tr.read_local(), local)
+    del tr
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["worst", "many_small", "mixed"])
 def test_full_size_prepared_copies(name):
     """At full size, the two-stage copies (both preparations first, as the
     overlapped passes do) give the same slab and destination bytes as the
