@@ -13,10 +13,11 @@
 //
 // One cooperative kernel, three phases separated by bounded grid barriers:
 //   1. per tile (32 lanes x 8K blocks): the tile's effect on each lane;
-//   2. one warp per lane (one block per lane for tall tables): a
-//      warp-shuffle scan of its tiles' effects gives every tile's entry
-//      prefix and the lane's run count, which is also added atomically to
-//      its 32-lane tile's total;
+//   2. one warp per lane: a warp-shuffle scan of its tiles' effects gives
+//      every tile's entry prefix and the lane's run count, which is also
+//      added atomically to its 32-lane tile's total (for tall tables, one
+//      warp per lane and chunk of 32 row tiles, with one more barrier
+//      between the chunks' own scans and the fold of earlier chunks);
 //   3. per tile: lane offsets (totals of earlier lane tiles plus a warp
 //      scan), then every thread re-walks its slice from its entry prefix
 //      and writes its runs.
