@@ -2,30 +2,38 @@
 // the READ splitting paragraph) as one cooperative kernel whose phases are
 // separated by a bounded grid barrier:
 //
-//   init     step 1, table level: lane count, zero-size slots, empty lanes,
-//            lane_first = prefix of runs_per_lane, arrays in sync, slab size
-//   decode   step 1 per run (zero count, one-block stride, span); the lane of
-//            each run; per-tile sums for the per-lane block prefix; the key
-//            bits that differ (which radix digits are active)
-//   keys     step 2: first block of each run (segmented prefix of counts in
-//            its lane), per-lane coverage, sort items, first radix histogram
-//   sort     step 2: stable LSD radix passes on (node, base) over the active
-//            digits, one barrier each; equal keys keep run order = (lane,
-//            first block) order
-//   adjacent step 3: sorted records; compat(p) = same node, first block,
-//   + cut    count and stride as p-1 and base-adjacent to it; group starts,
-//            with the "grown chunk still fits the stride" cut inside a
-//            compatible stretch; per tile the number of group starts
-//   cut,     only when some stretch outgrows its stride: the cut again with
-//   count    walks along such stretches in order, then the counts again
-//   groups   group records, run_group / run_off, bytes and read pieces
-//   emit     step 4: slab carve (groups back to back) and descriptors (one
-//            per dense group / per block, split at 32 MiB)
+//   init      step 1, table level: lane count, zero-size slots, empty lanes,
+//             lane_first = prefix of runs_per_lane, arrays in sync, slab size
+//   decode    step 1 per run (zero count, one-block stride, span); the lane of
+//             each run; per-tile sums for the per-lane block prefix; the key
+//             bits that differ (which radix digits are active)
+//   keys      step 2: first block of each run (segmented prefix of counts in
+//             its lane), per-lane coverage, sort items, first radix histogram
+//   hist      (2048-run tiles) before every radix pass but the first: the
+//             pass's per-tile histograms, counted in shared memory
+//   sort      step 2: stable LSD radix passes on (node, base) over the active
+//             digits, one barrier each; equal keys keep run order = (lane,
+//             first block) order.  The smaller tile bodies count the next
+//             pass's histograms with atomics as they scatter
+//   post-sort step 3: sorted records; compat(p) = same node, first block,
+//             count and stride as p-1 and base-adjacent to it; group starts,
+//             with the "grown chunk still fits the stride" cut inside a
+//             compatible stretch.  With 2048-run tiles the same phase goes on
+//             to the groups and the carve: each tile publishes its group
+//             count, then its bytes and reads, behind flags, and takes the
+//             earlier tiles' totals by looking back at theirs
+//   cut,      only when some stretch outgrows its stride: the cut again with
+//   count     walks along such stretches in order, then the counts again
+//   groups    (smaller tiles, or after the walks) group records, run_group /
+//             run_off, bytes and read pieces
+//   emit      step 4: slab carve (groups back to back) and descriptors (one
+//             per dense group / per block, split at 32 MiB)
 //
-// Runs are cut into tiles of 2048 (8 per thread of a 256-thread block), or
-// of 1024 when the table has no more 1024-run tiles than the grid has blocks;
-// only as many blocks as there are tiles take part, each owning tiles b,
-// b+P, ...
+// Runs are cut into tiles of 512, 1024 or 2048 (2, 4 or 8 per thread of a
+// 256-thread block): the smallest whose tiles all get a block.  Only as many
+// blocks as there are tiles take part, each owning tiles b, b+P, ...; when the
+// grid has two blocks per SM and there is at most a tile per SM, the first
+// block to start on each SM takes part, so no two working blocks share one.
 // A block gets the carry for its tile by an ordered reduction of the earlier
 // tiles' aggregates, so scans cost no extra barrier.  Every read of data
 // another block wrote in this kernel bypasses L1.  Tables of up to 2048 runs
