@@ -153,12 +153,13 @@ def test_planner_two_blocks_per_sm(case):
 
 
 @pytest.mark.parametrize("B,L,kind", [(20011, 6, "random"), (30013, 9, "random"), (40960, 4, "bump"),
-                                      (9001, 2, "bump")])
+                                      (9001, 2, "bump"), (30011, 40, "random"), (25000, 70, "bump")])
 def test_tall_tables_block_per_lane_scan(B, L, kind):
     """Tables with far more row tiles than lanes: the encoder's lane scan is
     spread over the grid, one warp per lane and chunk of 32 row tiles, each
     chunk folding in the totals of the lane's earlier chunks (pair runs, and
-    long runs broken by relocated blocks)."""
+    long runs broken by relocated blocks).  The last two also have a ragged
+    last lane tile (40 lanes: 32 + 8; 70: 32 + 32 + 6)."""
     rng = np.random.default_rng(B + L)
     if kind == "random":
         addr, seg_len, numa, pool = random_lanes(rng, B, L)

@@ -401,6 +401,21 @@ def test_verify_encode_tile_edges():
         assert check_verify(addr, size, tmpl) == b
 
 
+def test_verify_encode_tall_table():
+    """A table of far more row tiles than lanes (the spread lane scan) with a
+    ragged last lane tile: the template check cuts it in the middle, and the
+    prefix is run-encoded as the oracle encodes it."""
+    rng = np.random.default_rng(30011)
+    B, L = 30011, 40
+    addr = rng.integers(0, 1 << 30, (B, L), dtype=np.uint64)
+    addr[:, ::2] = (np.arange(B, dtype=np.uint64) * np.uint64(8192))[:, None] + np.uint64(64)
+    tmpl = np.full(L, 64, np.uint32)
+    for b in [17777, B - 1]:
+        size = np.tile(tmpl, (B, 1))
+        size[b, 37] = 0
+        assert check_verify(addr, size, tmpl) == b
+
+
 def test_verify_encode_full_size_default():
     wl = W.default()
     B, L = wl.addr.shape
